@@ -1,0 +1,452 @@
+#!/usr/bin/env python3
+"""Benchmark of the recurrent-state decode step on GB300.
+
+One step = one decode token of the serving workload (GDN, B = 256 requests,
+H = 48 heads, d = 128, four independent layer pools, states pre-warmed by 256
+eager updates) through all three storage variants, i.e. every step of the hot
+path: eager FP32 (read / update / write the dense state), deferred FP32 base +
+log (merge interval M = 16), per-window INT8 (window W = 16; appends, and the
+window-end fold + requantization on every 16th token).  The same tokens feed
+the three variants.
+
+Prints one JSON line.  ``value`` = head-steps (B * H * tokens * pools *
+variants) per second over all ranks, inputs resident in HBM; ``e2e`` = the
+same through ``ls_decode_step_host`` with host buffers; ``roofline`` = the
+dominant kernel (the eager step) against the measured HBM copy bandwidth.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "state-update decode steps/sec (B*H*tokens) and achieved HBM GB/s vs GB300 peak"
+UNIT = "head-steps/s"
+WORKLOAD = "gdn_serving_b256_h48_4pools"
+VARIANTS = (("eager", 0), ("deferred", 16), ("int8", 16))
+SWEEP_W = (8, 16, 32, 64, 128)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=512)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--batch", type=int, default=None, help="override B (profiling runs)")
+    ap.add_argument("--only", default=None, help="comma list of variants to run")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip e2e, window sweep and CPU baseline (profiling runs)")
+    ap.add_argument("--ring", type=int, default=64, help="distinct token inputs kept in HBM")
+    return ap.parse_args()
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_sources_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "recurrent_state_quantization_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, heads_per_launch: int):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, scaled
+    to `heads_per_launch`; None when the kernel sources changed since."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    digest = kernel_sources_digest()
+    for line in open(path):
+        m = dict(re.findall(r"(\w+)=(\S+)", line))
+        if m.get("kernel") == kernel and m.get("sources") == digest:
+            return float(m["dram_bytes_per_head"]) * heads_per_launch
+    return None
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def make_pools(w, variant, window, dev):
+    from recurrent_state_quantization_gb300 import StatePool
+    return [StatePool(w.num_slots, w.heads, variant, w.gate, window, device=dev)
+            for _ in range(w.pools)]
+
+
+def prewarm(w, pools_by_variant, slot_idx, masks, dev):
+    """Warm every pool's states with `prewarm_tokens` eager updates (the eager
+    kernel), then copy the warmed states into the other variants' pools."""
+    import torch
+    from recurrent_state_quantization_gb300 import workloads as wl
+    all_slots = torch.arange(w.num_slots, dtype=torch.int32, device=dev)
+    eager = pools_by_variant["eager"]
+    for p, pool in enumerate(eager):
+        for t in range(-w.prewarm_tokens, 0):
+            pool.decode_step(slot_idx, *wl.step_inputs(w, t, pool=p, device=dev, masks=masks))
+        warm = pool.read(all_slots)
+        for name, pools in pools_by_variant.items():
+            if name != "eager":
+                pools[p].load(all_slots, warm)
+        del warm
+    torch.cuda.synchronize()
+
+
+def run_native(args, rank, world, local):
+    import torch
+    import __graft_entry__
+    from recurrent_state_quantization_gb300 import bytemodel as bm
+    from recurrent_state_quantization_gb300 import workloads as wl
+
+    __graft_entry__.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    base = wl.WORKLOAD_BY_NAME[WORKLOAD]
+    w = base if args.batch is None else wl.Workload(**{**base.__dict__, "batch": args.batch,
+                                                        "num_slots": args.batch})
+    only = set(args.only.split(",")) if args.only else None
+    variants = [(n, W) for n, W in VARIANTS if only is None or n in only]
+    heads = w.batch * w.heads
+    slot_idx = wl.slot_index(w, dev)
+    masks = wl.static_masks(w, dev)
+
+    pools = {n: make_pools(w, n, W, dev) for n, W in variants}
+    if "eager" not in pools:
+        pools["eager"] = make_pools(w, "eager", 0, dev)
+    prewarm(w, pools, slot_idx, masks, dev)
+
+    # token inputs resident in HBM: a ring of distinct tokens per pool
+    ring = max(1, min(args.ring, args.steps + args.warmup))
+    inputs = [[wl.step_inputs(w, t, pool=p, device=dev, masks=masks) for t in range(ring)]
+              for p in range(w.pools)]
+    ys = {n: [torch.empty(w.batch, w.heads, w.d_v, device=dev) for _ in range(w.pools)]
+          for n, _ in variants}
+    stream = torch.cuda.current_stream()
+
+    def one_step(t, ev=None):
+        for vi, (n, _) in enumerate(variants):
+            if ev is not None:
+                ev[vi][0].record(stream)
+            for p in range(w.pools):
+                pools[n][p].decode_step(slot_idx, *inputs[p][t % ring], y=ys[n][p])
+            if ev is not None:
+                ev[vi][1].record(stream)
+
+    for t in range(args.warmup):
+        one_step(t)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+
+    clocks = Clocks(local)
+    clocks.start()
+    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+            for _ in variants] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for t in range(args.steps):
+        one_step(args.warmup + t, evs[t])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    elapsed_ms = start.elapsed_time(stop)
+    if world > 1:
+        tt = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+
+    hbm_peak, peak_kind = peaks()
+    per_variant = {}
+    for vi, (n, W) in enumerate(variants):
+        ms = sum(evs[t][vi][0].elapsed_time(evs[t][vi][1]) for t in range(args.steps))
+        hs = heads * w.pools * args.steps
+        bytes_ = bm.variant_bytes(n, w.gate, W) * hs
+        gbs = bytes_ / (ms * 1e-3) / 1e9
+        per_variant[n] = {"window": W or None, "ms_per_token_all_pools": ms / args.steps,
+                          "head_steps_per_s": hs / (ms * 1e-3),
+                          "algorithmic_bytes_per_head_step": bm.variant_bytes(n, w.gate, W),
+                          "achieved_gbs": gbs, "frac_of_" + peak_kind + "_hbm": gbs / hbm_peak}
+    total_hs = heads * w.pools * len(variants) * args.steps * world
+    value = total_hs / (elapsed_ms * 1e-3)
+    launches_per_step = sum(w.pools * (1 if n == "eager" else 2) for n, _ in variants)
+
+    out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+           "data": "synthetic",
+           "config": {"workload": w.name, "gate": "scalar (Gated DeltaNet)", "batch": w.batch,
+                      "heads": w.heads, "d_k": w.d_k, "d_v": w.d_v, "pools": w.pools,
+                      "variants": [f"{n}" + (f" window={W}" if W else "") for n, W in variants],
+                      "prewarm_tokens": w.prewarm_tokens, "distinct_token_inputs": ring,
+                      "l2": "inputs larger than L2: every pool's state is 0.2-0.8 GB and the "
+                            "step streams 4 pools x 3 variants (about 5 GB) per token",
+                      "parallelism": f"{world} independent replica(s), no collective"},
+           "gpu_launches": launches_per_step * args.steps,
+           "variants": per_variant}
+
+    # roofline of the dominant kernel: the eager step (one launch per call)
+    if "eager" in per_variant:
+        e = per_variant["eager"]
+        launch_ms = e["ms_per_token_all_pools"] / w.pools
+        bytes_launch = bm.eager_bytes(w.gate) * heads
+        achieved = bytes_launch / (launch_ms * 1e-3) / 1e9
+        out["roofline"] = {"bound": "hbm", "kernel": "eager_step_kernel", "achieved": achieved,
+                           "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
+                           "frac": achieved / hbm_peak,
+                           "algorithmic_bytes_per_launch": bytes_launch,
+                           "traffic": ncu_traffic("eager_step_kernel", heads)}
+    if clk is not None:
+        out["clocks"] = clk
+
+    if not args.no_extras:
+        out["int8_window_sweep"] = window_sweep(w, slot_idx, masks, inputs, ring, dev, hbm_peak,
+                                                peak_kind, pools["eager"])
+        out["e2e"] = e2e(w, variants, pools, slot_idx, dev)
+        if rank == 0:
+            out["cpu_baseline"] = cpu_baseline(w, variants, budget_s=6.0)
+    return out
+
+
+def window_sweep(w, slot_idx, masks, inputs, ring, dev, peak, peak_kind, eager_pools):
+    """INT8 head-steps/s and achieved algorithmic GB/s for each window W (a
+    whole number of windows, 4 pools, warmed states)."""
+    import torch
+    from recurrent_state_quantization_gb300 import bytemodel as bm
+    all_slots = torch.arange(w.num_slots, dtype=torch.int32, device=dev)
+    res = []
+    stream = torch.cuda.current_stream()
+    heads = w.batch * w.heads
+    for W in SWEEP_W:
+        pools = make_pools(w, "int8", W, dev)
+        for p in range(w.pools):
+            pools[p].load(all_slots, eager_pools[p].read(all_slots))
+        y = torch.empty(w.batch, w.heads, w.d_v, device=dev)
+        tokens = max(2 * W, 64)
+        for t in range(W):  # warm-up: one window
+            for p in range(w.pools):
+                pools[p].decode_step(slot_idx, *inputs[p][t % ring], y=y)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for t in range(tokens):
+            for p in range(w.pools):
+                pools[p].decode_step(slot_idx, *inputs[p][t % ring], y=y)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b)
+        hs = heads * w.pools * tokens
+        gbs = bm.int8_bytes(w.gate, W) * hs / (ms * 1e-3) / 1e9
+        res.append({"window": W, "tokens": tokens, "head_steps_per_s": hs / (ms * 1e-3),
+                    "achieved_gbs": gbs, "frac_of_" + peak_kind + "_hbm": gbs / peak})
+        del pools
+        torch.cuda.empty_cache()
+    return res
+
+
+def e2e(w, variants, pools, slot_idx, dev, tokens=24):
+    """The same step through ls_decode_step_host: inputs copied from pinned host
+    memory and y copied back inside the timed region, every call."""
+    import torch
+    from recurrent_state_quantization_gb300 import workloads as wl
+    host = []
+    for p in range(w.pools):
+        row = []
+        for t in range(4):
+            ins = wl.step_inputs(w, 10_000 + t, pool=p, device=dev)
+            row.append([x.cpu().pin_memory() for x in ins])
+        host.append(row)
+    hslots = slot_idx.cpu().pin_memory()
+    hy = torch.empty(w.batch, w.heads, w.d_v).pin_memory()
+    stream = torch.cuda.current_stream()
+
+    def step(t):
+        for n, _ in variants:
+            for p in range(w.pools):
+                pools[n][p].decode_step_host(hslots, *host[p][t % 4], hy)
+        stream.synchronize()  # the step's result is on the host
+
+    for t in range(2):
+        step(t)
+    t0 = time.perf_counter()
+    for t in range(tokens):
+        step(t)
+    dt = time.perf_counter() - t0
+    heads = w.batch * w.heads
+    calls = len(variants) * w.pools
+    h2d = calls * (4 * w.batch + 4 * heads * (w.d_k * 2 + w.d_v + w.dl + 1))
+    d2h = calls * 4 * heads * w.d_v
+    return {"value": heads * calls * tokens / dt, "unit": UNIT, "tokens": tokens,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "api": "ls_decode_step_host (pinned host buffers, cudaMemcpyAsync inside the "
+                   "library, host synchronizes on y every token)"}
+
+
+def cpu_baseline(w, variants, budget_s=6.0, steps=None):
+    """The double-precision CPU oracle, as it stands, on a bounded sample of the
+    workload: the 48 heads of one slot, token after token, for each variant
+    until `budget_s` seconds (or `steps` tokens) have passed."""
+    import numpy as np
+    import torch
+    import oracle
+    from recurrent_state_quantization_gb300 import workloads as wl
+    oracle.build_oracle()
+    idx = np.arange(w.heads, dtype=np.int64)
+    total_hs, total_s, toks = 0, 0.0, {}
+    for n, W in variants:
+        if n == "eager":
+            o = oracle.EagerOracle(w.heads, w.d_k, w.d_v, w.dl)
+        elif n == "deferred":
+            o = oracle.DeferredOracle(w.heads, w.d_k, w.d_v, w.dl, W)
+        else:
+            o = oracle.WindowInt8Oracle(w.heads, w.d_k, w.d_v, w.dl, W)
+        one = wl.Workload(**{**w.__dict__, "batch": 1, "num_slots": 1})
+        t_spent, t = 0.0, 0
+        while (steps is None and t_spent < budget_s) or (steps is not None and t < steps):
+            q, k, v, lam, beta = wl.step_inputs(one, t, device="cpu")
+            args = (q.reshape(w.heads, -1).numpy(), k.reshape(w.heads, -1).numpy(),
+                    v.reshape(w.heads, -1).numpy(), lam.reshape(w.heads, -1).numpy(),
+                    beta.reshape(-1).numpy())
+            t0 = time.perf_counter()
+            o.step(idx, *args)
+            t_spent += time.perf_counter() - t0
+            t += 1
+        toks[n] = t
+        total_hs += w.heads * t
+        total_s += t_spent
+    return {"value": total_hs / total_s, "unit": UNIT, "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"the {w.heads} heads of one slot of {w.name}, "
+                      + ", ".join(f"{n}: {toks[n]} tokens" for n, _ in variants)
+                      + "; double precision, OpenMP over heads; host time of the oracle calls"}
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step = one token of the
+    48 heads of one slot through the three variants."""
+    import oracle  # noqa: F401
+    from recurrent_state_quantization_gb300 import workloads as wl
+    w = wl.WORKLOAD_BY_NAME[WORKLOAD]
+    variants = list(VARIANTS)
+    cpu_baseline(w, variants, steps=args.warmup)
+    t0 = time.perf_counter()
+    res = cpu_baseline(w, variants, steps=args.steps)
+    wall = time.perf_counter() - t0
+    value = res["value"]
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * (w.heads * len(variants)) / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "heads": w.heads, "d_k": w.d_k,
+                       "d_v": w.d_v, "pools": w.pools,
+                       "variants": ["eager", "deferred window=16", "int8 window=16"],
+                       "sample_per_step": f"{w.heads} heads of one slot x 3 variants"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": res["cores"],
+                             "kind": "oracle", "sample": res["sample"]},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "wall_s": wall}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args)))
+        return 0
+    rank, world, local = dist_setup(args)
+    out = run_native(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(out))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

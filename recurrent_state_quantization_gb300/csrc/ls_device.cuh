@@ -1,0 +1,179 @@
+// ls_device.cuh -- device helpers of libls: bulk asynchronous copies with
+// mbarrier completion (sm_90+ / sm_103a), bounded waits, warp reductions,
+// and the thread <-> tile mapping shared by the decode and commit kernels.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "ls_internal.cuh"
+
+namespace ls {
+
+// ---- mbarrier + cp.async.bulk (1-D TMA) -----------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+// Make the initialised barriers visible to the asynchronous proxy.
+__device__ __forceinline__ void mbar_fence_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// Global -> shared bulk copy completing `bytes` transactions on `bar`.
+// dst, src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Iteration limit of every wait on an mbarrier.  A bulk copy from valid
+// memory completes in microseconds; the limit only keeps a kernel from
+// spinning forever if something went wrong.
+constexpr uint32_t kWaitLimit = 1u << 22;
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+    for (uint32_t it = 0; it < kWaitLimit; ++it)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+// ---- programmatic dependent launch ----------------------------------------
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_primary() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ---- loads / stores --------------------------------------------------------
+
+__device__ __forceinline__ float4 ldg4(const float* p) {
+    return __ldg(reinterpret_cast<const float4*>(p));
+}
+// Streaming load (read once, do not keep in L1).
+__device__ __forceinline__ float4 ld_stream4(const float* p) {
+    float4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+                 : "l"(p));
+    return r;
+}
+__device__ __forceinline__ void st4(float* p, float4 v) {
+    *reinterpret_cast<float4*>(p) = v;
+}
+
+// ---- reductions -------------------------------------------------------------
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+// Sum over the 8 lanes of a lane group (lanes that differ in bits 0..2).
+__device__ __forceinline__ float group8_sum(float x) {
+    x += __shfl_xor_sync(0xffffffffu, x, 1);
+    x += __shfl_xor_sync(0xffffffffu, x, 2);
+    x += __shfl_xor_sync(0xffffffffu, x, 4);
+    return x;
+}
+
+// ---- tile mapping -----------------------------------------------------------
+// A head's base tile is stored column-major, S^T: value column j holds the
+// d_k = 128 key rows contiguously (512 B in FP32, 128 B in INT8).  In the
+// decode and commit kernels each value column is owned by a group of 8 lanes
+// (g = lane & 7 picks the rows, c = lane >> 3 the column inside the warp's
+// 4 columns); round r (0..3) of warp w covers column j = 32 r + 4 w + c.
+// Each lane owns 16 key rows, in 4 runs of 4 consecutive rows:
+//   FP32: rows 32 m + 4 g + (0..3)  -> a quarter warp reads 128 contiguous B
+//   INT8: rows 16 g + 4 m + (0..3)  -> one 16-byte load per lane and column
+template <bool INT8>
+__device__ __forceinline__ int run_row(int g, int m) {
+    return INT8 ? 16 * g + 4 * m : 32 * m + 4 * g;
+}
+__device__ __forceinline__ int round_col(int r, int warp, int c) { return 32 * r + 4 * warp + c; }
+
+// Load the 16 tile values a lane owns in column j from shared memory.
+template <bool INT8>
+__device__ __forceinline__ void load_tile16(const unsigned char* tile, int j, int g, float (&s)[16]) {
+    if constexpr (INT8) {
+        const int4 raw = *reinterpret_cast<const int4*>(tile + j * kD + 16 * g);
+        const int w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                s[4 * m + e] = static_cast<float>(static_cast<int8_t>((w4[m] >> (8 * e)) & 0xff));
+            }
+        }
+    } else {
+        const float* t = reinterpret_cast<const float*>(tile) + j * kD;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const float4 v = *reinterpret_cast<const float4*>(t + 32 * m + 4 * g);
+            s[4 * m + 0] = v.x;
+            s[4 * m + 1] = v.y;
+            s[4 * m + 2] = v.z;
+            s[4 * m + 3] = v.w;
+        }
+    }
+}
+
+// Per-lane copy of a 128-vector at the lane's 16 rows.
+template <bool INT8>
+__device__ __forceinline__ void gather16(const float* vec, int g, float (&x)[16]) {
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const float4 v = *reinterpret_cast<const float4*>(vec + run_row<INT8>(g, m));
+        x[4 * m + 0] = v.x;
+        x[4 * m + 1] = v.y;
+        x[4 * m + 2] = v.z;
+        x[4 * m + 3] = v.w;
+    }
+}
+
+// Symmetric INT8 code of x with scale s (> 0): round half to even, clamp to
+// [-127, 127].  The division is the correctly rounded FP32 one.
+__device__ __forceinline__ int quant_code(float x, float s) {
+    if (!(s > 0.0f)) return 0;
+    int z = __float2int_rn(__fdiv_rn(x, s));
+    z = z > 127 ? 127 : z;
+    z = z < -127 ? -127 : z;
+    return z;
+}
+
+__device__ __forceinline__ void flag_status(int32_t* status, int32_t bit) {
+    atomicOr(status, bit);
+}
+
+}  // namespace ls

@@ -1,0 +1,116 @@
+// ls_fold.cu -- window commit and logical read of libls (sm_103a).
+//
+// Deferred / INT8: one warp per (slot, head) folds the live log into the base
+// (ls_window_commit: "DeltaLog: Deferred Materialization of Recurrent States
+// for Linear Attention Decoding", §3.1 merge without a new token; INT8 window
+// closed early and requantized, "LeapQuant: Efficient Linear Attention with
+// Accurate Recurrent State Quantization", §3.2 eq. 4) or into a caller buffer
+// (ls_pool_read: DeltaLog §3.2 eq. 7, the logical state), with the same
+// row-blocked fold the decode step uses at a window's end (ls_warp.cuh).
+// Eager: the logical state is the dense base; ls_pool_read transposes its
+// S^T tiles back to [d_k][d_v].
+#include <cuda_runtime.h>
+
+#include "ls_device.cuh"
+#include "ls_internal.cuh"
+#include "ls_warp.cuh"
+
+namespace ls {
+
+namespace {
+
+template <bool INT8, bool PER_KEY, int MODE>
+__global__ void __launch_bounds__(kThreads) fold_kernel(const AuxArgs a) {
+    __shared__ __align__(16) float lb_s[kWarps][kD];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const PoolView& pv = a.pv;
+    const int H = pv.H;
+    const int row = blockIdx.x * kWarps + warp;
+    if (row >= a.n * H) return;
+    const int n = row / H, h = row - n * H;
+    const int slot = __ldg(a.slots + n);
+    if (slot < 0 || slot >= pv.P) {
+        if (lane == 0) flag_status(pv.status, kDevSlotRange);
+        return;
+    }
+    const size_t hd = static_cast<size_t>(slot) * H + h;
+    const int L = pv.len[hd];
+    if (L < 0 || L >= pv.W) {
+        if (lane == 0) flag_status(pv.status, kDevBadState);
+        return;
+    }
+    if (MODE == kFoldCommit && L == 0) return;  // already at a boundary
+    float lb = 0.0f;
+    if constexpr (PER_KEY) {
+        *reinterpret_cast<float4*>(&lb_s[warp][4 * lane]) =
+            *reinterpret_cast<const float4*>(pv.lbar + hd * kD + 4 * lane);
+        __syncwarp();
+    } else {
+        lb = pv.lbar[hd];
+    }
+    float* out = nullptr;
+    if constexpr (MODE == kFoldRead) out = a.state_out + (static_cast<size_t>(n) * H + h) * (kD * kD);
+    fold_warp<INT8, PER_KEY, MODE>(pv, hd, L, lb_s[warp], lb, out, lane);
+    if constexpr (MODE == kFoldCommit) {
+        if constexpr (PER_KEY) st4(pv.lbar + hd * kD + 4 * lane, make_float4(0.f, 0.f, 0.f, 0.f));
+        else if (lane == 0) pv.lbar[hd] = 0.0f;
+        if (lane == 0) pv.len[hd] = 0;
+    }
+}
+
+// Eager base S^T [j][i] -> logical out[i][j].
+__global__ void __launch_bounds__(kThreads) eager_read_kernel(const AuxArgs a) {
+    extern __shared__ __align__(16) float tsm[];  // [128][129]
+    const PoolView& pv = a.pv;
+    const int H = pv.H;
+    const int n = blockIdx.x / H, h = blockIdx.x - n * H;
+    const int slot = __ldg(a.slots + n);
+    if (slot < 0 || slot >= pv.P) {
+        if (threadIdx.x == 0) flag_status(pv.status, kDevSlotRange);
+        return;
+    }
+    const size_t hd = static_cast<size_t>(slot) * H + h;
+    const float* base = reinterpret_cast<const float*>(pv.base) + hd * (kD * kD);
+    for (int idx = threadIdx.x; idx < kD * kD; idx += kThreads) {
+        const int j = idx >> 7, i = idx & (kD - 1);
+        tsm[i * (kD + 1) + j] = base[idx];
+    }
+    __syncthreads();
+    float* out = a.state_out + (static_cast<size_t>(n) * H + h) * (kD * kD);
+    for (int idx = threadIdx.x; idx < kD * kD; idx += kThreads) {
+        const int i = idx >> 7, j = idx & (kD - 1);
+        out[idx] = tsm[i * (kD + 1) + j];
+    }
+}
+
+template <bool INT8, bool PER_KEY>
+cudaError_t launch_mode(const AuxArgs& a, bool commit, cudaStream_t s) {
+    const int64_t rows = static_cast<int64_t>(a.n) * a.pv.H;
+    const dim3 grid(static_cast<unsigned>((rows + kWarps - 1) / kWarps));
+    if (commit)
+        fold_kernel<INT8, PER_KEY, kFoldCommit><<<grid, kThreads, 0, s>>>(a);
+    else
+        fold_kernel<INT8, PER_KEY, kFoldRead><<<grid, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fold(const AuxArgs& a, bool int8, bool per_key, bool commit, cudaStream_t s) {
+    if (int8)
+        return per_key ? launch_mode<true, true>(a, commit, s) : launch_mode<true, false>(a, commit, s);
+    return per_key ? launch_mode<false, true>(a, commit, s) : launch_mode<false, false>(a, commit, s);
+}
+
+cudaError_t launch_eager_read(const AuxArgs& a, cudaStream_t s) {
+    const dim3 grid(static_cast<unsigned>(a.n) * static_cast<unsigned>(a.pv.H));
+    eager_read_kernel<<<grid, kThreads, transpose_smem_bytes(), s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t prepare_fold_kernels() {
+    return cudaFuncSetAttribute(eager_read_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(transpose_smem_bytes()));
+}
+
+}  // namespace ls

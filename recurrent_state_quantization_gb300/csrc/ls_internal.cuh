@@ -1,0 +1,96 @@
+// ls_internal.cuh -- private declarations of libls (pool layout, kernel
+// arguments, launchers).  Shared only by the library's own translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace ls {
+
+constexpr int kD = 128;         // d_k = d_v
+constexpr int kThreads = 256;   // threads of every CTA (8 warps)
+constexpr int kWarps = kThreads / 32;
+
+// Device status word bits (mirror LS_DEV_* of ls.h).
+constexpr int32_t kDevSlotRange = 1;
+constexpr int32_t kDevTimeout = 2;
+constexpr int32_t kDevBadState = 4;
+
+// Device pointers into one pool (caller-owned memory).  "hd" below is the
+// state index slot * H + h.
+//
+// Base layouts:
+//   eager FP32        S^T, [P*H][d_v][d_k]: value column j holds the 128 key
+//                     rows contiguously (the eager kernel stages whole tiles
+//                     in shared memory and reduces columns over 8 lanes);
+//   deferred / INT8   S,   [P*H][d_k][d_v]: key row i holds the 128 value
+//                     columns contiguously (one warp owns a head, each lane
+//                     4 value columns; a row is one coalesced warp access and
+//                     a key row's absmax is a warp reduction).
+struct PoolView {
+    int32_t* status;       // [1] LS_DEV_* bits
+    void* base;            // FP32 or INT8 base states (see above)
+    float* scale;          // INT8: [P*H][d_k] per-key-row scales
+    float* lbar;           // log variants: [P*H][dl] cumulative log-decay
+    int32_t* len;          // log variants: [P*H] live log length
+    float* klog;           // [P*H][W][d_k]  key factors k
+    float* ulog;           // [P*H][W][d_v]  value factors u
+    float* lamlog;         // [P*H][W][dl]   cumulative log-decay snapshots
+    int32_t P, H, W, dl;
+};
+
+struct StepArgs {
+    PoolView pv;
+    const int32_t* slot_idx;
+    int32_t batch;
+    const float* q;
+    const float* k;
+    const float* v;
+    const float* lam;
+    const float* beta;
+    float* y;
+};
+
+struct AuxArgs {
+    PoolView pv;
+    const int32_t* slots;  // [n]
+    int32_t n;
+    const float* state_in;  // load: [n][H][d_k][d_v]
+    float* state_out;       // read: [n][H][d_k][d_v]
+    int8_t* codes_out;      // read_int8: [n][H][d_k][d_v]
+    float* scales_out;      // read_int8: [n][H][d_k]
+    int32_t* len_out;       // read_log_meta: [n][H]
+    float* lbar_out;        // read_log_meta: [n][H][dl]
+};
+
+// ---- shared-memory footprints (bytes) -------------------------------------
+constexpr size_t kVecBytes = kD * sizeof(float);
+__host__ __device__ constexpr size_t tile_bytes(bool int8) {
+    return int8 ? size_t(kD) * kD : size_t(kD) * kD * 4;
+}
+constexpr size_t kMiscBytes = 128;
+constexpr size_t kBarBytes = 64;
+__host__ __device__ constexpr size_t eager_smem_bytes() {
+    return tile_bytes(false) + 6 * kVecBytes + kMiscBytes + kBarBytes;
+}
+__host__ __device__ constexpr size_t transpose_smem_bytes() { return size_t(kD) * (kD + 1) * 4; }
+
+// ---- launchers (each in its own translation unit) -------------------------
+cudaError_t prepare_step_kernels();
+cudaError_t prepare_fold_kernels();
+cudaError_t prepare_aux_kernels();
+
+cudaError_t launch_eager_step(const StepArgs& a, bool per_key, cudaStream_t s);
+cudaError_t launch_log_step(const StepArgs& a, bool int8, bool per_key, cudaStream_t s);
+// deferred / INT8: fold the live log into the base (commit) or into a caller
+// buffer (read) for n slots.
+cudaError_t launch_fold(const AuxArgs& a, bool int8, bool per_key, bool commit, cudaStream_t s);
+cudaError_t launch_eager_read(const AuxArgs& a, cudaStream_t s);
+cudaError_t launch_load(const AuxArgs& a, bool int8, bool has_log, cudaStream_t s);
+cudaError_t launch_reset(const AuxArgs& a, bool int8, bool has_log, cudaStream_t s);
+cudaError_t launch_read_int8(const AuxArgs& a, cudaStream_t s);
+cudaError_t launch_read_log_meta(const AuxArgs& a, cudaStream_t s);
+
+}  // namespace ls

@@ -1,0 +1,210 @@
+"""Python binding of libls: a pool of recurrent states in caller-owned HBM.
+
+Argument marshalling only: every step of the decode path runs in the CUDA
+kernels of ``libls.so``; PyTorch provides the device memory and the stream.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from typing import Optional
+
+import torch
+
+from . import _native as N
+
+VARIANTS = {"eager": N.LS_EAGER_FP32, "deferred": N.LS_DEFERRED_FP32, "int8": N.LS_WINDOW_INT8}
+GATES = {"scalar": N.LS_GATE_SCALAR, "per_key": N.LS_GATE_PER_KEY}
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _need(t: torch.Tensor, name: str, dtype, device, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def required_bytes(num_slots, num_heads, variant="eager", gate="scalar", window=0,
+                   d_k=128, d_v=128) -> int:
+    lib = N.load()
+    d = N.LsDesc(num_slots, num_heads, d_k, d_v, VARIANTS[variant], GATES[gate], window, 0)
+    out = C.c_size_t(0)
+    N.check(lib.ls_pool_required_bytes(C.byref(d), C.byref(out)), "ls_pool_required_bytes")
+    return int(out.value)
+
+
+class StatePool:
+    """``num_slots`` x ``num_heads`` recurrent states of one layer on one GPU.
+
+    variant: "eager" (dense FP32), "deferred" (FP32 base + log, merge interval
+    ``window``) or "int8" (INT8 base with per-key-row scales, window ``window``).
+    gate: "scalar" (Gated DeltaNet) or "per_key" (KDA).
+    """
+
+    def __init__(self, num_slots: int, num_heads: int, variant: str = "eager",
+                 gate: str = "scalar", window: int = 0, d_k: int = 128, d_v: int = 128,
+                 device=None, stream=None):
+        self.lib = N.load()
+        self.variant, self.gate = variant, gate
+        self.P, self.H, self.d_k, self.d_v = int(num_slots), int(num_heads), int(d_k), int(d_v)
+        self.window = int(window)
+        self.dl = 1 if gate == "scalar" else self.d_k
+        dev = torch.device(device) if device is not None else torch.device("cuda")
+        if dev.type != "cuda":
+            raise ValueError("StatePool lives on a CUDA device")
+        if dev.index is None:
+            dev = torch.device("cuda", torch.cuda.current_device())
+        self.device = dev
+        self.desc = N.LsDesc(self.P, self.H, self.d_k, self.d_v, VARIANTS[variant], GATES[gate],
+                             self.window, 0)
+        nbytes = C.c_size_t(0)
+        N.check(self.lib.ls_pool_required_bytes(C.byref(self.desc), C.byref(nbytes)),
+                "ls_pool_required_bytes")
+        self.nbytes = int(nbytes.value)
+        with torch.cuda.device(self.device):
+            self.mem = torch.empty(self.nbytes + 256, dtype=torch.uint8, device=self.device)
+        off = (-self.mem.data_ptr()) % 256
+        self._mem_ptr = self.mem.data_ptr() + off
+        handle = C.c_void_p()
+        with torch.cuda.device(self.device):
+            N.check(self.lib.ls_pool_create(C.byref(self.desc), C.c_void_p(self._mem_ptr),
+                                            self.nbytes, C.c_void_p(_stream(stream)),
+                                            C.byref(handle)), "ls_pool_create")
+        self.handle = handle
+        self._staging = None
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None and h.value:
+            try:
+                self.lib.ls_pool_destroy(h)
+            except Exception:
+                pass
+            self.handle = None
+
+    # ---- helpers ----------------------------------------------------------
+    def _slots(self, slots) -> torch.Tensor:
+        if not isinstance(slots, torch.Tensor):
+            slots = torch.as_tensor(list(slots) if not isinstance(slots, range) else list(slots),
+                                    dtype=torch.int32)
+        if slots.dtype != torch.int32:
+            slots = slots.to(torch.int32)
+        return slots.to(self.device).contiguous()
+
+    # ---- the C ABI calls ---------------------------------------------------
+    def decode_step(self, slot_idx, q, k, v, log_decay, beta, y=None, stream=None):
+        """One token for ``batch`` requests; returns y [batch, H, d_v]."""
+        slot_idx = self._slots(slot_idx)
+        B = int(slot_idx.numel())
+        dev, f32 = self.device, torch.float32
+        _need(q, "q", f32, dev, (B, self.H, self.d_k))
+        _need(k, "k", f32, dev, (B, self.H, self.d_k))
+        _need(v, "v", f32, dev, (B, self.H, self.d_v))
+        _need(log_decay, "log_decay", f32, dev,
+              (B, self.H) if self.dl == 1 else (B, self.H, self.d_k))
+        _need(beta, "beta", f32, dev, (B, self.H))
+        if y is None:
+            y = torch.empty(B, self.H, self.d_v, dtype=f32, device=dev)
+        _need(y, "y", f32, dev, (B, self.H, self.d_v))
+        rc = self.lib.ls_decode_step(self.handle, _ptr(slot_idx), B, _ptr(q), _ptr(k), _ptr(v),
+                                     _ptr(log_decay), _ptr(beta), _ptr(y),
+                                     C.c_void_p(_stream(stream)))
+        N.check(rc, "ls_decode_step")
+        return y
+
+    def staging_bytes(self, batch: int) -> int:
+        out = C.c_size_t(0)
+        N.check(self.lib.ls_step_staging_bytes(self.handle, int(batch), C.byref(out)),
+                "ls_step_staging_bytes")
+        return int(out.value)
+
+    def decode_step_host(self, slot_idx, q, k, v, log_decay, beta, y, stream=None):
+        """ls_decode_step_host: host (pinned) inputs and output; the copies run
+        inside the library on ``stream``.  Synchronize before reading y."""
+        B = int(slot_idx.numel())
+        for name, t in (("slot_idx", slot_idx), ("q", q), ("k", k), ("v", v),
+                        ("log_decay", log_decay), ("beta", beta), ("y", y)):
+            if t.device.type != "cpu" or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous host tensor")
+        need = self.staging_bytes(B)
+        if self._staging is None or self._staging.numel() < need + 256:
+            self._staging = torch.empty(need + 256, dtype=torch.uint8, device=self.device)
+        sp = self._staging.data_ptr() + ((-self._staging.data_ptr()) % 256)
+        rc = self.lib.ls_decode_step_host(self.handle, _ptr(slot_idx), B, _ptr(q), _ptr(k),
+                                          _ptr(v), _ptr(log_decay), _ptr(beta), _ptr(y),
+                                          C.c_void_p(sp), need, C.c_void_p(_stream(stream)))
+        N.check(rc, "ls_decode_step_host")
+        return y
+
+    def window_commit(self, slots, stream=None):
+        slots = self._slots(slots)
+        N.check(self.lib.ls_window_commit(self.handle, _ptr(slots), int(slots.numel()),
+                                          C.c_void_p(_stream(stream))), "ls_window_commit")
+
+    def read(self, slots, out=None, stream=None) -> torch.Tensor:
+        """Logical states [n, H, d_k, d_v] (FP32) of ``slots``."""
+        slots = self._slots(slots)
+        n = int(slots.numel())
+        if out is None:
+            out = torch.empty(n, self.H, self.d_k, self.d_v, dtype=torch.float32,
+                              device=self.device)
+        _need(out, "out", torch.float32, self.device, (n, self.H, self.d_k, self.d_v))
+        N.check(self.lib.ls_pool_read(self.handle, _ptr(slots), n, _ptr(out),
+                                      C.c_void_p(_stream(stream))), "ls_pool_read")
+        return out
+
+    def load(self, slots, state: torch.Tensor, stream=None):
+        slots = self._slots(slots)
+        n = int(slots.numel())
+        _need(state, "state", torch.float32, self.device, (n, self.H, self.d_k, self.d_v))
+        N.check(self.lib.ls_pool_load(self.handle, _ptr(slots), n, _ptr(state),
+                                      C.c_void_p(_stream(stream))), "ls_pool_load")
+
+    def reset(self, slots, stream=None):
+        slots = self._slots(slots)
+        N.check(self.lib.ls_pool_reset_slots(self.handle, _ptr(slots), int(slots.numel()),
+                                             C.c_void_p(_stream(stream))), "ls_pool_reset_slots")
+
+    def read_int8(self, slots, stream=None):
+        """(codes [n, H, d_k, d_v] int8, scales [n, H, d_k] float32) of the INT8 base."""
+        slots = self._slots(slots)
+        n = int(slots.numel())
+        codes = torch.empty(n, self.H, self.d_k, self.d_v, dtype=torch.int8, device=self.device)
+        scales = torch.empty(n, self.H, self.d_k, dtype=torch.float32, device=self.device)
+        N.check(self.lib.ls_pool_read_int8(self.handle, _ptr(slots), n, _ptr(codes),
+                                           _ptr(scales), C.c_void_p(_stream(stream))),
+                "ls_pool_read_int8")
+        return codes, scales
+
+    def read_log_meta(self, slots, stream=None):
+        """(live log length [n, H] int32, cumulative log-decay [n, H, dl] float32)."""
+        slots = self._slots(slots)
+        n = int(slots.numel())
+        ln = torch.empty(n, self.H, dtype=torch.int32, device=self.device)
+        lb = torch.empty(n, self.H, self.dl, dtype=torch.float32, device=self.device)
+        N.check(self.lib.ls_pool_read_log_meta(self.handle, _ptr(slots), n, _ptr(ln), _ptr(lb),
+                                               C.c_void_p(_stream(stream))),
+                "ls_pool_read_log_meta")
+        return ln, lb
+
+    def status(self, stream=None) -> int:
+        """Synchronize, return and clear the device status word (LS_DEV_* bits)."""
+        out = C.c_int32(0)
+        N.check(self.lib.ls_pool_status(self.handle, C.c_void_p(_stream(stream)),
+                                        C.byref(out)), "ls_pool_status")
+        return int(out.value)

@@ -1,0 +1,121 @@
+"""Host-side checks of libls that need no GPU: the library loads, exports every
+entry point include/ls.h declares, and validates descriptors and arguments
+before touching CUDA."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    from recurrent_state_quantization_gb300 import _native
+    return _native.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "ls.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ls_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for needed in ("ls_pool_create", "ls_decode_step", "ls_window_commit", "ls_pool_read"):
+        assert needed in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from recurrent_state_quantization_gb300 import _native
+    names = declared_functions()
+    assert sorted(_native.EXPORTS) == names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def _desc(**kw):
+    from recurrent_state_quantization_gb300 import _native as N
+    d = dict(num_slots=4, num_heads=2, d_k=128, d_v=128, variant=N.LS_WINDOW_INT8,
+             gate=N.LS_GATE_SCALAR, window=16, flags=0)
+    d.update(kw)
+    return N.LsDesc(**d)
+
+
+def _bytes(lib, d):
+    out = C.c_size_t(0)
+    rc = lib.ls_pool_required_bytes(C.byref(d), C.byref(out))
+    return rc, out.value
+
+
+def test_required_bytes_layout(lib):
+    from recurrent_state_quantization_gb300 import _native as N
+    P, Hh, W = 4, 2, 16
+    nh = P * Hh
+    al = lambda x: (x + 255) // 256 * 256
+    # eager: header + dense FP32 states
+    rc, b = _bytes(lib, _desc(variant=N.LS_EAGER_FP32, window=0))
+    assert rc == 0 and b == 256 + al(nh * 128 * 128 * 4)
+    # INT8, scalar gate: INT8 base, scales, lbar, len, W entries (K, U, log-decay)
+    rc, b = _bytes(lib, _desc())
+    expect = (256 + al(nh * 128 * 128) + al(nh * 128 * 4) + al(nh * 4)
+              + al(nh * 4) + 2 * al(nh * W * 128 * 4) + al(nh * W * 4))
+    assert rc == 0 and b == expect
+    # deferred, per-key gate
+    rc, b = _bytes(lib, _desc(variant=N.LS_DEFERRED_FP32, gate=N.LS_GATE_PER_KEY))
+    expect = (256 + al(nh * 128 * 128 * 4) + al(nh * 128 * 4) + al(nh * 4)
+              + 3 * al(nh * W * 128 * 4))
+    assert rc == 0 and b == expect
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("d_k", 64, -5), ("d_v", 256, -5), ("window", 0, -5), ("window", 257, -5),
+    ("variant", 3, -1), ("gate", 2, -1), ("num_slots", 0, -1), ("num_heads", -1, -1),
+    ("flags", 1, -1)])
+def test_bad_descriptors(lib, field, value, code):
+    rc, _ = _bytes(lib, _desc(**{field: value}))
+    assert rc == code
+
+
+def test_eager_ignores_window(lib):
+    from recurrent_state_quantization_gb300 import _native as N
+    rc, _ = _bytes(lib, _desc(variant=N.LS_EAGER_FP32, window=0))
+    assert rc == 0
+
+
+def test_null_arguments_are_rejected(lib):
+    from recurrent_state_quantization_gb300 import _native as N
+    assert lib.ls_pool_required_bytes(None, None) == N.LS_ERR_INVALID
+    P = None
+    assert lib.ls_decode_step(P, None, 1, None, None, None, None, None, None, None) == \
+        N.LS_ERR_INVALID
+    assert lib.ls_window_commit(P, None, 0, None) == N.LS_ERR_INVALID
+    assert lib.ls_pool_read(P, None, 0, None, None) == N.LS_ERR_INVALID
+    out = C.c_int32(0)
+    assert lib.ls_pool_status(P, None, C.byref(out)) == N.LS_ERR_INVALID
+    assert lib.ls_pool_destroy(None) == N.LS_OK
+    d = _desc()
+    h = C.c_void_p()
+    assert lib.ls_pool_create(C.byref(d), None, 0, None, C.byref(h)) == N.LS_ERR_INVALID
+
+
+def test_error_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5, -99):
+        s = lib.ls_error_string(code)
+        assert isinstance(s, bytes) and len(s) > 0
+    assert lib.ls_abi_version() == 1
+
+
+def test_product_path_does_not_import_the_oracle():
+    """The package must not reach the CPU oracle (no fallback path)."""
+    pkg = os.path.join(ROOT, "recurrent_state_quantization_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "ls_oracle" not in text, f

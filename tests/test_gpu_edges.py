@@ -1,0 +1,251 @@
+"""Edge cases of the C ABI on the GPU: empty batches, bad slots, alignment,
+slot lifecycle (load / reset / commit / read), per-slot window phases, host
+buffers, the largest window.  Everything is compared with the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+D = 128
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def _mods():
+    import oracle
+    import _harness as H
+    from recurrent_state_quantization_gb300 import StatePool, LsError
+    from recurrent_state_quantization_gb300 import workloads as wl
+    from recurrent_state_quantization_gb300 import _native as N
+    return oracle, H, StatePool, LsError, wl, N
+
+
+def _inputs(w, t, dev, B=None):
+    from recurrent_state_quantization_gb300 import workloads as wl
+    return wl.step_inputs(w, t, device=dev)
+
+
+@pytest.mark.parametrize("variant,window", [("eager", 0), ("deferred", 4), ("int8", 4)])
+def test_empty_batch_is_noop(variant, window):
+    _, _, StatePool, _, _, _ = _mods()
+    pool = StatePool(3, 2, variant, "scalar", window)
+    z = lambda *s: torch.empty(*s, device="cuda")
+    y = pool.decode_step(torch.empty(0, dtype=torch.int32, device="cuda"), z(0, 2, D), z(0, 2, D),
+                         z(0, 2, D), z(0, 2), z(0, 2))
+    assert y.shape == (0, 2, D)
+    assert torch.all(pool.read(range(3)) == 0)
+    pool.window_commit([])
+    pool.reset([])
+    assert pool.status() == 0
+
+
+@pytest.mark.parametrize("variant,window", [("eager", 0), ("deferred", 4), ("int8", 4)])
+def test_out_of_range_slot_is_flagged_and_skipped(variant, window):
+    oracle, H, StatePool, _, wl, N = _mods()
+    w = wl.custom(batch=3, heads=2, num_slots=4, seed=5)
+    pool = StatePool(4, 2, variant, "scalar", window)
+    orc = H.make_oracle(variant, 8, 1, window)
+    slots = torch.tensor([2, 9, 0], dtype=torch.int32, device="cuda")
+    q, k, v, lam, beta = _inputs(w, 0, "cuda")
+    y = pool.decode_step(slots, q, k, v, lam, beta)
+    st = pool.status()
+    assert st & N.LS_DEV_SLOT_RANGE
+    assert torch.all(torch.isnan(y[1]))
+    rows = np.array([0, 1, 4, 5])
+    hq = H.host_inputs((q, k, v, lam, beta), w, rows)
+    yo = orc.step(np.array([4, 5, 0, 1]), *hq)
+    yg = y.reshape(6, D)[torch.as_tensor(rows, device="cuda")].double().cpu().numpy()
+    assert H.relmax(yg, yo) <= 1e-4
+    assert pool.status() == 0  # cleared by the previous read
+
+
+def test_argument_errors():
+    _, _, StatePool, LsError, wl, N = _mods()
+    pool = StatePool(2, 2, "eager", "scalar", 0)
+    w = wl.custom(batch=2, heads=2, num_slots=2, seed=3)
+    q, k, v, lam, beta = _inputs(w, 0, "cuda")
+    slots = torch.tensor([0, 1], dtype=torch.int32, device="cuda")
+    buf = torch.empty(2 * 2 * D + 1, device="cuda")
+    q_bad = buf[1:].view(2, 2, D)  # 4-byte offset: not 16-byte aligned
+    q_bad.copy_(q)
+    with pytest.raises(LsError) as e:
+        pool.decode_step(slots, q_bad, k, v, lam, beta)
+    assert e.value.code == N.LS_ERR_ALIGN
+    w3 = wl.custom(batch=3, heads=2, num_slots=3, seed=3)
+    with pytest.raises(LsError) as e:
+        pool.decode_step(torch.tensor([0, 1, 0], dtype=torch.int32, device="cuda"),
+                         *_inputs(w3, 0, "cuda"))
+    assert e.value.code == N.LS_ERR_SLOT
+    with pytest.raises(LsError) as e:
+        StatePool(2, 2, "int8", "scalar", 0)  # window 0 is not a window
+    assert e.value.code == N.LS_ERR_SIZE
+    with pytest.raises(LsError) as e:
+        StatePool(2, 2, "deferred", "scalar", 257)
+    assert e.value.code == N.LS_ERR_SIZE
+
+
+@pytest.mark.parametrize("gate", ["scalar", "per_key"])
+@pytest.mark.parametrize("variant,window", [("eager", 0), ("deferred", 5), ("int8", 5)])
+def test_beta_zero_no_decay_keeps_state(gate, variant, window):
+    oracle, H, StatePool, _, wl, _ = _mods()
+    w = wl.custom(gate=gate, batch=2, heads=3, num_slots=2, seed=8)
+    pool = StatePool(2, 3, variant, gate, window)
+    S0 = wl.initial_state(w, "cuda")
+    pool.load(range(2), S0)
+    before = pool.read(range(2))
+    for t in range(7):
+        q, k, v, lam, beta = _inputs(w, t, "cuda")
+        y = pool.decode_step(range(2), q, k, v, torch.zeros_like(lam), torch.zeros_like(beta))
+        expect = torch.einsum("bhij,bhi->bhj", before.double(), q.double())
+        assert H.relmax(y.double().cpu().numpy(), expect.cpu().numpy()) <= 1e-5
+    after = pool.read(range(2))
+    if variant == "eager":
+        assert torch.equal(after, before)
+    else:
+        assert H.relmax(after.double().cpu().numpy(), before.double().cpu().numpy()) <= 1e-6
+
+
+@pytest.mark.parametrize("gate", ["scalar", "per_key"])
+@pytest.mark.parametrize("variant", ["eager", "deferred", "int8"])
+def test_load_then_read(gate, variant):
+    oracle, H, StatePool, _, wl, _ = _mods()
+    w = wl.custom(gate=gate, batch=3, heads=2, num_slots=5, seed=9)
+    pool = StatePool(5, 2, variant, gate, 4 if variant != "eager" else 0)
+    S = wl.initial_state(w, "cuda", scale=3.0)[:3].contiguous()
+    S[1, 0, 7, :] = 0.0  # a zero key row
+    slots = torch.tensor([4, 0, 2], dtype=torch.int32, device="cuda")
+    pool.load(slots, S)
+    back = pool.read(slots)
+    if variant != "int8":
+        assert torch.equal(back, S)
+    else:
+        Z, s = pool.read_int8(slots)
+        Zo, so = oracle.quantize_rows(S.double().cpu().numpy())
+        assert np.array_equal(Z.cpu().numpy(), Zo)
+        assert np.array_equal(s.cpu().numpy(), so)
+        deq = oracle.dequantize_rows(Zo, so)
+        assert H.relmax(back.double().cpu().numpy(), deq) <= 1e-7
+    untouched = pool.read([1, 3])
+    assert torch.all(untouched == 0)
+
+
+@pytest.mark.parametrize("gate", ["scalar", "per_key"])
+@pytest.mark.parametrize("variant,window", [("deferred", 8), ("int8", 8)])
+def test_commit_mid_window_and_reset(gate, variant, window):
+    oracle, H, StatePool, _, wl, _ = _mods()
+    w = wl.custom(gate=gate, batch=4, heads=2, num_slots=4, seed=12, lam_scale=0.3)
+    p = H.Pair(w, variant, window)
+    for t in range(5):
+        p.step(t)
+    before = p.pool.read(p.slot_idx).double().cpu().numpy()
+    commit_slots = torch.tensor([1, 3], dtype=torch.int32, device="cuda")
+    p.pool.window_commit(commit_slots)
+    st_idx = np.concatenate([np.arange(2) + 2 * 1, np.arange(2) + 2 * 3])
+    p.orc.commit(st_idx)
+    ln, lb = p.pool.read_log_meta(torch.arange(4, dtype=torch.int32, device="cuda"))
+    assert ln.cpu().tolist() == [[5, 5], [0, 0], [5, 5], [0, 0]]
+    assert torch.all(lb[[1, 3]] == 0)
+    after = p.pool.read(p.slot_idx).double().cpu().numpy()
+    if variant == "deferred":
+        assert H.relmax(after, before) <= 1e-6
+    else:
+        frac, mx = p.code_mismatch()
+        assert mx <= 1 and frac <= 1e-4
+        assert H.rel_l2(after, before) <= 1e-2
+    p.pool.window_commit(commit_slots)  # empty logs: unchanged
+    assert np.array_equal(p.pool.read(p.slot_idx).double().cpu().numpy(), after)
+    for t in range(5, 5 + window):  # windows now end at different tokens per slot
+        p.step(t)
+    check = p.y_rel_l2() if variant == "int8" else p.y_err()
+    assert check <= (2e-3 if variant == "int8" else 1e-4)
+    p.pool.reset(commit_slots)
+    z = p.pool.read(commit_slots)
+    assert torch.all(z == 0)
+    ln, _ = p.pool.read_log_meta(commit_slots)
+    assert torch.all(ln == 0)
+    assert p.pool.status() == 0
+
+
+@pytest.mark.parametrize("gate", ["scalar", "per_key"])
+@pytest.mark.parametrize("variant,window", [("eager", 0), ("deferred", 4), ("int8", 4)])
+def test_changing_batches_keep_per_slot_phase(gate, variant, window):
+    """Different subsets of slots decode at different tokens (continuous
+    batching), so every slot is at its own position in its window."""
+    oracle, H, StatePool, _, wl, _ = _mods()
+    P, Hh = 6, 2
+    w = wl.custom(gate=gate, batch=P, heads=Hh, num_slots=P, seed=21, lam_scale=0.3)
+    pool = StatePool(P, Hh, variant, gate, window)
+    orc = H.make_oracle(variant, P * Hh, w.dl, window)
+    rng = np.random.default_rng(0)
+    worst = 0.0
+    for t in range(23):
+        nb = int(rng.integers(1, P + 1))
+        slots = np.sort(rng.choice(P, nb, replace=False)).astype(np.int32)
+        q, k, v, lam, beta = _inputs(w, t, "cuda")
+        sel = torch.as_tensor(np.arange(nb), device="cuda")
+        ins = [x[:nb].contiguous() for x in (q, k, v, lam, beta)]
+        y = pool.decode_step(torch.as_tensor(slots, device="cuda"), *ins)
+        sub = wl.custom(gate=gate, batch=nb, heads=Hh, num_slots=P, seed=21)
+        rows = np.arange(nb * Hh)
+        yo = orc.step((slots[:, None] * Hh + np.arange(Hh)).reshape(-1),
+                      *H.host_inputs(ins, sub, rows))
+        yg = y.reshape(-1, D).double().cpu().numpy()
+        worst = max(worst, H.rel_l2(yg, yo) if variant == "int8" else H.relmax(yg, yo))
+    assert worst <= (2e-3 if variant == "int8" else 1e-4)
+    S = pool.read(range(P)).reshape(-1, D, D).double().cpu().numpy()
+    So = orc.logical(np.arange(P * Hh))
+    if variant == "int8":
+        assert H.rel_l2(S, So) <= 2e-3
+    else:
+        assert H.relmax(S, So) <= 1e-4
+    if variant != "eager":
+        ln, _ = pool.read_log_meta(range(P))
+        cnt = orc.cnt if variant == "int8" else orc.L
+        assert np.array_equal(ln.cpu().numpy().reshape(-1), cnt)
+
+
+@pytest.mark.parametrize("variant,window", [("eager", 0), ("deferred", 4), ("int8", 4)])
+def test_host_buffer_entry_point(variant, window):
+    _, H, StatePool, _, wl, _ = _mods()
+    w = wl.custom(gate="per_key", batch=3, heads=2, num_slots=3, seed=4)
+    a = StatePool(3, 2, variant, "per_key", window)
+    b = StatePool(3, 2, variant, "per_key", window)
+    slots = torch.tensor([2, 0, 1], dtype=torch.int32)
+    for t in range(6):
+        ins = _inputs(w, t, "cuda")
+        ya = a.decode_step(slots.cuda(), *ins)
+        hs = [x.cpu().pin_memory() for x in ins]
+        yb = torch.empty(3, 2, D).pin_memory()
+        b.decode_step_host(slots.pin_memory(), *hs, yb)
+        torch.cuda.synchronize()
+        assert torch.equal(ya.cpu(), yb)
+    assert torch.equal(a.read(range(3)), b.read(range(3)))
+
+
+@pytest.mark.parametrize("variant", ["deferred", "int8"])
+def test_largest_window(variant):
+    oracle, H, StatePool, _, wl, _ = _mods()
+    w = wl.custom(gate="scalar", batch=2, heads=2, num_slots=2, tokens=260, seed=30,
+                  lam_scale=0.02)
+    p = H.Pair(w, variant, 256)
+    for t in range(w.tokens):
+        if variant == "int8" and t == 256:
+            p.force_boundary()
+        p.step(t)
+        if variant == "int8" and t == 255:
+            frac, mx = p.code_mismatch()
+            assert mx <= 1 and frac <= 1e-4
+    ln, _ = p.pool.read_log_meta(p.slot_idx)
+    assert torch.all(ln == 4)
+    if variant == "int8":
+        assert p.y_rel_l2() <= 2e-3
+    else:
+        assert p.y_err() <= 1e-4 and p.state_err() <= 1e-4
