@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip e2e, window sweep and CPU baseline (profiling runs)")
     ap.add_argument("--ring", type=int, default=64, help="distinct token inputs kept in HBM")
+    ap.add_argument("--pools", type=int, default=None, help="override the pool count (profiling runs)")
     return ap.parse_args()
 
 
@@ -181,8 +182,12 @@ def run_native(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     base = wl.WORKLOAD_BY_NAME[WORKLOAD]
-    w = base if args.batch is None else wl.Workload(**{**base.__dict__, "batch": args.batch,
-                                                        "num_slots": args.batch})
+    over = {}
+    if args.batch is not None:
+        over.update(batch=args.batch, num_slots=args.batch)
+    if args.pools is not None:
+        over.update(pools=args.pools)
+    w = wl.Workload(**{**base.__dict__, **over}) if over else base
     only = set(args.only.split(",")) if args.only else None
     variants = [(n, W) for n, W in VARIANTS if only is None or n in only]
     heads = w.batch * w.heads

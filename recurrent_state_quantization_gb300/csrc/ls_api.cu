@@ -63,7 +63,9 @@ int make_layout(const ls_pool_desc* d, Layout* L) {
     L->ulog = off;
     off = align_up(off + nh * W * kD * 4);
     L->lamlog = off;
-    off = align_up(off + nh * W * dl * 4);
+    // scalar gate: one snapshot per entry, per-state stride padded to a
+    // multiple of 4 floats so every state's snapshots start 16-byte aligned
+    off = align_up(off + nh * (dl == 1 ? (W + 3) / 4 * 4 : W * dl) * 4);
     L->total = off;
     return LS_OK;
 }
@@ -83,6 +85,7 @@ ls::PoolView make_view(const ls_pool_desc& d, const Layout& L, unsigned char* m)
     v.H = d.num_heads;
     v.W = log ? d.window : 0;
     v.dl = d.gate == LS_GATE_PER_KEY ? kD : 1;
+    v.lam_stride = d.gate == LS_GATE_PER_KEY ? v.W * kD : (v.W + 3) / 4 * 4;
     return v;
 }
 

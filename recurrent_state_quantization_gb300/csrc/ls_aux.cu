@@ -58,8 +58,8 @@ __global__ void __launch_bounds__(kThreads) load_eager_kernel(const AuxArgs a) {
     }
 }
 
-// Deferred / INT8: state_in[n][h] -> base [i][j]; INT8 quantizes every key
-// row with its own scale (the rule of a window end).  Warp w takes rows
+// Deferred / INT8: state_in[n][h] -> base; INT8 quantizes every key row with
+// its own scale (the rule of a window end).  Warp w takes the 4-row groups
 // w, w + 8, ...; lane l columns 4l..4l+3.
 template <bool INT8>
 __global__ void __launch_bounds__(kThreads) load_rows_kernel(const AuxArgs a) {
@@ -71,17 +71,25 @@ __global__ void __launch_bounds__(kThreads) load_rows_kernel(const AuxArgs a) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const size_t hd = static_cast<size_t>(slot) * H + h;
     const float* in = a.state_in + (static_cast<size_t>(n) * H + h) * (kD * kD);
-    for (int i = warp; i < kD; i += kWarps) {
-        const float4 v = ldg4(in + i * kD + 4 * lane);
+    for (int i4 = warp; i4 < kD / 4; i4 += kWarps) {
+        float4 v[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) v[m] = ldg4(in + (4 * i4 + m) * kD + 4 * lane);
         if constexpr (!INT8) {
-            st4(reinterpret_cast<float*>(pv.base) + hd * (kD * kD) + i * kD + 4 * lane, v);
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                st4(reinterpret_cast<float*>(pv.base) + hd * (kD * kD) + (4 * i4 + m) * kD + 4 * lane,
+                    v[m]);
         } else {
-            float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-            m = warp_max(m);
-            const float s = __fdiv_rn(m, 127.0f);
-            reinterpret_cast<uint32_t*>(pv.base)[hd * (kD * kD / 4) + i * (kD / 4) + lane] =
-                pack_codes4(v, s);
-            if (lane == 0) pv.scale[hd * kD + i] = s;
+            float sc[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                float mx = fmaxf(fmaxf(fabsf(v[m].x), fabsf(v[m].y)), fmaxf(fabsf(v[m].z), fabsf(v[m].w)));
+                mx = warp_max(mx);
+                sc[m] = __fdiv_rn(mx, 127.0f);
+                if (lane == 0) pv.scale[hd * kD + 4 * i4 + m] = sc[m];
+            }
+            reinterpret_cast<uint4*>(pv.base)[quad_index(hd, i4, lane)] = pack_quad(v, sc);
         }
     }
     clear_log(pv, hd);
@@ -105,19 +113,27 @@ __global__ void __launch_bounds__(kThreads) reset_kernel(const AuxArgs a) {
     clear_log(pv, hd);
 }
 
-// INT8 codes (already [i][j]) and scales of n slots.
+// INT8 codes in the logical layout codes[n][h][i][j] and scales[n][h][i].
 __global__ void __launch_bounds__(kThreads) read_int8_kernel(const AuxArgs a) {
     const PoolView& pv = a.pv;
     const int H = pv.H;
     const int n = blockIdx.x / H, h = blockIdx.x - n * H;
     int slot;
     if (!slot_of(a, n, &slot)) return;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const size_t hd = static_cast<size_t>(slot) * H + h;
     const size_t o = static_cast<size_t>(n) * H + h;
-    const int4* src = reinterpret_cast<const int4*>(reinterpret_cast<const int8_t*>(pv.base) +
-                                                    hd * (kD * kD));
-    int4* dst = reinterpret_cast<int4*>(a.codes_out + o * (kD * kD));
-    for (int idx = threadIdx.x; idx < kD * kD / 16; idx += kThreads) dst[idx] = src[idx];
+    uint32_t* codes = reinterpret_cast<uint32_t*>(a.codes_out + o * (kD * kD));
+    for (int i4 = warp; i4 < kD / 4; i4 += kWarps) {
+        const uint4 w = reinterpret_cast<const uint4*>(pv.base)[quad_index(hd, i4, lane)];
+        // row r of the quad: byte r of each column word
+        const uint32_t lo01 = __byte_perm(w.x, w.y, 0x5140), hi01 = __byte_perm(w.x, w.y, 0x7362);
+        const uint32_t lo23 = __byte_perm(w.z, w.w, 0x5140), hi23 = __byte_perm(w.z, w.w, 0x7362);
+        codes[(4 * i4 + 0) * (kD / 4) + lane] = __byte_perm(lo01, lo23, 0x5410);
+        codes[(4 * i4 + 1) * (kD / 4) + lane] = __byte_perm(lo01, lo23, 0x7632);
+        codes[(4 * i4 + 2) * (kD / 4) + lane] = __byte_perm(hi01, hi23, 0x5410);
+        codes[(4 * i4 + 3) * (kD / 4) + lane] = __byte_perm(hi01, hi23, 0x7632);
+    }
     if (threadIdx.x < kD) a.scales_out[o * kD + threadIdx.x] = pv.scale[hd * kD + threadIdx.x];
 }
 

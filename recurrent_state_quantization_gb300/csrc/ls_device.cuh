@@ -1,6 +1,6 @@
 // ls_device.cuh -- device helpers of libls: bulk asynchronous copies with
 // mbarrier completion (sm_90+ / sm_103a), bounded waits, warp reductions,
-// and the thread <-> tile mapping shared by the decode and commit kernels.
+// the INT8 rounding rule, and the eager kernel's thread <-> tile mapping.
 #pragma once
 
 #include <cstdint>
@@ -20,6 +20,12 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
                  : "memory");
+}
+
+// Invalidate a barrier whose phases are all complete, before its memory is
+// used for anything else.
+__device__ __forceinline__ void mbar_inval(uint64_t* bar) {
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // Make the initialised barriers visible to the asynchronous proxy.
@@ -44,6 +50,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
+// Order this thread's earlier generic-proxy shared-memory accesses before its
+// later asynchronous-proxy ones (a bulk copy refilling a stage just read).
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -65,15 +77,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     for (uint32_t it = 0; it < kWaitLimit; ++it)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
-}
-
-// ---- programmatic dependent launch ----------------------------------------
-
-__device__ __forceinline__ void pdl_launch_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_wait_primary() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ---- loads / stores --------------------------------------------------------
@@ -108,53 +111,34 @@ __device__ __forceinline__ float group8_sum(float x) {
     return x;
 }
 
-// ---- tile mapping -----------------------------------------------------------
-// A head's base tile is stored column-major, S^T: value column j holds the
-// d_k = 128 key rows contiguously (512 B in FP32, 128 B in INT8).  In the
-// decode and commit kernels each value column is owned by a group of 8 lanes
-// (g = lane & 7 picks the rows, c = lane >> 3 the column inside the warp's
-// 4 columns); round r (0..3) of warp w covers column j = 32 r + 4 w + c.
-// Each lane owns 16 key rows, in 4 runs of 4 consecutive rows:
-//   FP32: rows 32 m + 4 g + (0..3)  -> a quarter warp reads 128 contiguous B
-//   INT8: rows 16 g + 4 m + (0..3)  -> one 16-byte load per lane and column
-template <bool INT8>
-__device__ __forceinline__ int run_row(int g, int m) {
-    return INT8 ? 16 * g + 4 * m : 32 * m + 4 * g;
-}
+// ---- eager tile mapping -------------------------------------------------------
+// The eager kernel stages a head's S^T tile (value column j = 128 contiguous
+// key rows, 512 B) in shared memory.  Each value column is owned by a group of
+// 8 lanes (g = lane & 7 picks the rows, c = lane >> 3 the column inside the
+// warp's 4 columns); round r (0..3) of warp w covers column j = 32 r + 4 w + c.
+// Lane g owns the 16 key rows 32 m + 4 g + (0..3), m = 0..3, so a quarter warp
+// reads 128 contiguous bytes of one column.
+__device__ __forceinline__ int run_row(int g, int m) { return 32 * m + 4 * g; }
 __device__ __forceinline__ int round_col(int r, int warp, int c) { return 32 * r + 4 * warp + c; }
 
-// Load the 16 tile values a lane owns in column j from shared memory.
-template <bool INT8>
+// The 16 tile values a lane owns in column j.
 __device__ __forceinline__ void load_tile16(const unsigned char* tile, int j, int g, float (&s)[16]) {
-    if constexpr (INT8) {
-        const int4 raw = *reinterpret_cast<const int4*>(tile + j * kD + 16 * g);
-        const int w4[4] = {raw.x, raw.y, raw.z, raw.w};
+    const float* t = reinterpret_cast<const float*>(tile) + j * kD;
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                s[4 * m + e] = static_cast<float>(static_cast<int8_t>((w4[m] >> (8 * e)) & 0xff));
-            }
-        }
-    } else {
-        const float* t = reinterpret_cast<const float*>(tile) + j * kD;
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const float4 v = *reinterpret_cast<const float4*>(t + 32 * m + 4 * g);
-            s[4 * m + 0] = v.x;
-            s[4 * m + 1] = v.y;
-            s[4 * m + 2] = v.z;
-            s[4 * m + 3] = v.w;
-        }
+    for (int m = 0; m < 4; ++m) {
+        const float4 v = *reinterpret_cast<const float4*>(t + 32 * m + 4 * g);
+        s[4 * m + 0] = v.x;
+        s[4 * m + 1] = v.y;
+        s[4 * m + 2] = v.z;
+        s[4 * m + 3] = v.w;
     }
 }
 
 // Per-lane copy of a 128-vector at the lane's 16 rows.
-template <bool INT8>
 __device__ __forceinline__ void gather16(const float* vec, int g, float (&x)[16]) {
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-        const float4 v = *reinterpret_cast<const float4*>(vec + run_row<INT8>(g, m));
+        const float4 v = *reinterpret_cast<const float4*>(vec + run_row(g, m));
         x[4 * m + 0] = v.x;
         x[4 * m + 1] = v.y;
         x[4 * m + 2] = v.z;

@@ -1,12 +1,12 @@
 // ls_fold.cu -- window commit and logical read of libls (sm_103a).
 //
-// Deferred / INT8: one warp per (slot, head) folds the live log into the base
+// Deferred / INT8: one CTA per (slot, head) folds the live log into the base
 // (ls_window_commit: "DeltaLog: Deferred Materialization of Recurrent States
 // for Linear Attention Decoding", §3.1 merge without a new token; INT8 window
 // closed early and requantized, "LeapQuant: Efficient Linear Attention with
 // Accurate Recurrent State Quantization", §3.2 eq. 4) or into a caller buffer
 // (ls_pool_read: DeltaLog §3.2 eq. 7, the logical state), with the same
-// row-blocked fold the decode step uses at a window's end (ls_warp.cuh).
+// CTA-cooperative fold the decode step uses at a window's end (ls_warp.cuh).
 // Eager: the logical state is the dense base; ls_pool_read transposes its
 // S^T tiles back to [d_k][d_v].
 #include <cuda_runtime.h>
@@ -20,41 +20,44 @@ namespace ls {
 namespace {
 
 template <bool INT8, bool PER_KEY, int MODE>
-__global__ void __launch_bounds__(kThreads) fold_kernel(const AuxArgs a) {
-    __shared__ __align__(16) float lb_s[kWarps][kD];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+__global__ void __launch_bounds__(kThreads, 2) fold_kernel(const AuxArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
     const PoolView& pv = a.pv;
     const int H = pv.H;
-    const int row = blockIdx.x * kWarps + warp;
-    if (row >= a.n * H) return;
-    const int n = row / H, h = row - n * H;
+    const int n = blockIdx.x / H, h = blockIdx.x - n * H;
     const int slot = __ldg(a.slots + n);
     if (slot < 0 || slot >= pv.P) {
-        if (lane == 0) flag_status(pv.status, kDevSlotRange);
+        if (threadIdx.x == 0) flag_status(pv.status, kDevSlotRange);
         return;
     }
     const size_t hd = static_cast<size_t>(slot) * H + h;
     const int L = pv.len[hd];
     if (L < 0 || L >= pv.W) {
-        if (lane == 0) flag_status(pv.status, kDevBadState);
+        if (threadIdx.x == 0) flag_status(pv.status, kDevBadState);
         return;
     }
     if (MODE == kFoldCommit && L == 0) return;  // already at a boundary
-    float lb = 0.0f;
-    if constexpr (PER_KEY) {
-        *reinterpret_cast<float4*>(&lb_s[warp][4 * lane]) =
-            *reinterpret_cast<const float4*>(pv.lbar + hd * kD + 4 * lane);
-        __syncwarp();
-    } else {
-        lb = pv.lbar[hd];
+    const FoldSmem fs = fold_smem(smem, INT8);
+    if (threadIdx.x == 0) {
+        mbar_init(fs.bar, 1);
+        mbar_fence_init();
     }
+    __syncthreads();
+    // per-key gate: lbar is read row by row from global memory (it is reset
+    // only after the fold); scalar gate: one value
+    const float lb = PER_KEY ? 0.0f : pv.lbar[hd];
     float* out = nullptr;
     if constexpr (MODE == kFoldRead) out = a.state_out + (static_cast<size_t>(n) * H + h) * (kD * kD);
-    fold_warp<INT8, PER_KEY, MODE>(pv, hd, L, lb_s[warp], lb, out, lane);
-    if constexpr (MODE == kFoldCommit) {
-        if constexpr (PER_KEY) st4(pv.lbar + hd * kD + 4 * lane, make_float4(0.f, 0.f, 0.f, 0.f));
-        else if (lane == 0) pv.lbar[hd] = 0.0f;
-        if (lane == 0) pv.len[hd] = 0;
+    const bool ok = fold_cta<INT8, PER_KEY, MODE>(pv, hd, L, pv.lbar + hd * (PER_KEY ? kD : 1), lb,
+                                                  out, fs, 0u);
+    if (MODE == kFoldCommit && ok) {
+        __syncthreads();  // every reader of lbar is done
+        if (PER_KEY) {
+            if (threadIdx.x < kD / 4) st4(pv.lbar + hd * kD + 4 * threadIdx.x, make_float4(0.f, 0.f, 0.f, 0.f));
+        } else if (threadIdx.x == 0) {
+            pv.lbar[hd] = 0.0f;
+        }
+        if (threadIdx.x == 0) pv.len[hd] = 0;
     }
 }
 
@@ -85,13 +88,26 @@ __global__ void __launch_bounds__(kThreads) eager_read_kernel(const AuxArgs a) {
 
 template <bool INT8, bool PER_KEY>
 cudaError_t launch_mode(const AuxArgs& a, bool commit, cudaStream_t s) {
-    const int64_t rows = static_cast<int64_t>(a.n) * a.pv.H;
-    const dim3 grid(static_cast<unsigned>((rows + kWarps - 1) / kWarps));
+    const dim3 grid(static_cast<unsigned>(a.n) * static_cast<unsigned>(a.pv.H));
+    const size_t sm = fold_smem_bytes(INT8);
     if (commit)
-        fold_kernel<INT8, PER_KEY, kFoldCommit><<<grid, kThreads, 0, s>>>(a);
+        fold_kernel<INT8, PER_KEY, kFoldCommit><<<grid, kThreads, sm, s>>>(a);
     else
-        fold_kernel<INT8, PER_KEY, kFoldRead><<<grid, kThreads, 0, s>>>(a);
+        fold_kernel<INT8, PER_KEY, kFoldRead><<<grid, kThreads, sm, s>>>(a);
     return cudaGetLastError();
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, size_t bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(bytes));
+}
+
+template <bool INT8, bool PER_KEY>
+cudaError_t prepare_mode() {
+    cudaError_t e = set_smem(fold_kernel<INT8, PER_KEY, kFoldCommit>, fold_smem_bytes(INT8));
+    if (e != cudaSuccess) return e;
+    return set_smem(fold_kernel<INT8, PER_KEY, kFoldRead>, fold_smem_bytes(INT8));
 }
 
 }  // namespace
@@ -109,8 +125,12 @@ cudaError_t launch_eager_read(const AuxArgs& a, cudaStream_t s) {
 }
 
 cudaError_t prepare_fold_kernels() {
-    return cudaFuncSetAttribute(eager_read_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(transpose_smem_bytes()));
+    cudaError_t e;
+    if ((e = prepare_mode<false, false>()) != cudaSuccess) return e;
+    if ((e = prepare_mode<false, true>()) != cudaSuccess) return e;
+    if ((e = prepare_mode<true, false>()) != cudaSuccess) return e;
+    if ((e = prepare_mode<true, true>()) != cudaSuccess) return e;
+    return set_smem(eager_read_kernel, transpose_smem_bytes());
 }
 
 }  // namespace ls

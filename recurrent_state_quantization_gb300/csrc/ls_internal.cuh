@@ -25,10 +25,15 @@ constexpr int32_t kDevBadState = 4;
 //   eager FP32        S^T, [P*H][d_v][d_k]: value column j holds the 128 key
 //                     rows contiguously (the eager kernel stages whole tiles
 //                     in shared memory and reduces columns over 8 lanes);
-//   deferred / INT8   S,   [P*H][d_k][d_v]: key row i holds the 128 value
+//   deferred FP32     S,   [P*H][d_k][d_v]: key row i holds the 128 value
 //                     columns contiguously (one warp owns a head, each lane
-//                     4 value columns; a row is one coalesced warp access and
-//                     a key row's absmax is a warp reduction).
+//                     4 value columns; a row is one 512-byte warp access and
+//                     a key row's absmax is a warp reduction);
+//   INT8              S in 4x4 column quads: byte (i, j) of a head sits at
+//                     ((i/4) * 32 + j/4) * 16 + (j%4) * 4 + i%4, so a 32-bit
+//                     word holds 4 key rows of one value column (one dp4a
+//                     operand) and 32 lanes read 4 whole rows in one 512-byte
+//                     access (lane l: columns 4l..4l+3).
 struct PoolView {
     int32_t* status;       // [1] LS_DEV_* bits
     void* base;            // FP32 or INT8 base states (see above)
@@ -37,8 +42,10 @@ struct PoolView {
     int32_t* len;          // log variants: [P*H] live log length
     float* klog;           // [P*H][W][d_k]  key factors k
     float* ulog;           // [P*H][W][d_v]  value factors u
-    float* lamlog;         // [P*H][W][dl]   cumulative log-decay snapshots
+    float* lamlog;         // [P*H][lam_stride] cumulative log-decay snapshots:
+                           //   per-key gate [W][d_k]; scalar gate [W] padded to 4
     int32_t P, H, W, dl;
+    int32_t lam_stride;    // floats per state in lamlog
 };
 
 struct StepArgs {

@@ -120,15 +120,15 @@ __global__ void __launch_bounds__(kThreads, 3) eager_step_kernel(const StepArgs 
 
     const int g = lane & 7, c = lane >> 3;
     float xk[16], xq[16];
-    gather16<false>(xk_s, g, xk);
-    gather16<false>(xq_s, g, xq);
+    gather16(xk_s, g, xk);
+    gather16(xq_s, g, xq);
 
 #pragma unroll 1
     for (int r = 0; r < 4; ++r) {
         const int j = round_col(r, warp, c);
         if (!wait_quarter(bars, r, a.pv.status)) return;
         float s[16];
-        load_tile16<false>(tile, j, g, s);
+        load_tile16(tile, j, g, s);
         float rr = 0.0f, yy = 0.0f;
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 3) eager_step_kernel(const StepArgs 
         float* dst = gtile + j * kD;
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-            const int i0 = run_row<false>(g, m);
+            const int i0 = run_row(g, m);
             const float4 al4 = *reinterpret_cast<const float4*>(al_s + i0);
             const float4 k4 = *reinterpret_cast<const float4*>(k_s + i0);
             float4 o;
@@ -169,41 +169,101 @@ __global__ void __launch_bounds__(kThreads, 3) eager_step_kernel(const StepArgs 
 //   on the window's last token the W entries are folded into the base right
 //   away by the same warp (DeltaLog eq. 6; LeapQuant eq. 4 + requantization),
 //   after y was formed from the unquantized state.
+//
+// Data movement: every warp streams its head through a private ring of
+// kRing shared-memory stages with 1-D bulk asynchronous copies (TMA,
+// cp.async.bulk), one mbarrier per stage.  Lane 0 issues, all lanes consume,
+// and up to kRing chunks of 4 KiB stay in flight per warp whatever the
+// window length.  The items of a head, in order:
+//   0          token inputs: k, q, v (+ lambda, lbar for the per-key gate,
+//              + key-row scales for INT8)
+//   1 .. NT    base chunks of 4 KiB (32 INT8 rows / 8 FP32 rows)
+//   then       log chunks: K and U of EPC entries (+ their snapshots)
 // The warp is the single writer of its head's log metadata.
 // ---------------------------------------------------------------------------
-template <bool INT8>
-struct RowWord {
-    using T = typename std::conditional<INT8, uint32_t, float4>::type;
-    static __device__ __forceinline__ T load(const void* base, size_t hd, int i, int lane) {
-        if constexpr (INT8) {
-            const uint32_t* p = reinterpret_cast<const uint32_t*>(base) + hd * (kD * kD / 4) +
-                                i * (kD / 4) + lane;
-            uint32_t w;
-            asm volatile("ld.global.nc.L1::no_allocate.b32 %0, [%1];" : "=r"(w) : "l"(p));
-            return w;
-        } else {
-            return ld_stream4(reinterpret_cast<const float*>(base) + hd * (kD * kD) + i * kD +
-                              4 * lane);
-        }
-    }
-    static __device__ __forceinline__ float4 values(T w) {
-        if constexpr (INT8) {
-            return codes4(w);
-        } else {
-            return w;
-        }
-    }
+constexpr int kRing = 3;
+constexpr int kChunk = 4096;
+constexpr int kStage = kChunk + 16;  // a scalar-gate log chunk adds 16 B of snapshots
+
+struct WarpSmem {
+    unsigned char ring[kRing][kStage];
+    union {
+        float4 xkq[kD];    // FP32 base: per key row i (xk_i, xk_i, xq_i, xq_i), xk = e.k, xq = e.q
+        uint4 dig[32][2];  // INT8 base: per 4-row group, base-256 digits of xk ([0]) and xq ([1]):
+                           //   word d = digit d of rows 4g..4g+3 (byte r = row 4g + r)
+    };
+    uint64_t bar[3];
+    uint32_t bar_live;  // bar[] initialised by this warp (lane 0 sets it)
+    uint32_t pad;
 };
+static_assert(sizeof(WarpSmem) % 16 == 0, "per-warp shared block must keep 16-byte alignment");
+static_assert(kWarps * sizeof(WarpSmem) >= fold_smem_bytes(false),
+              "the window-end fold reuses the rings as staging");
+
+constexpr size_t step_smem_bytes() { return kWarps * sizeof(WarpSmem); }
 
 template <bool INT8, bool PER_KEY>
-__global__ void __launch_bounds__(kThreads) log_step_kernel(const StepArgs a) {
-    __shared__ __align__(16) float2 xkq_s[kWarps][kD];  // (e s k, e s q) per key row
-    __shared__ __align__(16) float lp_s[kWarps][kD];    // lp per key row (per-key gate)
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+struct Plan {
+    static constexpr int NT = INT8 ? 4 : 16;           // base chunks
+    static constexpr int EPC = PER_KEY ? 2 : 4;        // log entries per chunk
+    static constexpr int ROWS = INT8 ? 32 : 8;         // key rows per base chunk
+};
+
+// Issue item `it` of head hd into stage it % kRing (lane 0 only).
+template <bool INT8, bool PER_KEY>
+__device__ __forceinline__ void issue_item(WarpSmem& ws, const StepArgs& a, int row, size_t hd,
+                                           int L, int it) {
+    using P = Plan<INT8, PER_KEY>;
+    const PoolView& pv = a.pv;
+    unsigned char* dst = ws.ring[it % kRing];
+    uint64_t* bar = &ws.bar[it % kRing];
+    fence_proxy_async();  // the stage's previous contents were read by the generic proxy
+    if (it == 0) {
+        const size_t ro = static_cast<size_t>(row) * kD;
+        uint32_t bytes = 3 * kVecBytes + (PER_KEY ? 2 * kVecBytes : 0) + (INT8 ? kVecBytes : 0);
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_g2s(dst, a.k + ro, kVecBytes, bar);
+        bulk_g2s(dst + kVecBytes, a.q + ro, kVecBytes, bar);
+        bulk_g2s(dst + 2 * kVecBytes, a.v + ro, kVecBytes, bar);
+        uint32_t off = 3 * kVecBytes;
+        if constexpr (PER_KEY) {
+            bulk_g2s(dst + off, a.lam + ro, kVecBytes, bar);
+            bulk_g2s(dst + off + kVecBytes, pv.lbar + hd * kD, kVecBytes, bar);
+            off += 2 * kVecBytes;
+        }
+        if constexpr (INT8) bulk_g2s(dst + off, pv.scale + hd * kD, kVecBytes, bar);
+    } else if (it <= P::NT) {
+        mbar_arrive_expect_tx(bar, kChunk);
+        bulk_g2s(dst, reinterpret_cast<const unsigned char*>(pv.base) + hd * tile_bytes(INT8) +
+                          static_cast<size_t>(it - 1) * kChunk,
+                 kChunk, bar);
+    } else {
+        const int e0 = (it - 1 - P::NT) * P::EPC;
+        const int n = min(P::EPC, L - e0);
+        const size_t eo = (hd * static_cast<size_t>(pv.W) + e0) * kD;
+        const uint32_t part = static_cast<uint32_t>(n) * kVecBytes;
+        const size_t lb0 = hd * static_cast<size_t>(pv.lam_stride);
+        mbar_arrive_expect_tx(bar, PER_KEY ? 3 * part : 2 * part + 16);
+        bulk_g2s(dst, pv.klog + eo, part, bar);
+        bulk_g2s(dst + P::EPC * kVecBytes, pv.ulog + eo, part, bar);
+        if constexpr (PER_KEY)
+            bulk_g2s(dst + 2 * P::EPC * kVecBytes, pv.lamlog + lb0 + static_cast<size_t>(e0) * kD,
+                     part, bar);
+        else  // 4 snapshots; e0 is a multiple of 4 and the stride is padded to 4
+            bulk_g2s(dst + kChunk, pv.lamlog + lb0 + e0, 16, bar);
+    }
+}
+
+// One warp decodes one (request, head).  Returns the state index hd when this
+// token closed the head's window (its W entries still have to be folded into
+// the base), -1 otherwise; *lp_out receives the scalar-gate log-decay.
+template <bool INT8, bool PER_KEY>
+__device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, int row,
+                                               float* lp_out) {
+    using P = Plan<INT8, PER_KEY>;
+    const int lane = threadIdx.x & 31;
     const PoolView& pv = a.pv;
     const int H = pv.H, W = pv.W;
-    const int row = blockIdx.x * kWarps + warp;
-    if (row >= a.batch * H) return;
     const int b = row / H, h = row - b * H;
     const size_t ro = static_cast<size_t>(row) * kD + 4 * lane;
     const float4 nan4 = make_float4(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000),
@@ -212,116 +272,272 @@ __global__ void __launch_bounds__(kThreads) log_step_kernel(const StepArgs a) {
     if (slot < 0 || slot >= pv.P) {
         if (lane == 0) flag_status(pv.status, kDevSlotRange);
         st4(a.y + ro, nan4);
-        return;
+        return -1;
     }
     const size_t hd = static_cast<size_t>(slot) * H + h;
     const int L = pv.len[hd];
     if (L < 0 || L >= W) {  // the pool memory of this state was overwritten
         if (lane == 0) flag_status(pv.status, kDevBadState);
         st4(a.y + ro, nan4);
-        return;
+        return -1;
     }
-
-    // ---- token inputs; lane l holds key rows / value columns 4l..4l+3 ------
-    const float4 k4 = ldg4(a.k + ro), q4 = ldg4(a.q + ro), v4 = ldg4(a.v + ro);
-    float4 lp4;
-    if constexpr (PER_KEY) {
-        const float4 lam4 = ldg4(a.lam + ro);
-        const float4 lb4 = *reinterpret_cast<const float4*>(pv.lbar + hd * kD + 4 * lane);
-        lp4 = make_float4(lb4.x + lam4.x, lb4.y + lam4.y, lb4.z + lam4.z, lb4.w + lam4.w);
-    } else {
-        const float lp = pv.lbar[hd] + __ldg(a.lam + row);
-        lp4 = make_float4(lp, lp, lp, lp);
+    const int NI = 1 + P::NT + (L + P::EPC - 1) / P::EPC;
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < kRing; ++s) mbar_init(&ws.bar[s], 1);
+        ws.bar_live = 1u;
+        mbar_fence_init();
+        for (int it = 0; it < min(kRing, NI); ++it) issue_item<INT8, PER_KEY>(ws, a, row, hd, L, it);
     }
     const float beta = __ldg(a.beta + row);
-    float4 es4 = make_float4(expf(lp4.x), expf(lp4.y), expf(lp4.z), expf(lp4.w));
-    if constexpr (INT8) {
-        const float4 s4 = *reinterpret_cast<const float4*>(pv.scale + hd * kD + 4 * lane);
-        es4 = make_float4(es4.x * s4.x, es4.y * s4.y, es4.z * s4.z, es4.w * s4.w);
-    }
-    {
-        float4* xs = reinterpret_cast<float4*>(&xkq_s[warp][4 * lane]);
-        xs[0] = make_float4(es4.x * k4.x, es4.x * q4.x, es4.y * k4.y, es4.y * q4.y);
-        xs[1] = make_float4(es4.z * k4.z, es4.z * q4.z, es4.w * k4.w, es4.w * q4.w);
-        if constexpr (PER_KEY) *reinterpret_cast<float4*>(&lp_s[warp][4 * lane]) = lp4;
-    }
-    const float kq = warp_sum(fmaf(k4.x, q4.x, fmaf(k4.y, q4.y, fmaf(k4.z, q4.z, k4.w * q4.w))));
+    float lp_scalar = 0.0f;
+    if constexpr (!PER_KEY) lp_scalar = pv.lbar[hd] + __ldg(a.lam + row);
     __syncwarp();
 
-    // ---- base GEMVs: stream the key rows, lane keeps its 4 columns ----------
+    float4 k4, q4, v4, lp4;
+    float kq = 0.0f;
     float2 r01 = make_float2(0.f, 0.f), r23 = r01, y01 = r01, y23 = r01;
-    constexpr int RB = INT8 ? 32 : 8;  // rows in flight per lane (128 B words / 512 B rows)
-#pragma unroll 1
-    for (int i0 = 0; i0 < kD; i0 += RB) {
-        typename RowWord<INT8>::T z[RB];
+    // INT8: exact integer GEMVs.  xk (and xq) are written in fixed point
+    // against their absmax, x_i ~ X_i * sx 2^-30 with |X_i| <= 2^30, and X_i
+    // as four signed base-256 digits; dp4a multiplies 4 key rows of one value
+    // column by 4 digits at a time into int32 accumulators (|acc| < 2^21).
+    int acck[4][4], accq[4][4];
+    float sxk = 0.0f, sxq = 0.0f;
+    if constexpr (INT8) {
 #pragma unroll
-        for (int rr = 0; rr < RB; ++rr) z[rr] = RowWord<INT8>::load(pv.base, hd, i0 + rr, lane);
+        for (int m = 0; m < 4; ++m)
 #pragma unroll
-        for (int rr = 0; rr < RB; ++rr) {
-            const float2 x = xkq_s[warp][i0 + rr];
-            const float4 v = RowWord<INT8>::values(z[rr]);
-            const float2 v01 = make_float2(v.x, v.y), v23 = make_float2(v.z, v.w);
-            const float2 xk = make_float2(x.x, x.x), xq = make_float2(x.y, x.y);
-            r01 = __ffma2_rn(v01, xk, r01);
-            r23 = __ffma2_rn(v23, xk, r23);
-            y01 = __ffma2_rn(v01, xq, y01);
-            y23 = __ffma2_rn(v23, xq, y23);
-        }
+            for (int d = 0; d < 4; ++d) acck[m][d] = accq[m][d] = 0;
     }
-    float4 r4 = make_float4(r01.x, r01.y, r23.x, r23.y);
-    float4 y4 = make_float4(y01.x, y01.y, y23.x, y23.y);
-
-    // ---- replay of the live log ----------------------------------------------
-    const size_t e0 = hd * static_cast<size_t>(W);
-#pragma unroll 2
-    for (int l = 0; l < L; ++l) {
-        const size_t eo = (e0 + l) * kD + 4 * lane;
-        const float4 K4 = ldg4(pv.klog + eo);
-        const float4 U4 = ldg4(pv.ulog + eo);
-        float ck, cq;
-        if constexpr (PER_KEY) {
-            const float4 Lm = ldg4(pv.lamlog + eo);
-            const float ax = K4.x * expf(lp4.x - Lm.x), ay = K4.y * expf(lp4.y - Lm.y);
-            const float az = K4.z * expf(lp4.z - Lm.z), aw = K4.w * expf(lp4.w - Lm.w);
-            ck = warp_sum(fmaf(ax, k4.x, fmaf(ay, k4.y, fmaf(az, k4.z, aw * k4.w))));
-            cq = warp_sum(fmaf(ax, q4.x, fmaf(ay, q4.y, fmaf(az, q4.z, aw * q4.w))));
-        } else {
-            const float g = expf(lp4.x - __ldg(pv.lamlog + e0 + l));
-            ck = warp_sum(fmaf(K4.x, k4.x, fmaf(K4.y, k4.y, fmaf(K4.z, k4.z, K4.w * k4.w)))) * g;
-            cq = warp_sum(fmaf(K4.x, q4.x, fmaf(K4.y, q4.y, fmaf(K4.z, q4.z, K4.w * q4.w)))) * g;
+#pragma unroll 1
+    for (int it = 0; it < NI; ++it) {
+        const int stg = it % kRing;
+        const bool ok = mbar_wait_bounded(&ws.bar[stg], (it / kRing) & 1);
+        if (__any_sync(0xffffffffu, !ok)) {
+            // a copy did not land: flag, drain what is still in flight, give up
+            if (lane == 0) {
+                flag_status(pv.status, kDevTimeout);
+                for (int j = it; j < min(NI, it + kRing); ++j)
+                    mbar_wait_bounded(&ws.bar[j % kRing], (j / kRing) & 1);
+            }
+            __syncwarp();
+            st4(a.y + ro, nan4);
+            return -1;
         }
-        r4 = make_float4(fmaf(ck, U4.x, r4.x), fmaf(ck, U4.y, r4.y), fmaf(ck, U4.z, r4.z),
-                         fmaf(ck, U4.w, r4.w));
-        y4 = make_float4(fmaf(cq, U4.x, y4.x), fmaf(cq, U4.y, y4.y), fmaf(cq, U4.z, y4.z),
-                         fmaf(cq, U4.w, y4.w));
+        const unsigned char* st = ws.ring[stg];
+        const float4* st4p = reinterpret_cast<const float4*>(st);
+        if (it == 0) {
+            k4 = st4p[lane];
+            q4 = st4p[32 + lane];
+            v4 = st4p[64 + lane];
+            int off = 96;
+            if constexpr (PER_KEY) {
+                const float4 lam4 = st4p[off + lane];
+                const float4 lb4 = st4p[off + 32 + lane];
+                lp4 = make_float4(lb4.x + lam4.x, lb4.y + lam4.y, lb4.z + lam4.z, lb4.w + lam4.w);
+                off += 64;
+            } else {
+                lp4 = make_float4(lp_scalar, lp_scalar, lp_scalar, lp_scalar);
+            }
+            float4 es = make_float4(expf(lp4.x), expf(lp4.y), expf(lp4.z), expf(lp4.w));
+            if constexpr (INT8) {
+                const float4 s4 = st4p[off + lane];
+                es = make_float4(es.x * s4.x, es.y * s4.y, es.z * s4.z, es.w * s4.w);
+            }
+            const float xk[4] = {es.x * k4.x, es.y * k4.y, es.z * k4.z, es.w * k4.w};
+            const float xq[4] = {es.x * q4.x, es.y * q4.y, es.z * q4.z, es.w * q4.w};
+            if constexpr (INT8) {
+                sxk = warp_max(fmaxf(fmaxf(fabsf(xk[0]), fabsf(xk[1])), fmaxf(fabsf(xk[2]), fabsf(xk[3]))));
+                sxq = warp_max(fmaxf(fmaxf(fabsf(xq[0]), fabsf(xq[1])), fmaxf(fabsf(xq[2]), fabsf(xq[3]))));
+                const float fk = sxk > 0.0f ? __fdiv_rn(1073741824.0f, sxk) : 0.0f;  // 2^30 / sx
+                const float fq = sxq > 0.0f ? __fdiv_rn(1073741824.0f, sxq) : 0.0f;
+                uint32_t dk[4] = {0u, 0u, 0u, 0u}, dq[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {  // key row 4*lane + r
+                    int a[4], c[4];
+                    digits4(min(max(__float2int_rn(xk[r] * fk), -1073741824), 1073741824), a);
+                    digits4(min(max(__float2int_rn(xq[r] * fq), -1073741824), 1073741824), c);
+#pragma unroll
+                    for (int d = 0; d < 4; ++d) {
+                        dk[d] |= (static_cast<uint32_t>(a[d]) & 0xffu) << (8 * r);
+                        dq[d] |= (static_cast<uint32_t>(c[d]) & 0xffu) << (8 * r);
+                    }
+                }
+                ws.dig[lane][0] = make_uint4(dk[0], dk[1], dk[2], dk[3]);
+                ws.dig[lane][1] = make_uint4(dq[0], dq[1], dq[2], dq[3]);
+            } else {
+#pragma unroll
+                for (int m = 0; m < 4; ++m) ws.xkq[4 * lane + m] = make_float4(xk[m], xk[m], xq[m], xq[m]);
+            }
+            kq = warp_sum(fmaf(k4.x, q4.x, fmaf(k4.y, q4.y, fmaf(k4.z, q4.z, k4.w * q4.w))));
+            __syncwarp();  // xk / xq visible to every lane before the base chunks
+        } else if (it <= P::NT) {
+            // base GEMVs over this chunk's key rows; the lane keeps its 4 columns
+            const int row0 = (it - 1) * P::ROWS;
+            if constexpr (INT8) {
+#pragma unroll
+                for (int g = 0; g < P::ROWS / 4; ++g) {
+                    const uint4 cw = reinterpret_cast<const uint4*>(st)[g * 32 + lane];
+                    const uint4 dk = ws.dig[row0 / 4 + g][0];
+                    const uint4 dq = ws.dig[row0 / 4 + g][1];
+                    const int col[4] = {static_cast<int>(cw.x), static_cast<int>(cw.y),
+                                        static_cast<int>(cw.z), static_cast<int>(cw.w)};
+                    const int kd[4] = {static_cast<int>(dk.x), static_cast<int>(dk.y),
+                                       static_cast<int>(dk.z), static_cast<int>(dk.w)};
+                    const int qd[4] = {static_cast<int>(dq.x), static_cast<int>(dq.y),
+                                       static_cast<int>(dq.z), static_cast<int>(dq.w)};
+#pragma unroll
+                    for (int m = 0; m < 4; ++m)
+#pragma unroll
+                        for (int d = 0; d < 4; ++d) {
+                            acck[m][d] = __dp4a(col[m], kd[d], acck[m][d]);
+                            accq[m][d] = __dp4a(col[m], qd[d], accq[m][d]);
+                        }
+                }
+                if (it == P::NT) {  // all key rows seen: back to floating point
+                    // sum_d acc_d 256^d: digits 1 and 2 combine exactly in int32
+                    // (|acc| < 2^21), the rest in FP32 (three roundings)
+                    const float ck = sxk * 9.31322574615478515625e-10f;  // sx 2^-30
+                    const float cq = sxq * 9.31322574615478515625e-10f;
+                    float rk[4], rq[4];
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const int tk = acck[m][1] + (acck[m][2] << 8);
+                        const int tq = accq[m][1] + (accq[m][2] << 8);
+                        rk[m] = fmaf(static_cast<float>(acck[m][3]), 16777216.0f,
+                                     fmaf(static_cast<float>(tk), 256.0f,
+                                          static_cast<float>(acck[m][0]))) * ck;
+                        rq[m] = fmaf(static_cast<float>(accq[m][3]), 16777216.0f,
+                                     fmaf(static_cast<float>(tq), 256.0f,
+                                          static_cast<float>(accq[m][0]))) * cq;
+                    }
+                    r01 = make_float2(rk[0], rk[1]);
+                    r23 = make_float2(rk[2], rk[3]);
+                    y01 = make_float2(rq[0], rq[1]);
+                    y23 = make_float2(rq[2], rq[3]);
+                }
+            } else {
+#pragma unroll
+                for (int g = 0; g < P::ROWS / 4; ++g) {
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const float4 v = st4p[(4 * g + m) * 32 + lane];
+                        const float4 x = ws.xkq[row0 + 4 * g + m];  // (xk, xk, xq, xq)
+                        const float2 xk = make_float2(x.x, x.y), xq = make_float2(x.z, x.w);
+                        const float2 v01 = make_float2(v.x, v.y), v23 = make_float2(v.z, v.w);
+                        r01 = __ffma2_rn(v01, xk, r01);
+                        r23 = __ffma2_rn(v23, xk, r23);
+                        y01 = __ffma2_rn(v01, xq, y01);
+                        y23 = __ffma2_rn(v23, xq, y23);
+                    }
+                }
+            }
+        } else {
+            // replay of this chunk's log entries (LeapQuant eq. 9)
+            const int e0 = (it - 1 - P::NT) * P::EPC;
+            const int n = min(P::EPC, L - e0);
+            for (int e = 0; e < n; ++e) {
+                const float4 K4 = st4p[e * 32 + lane];
+                const float4 U4 = st4p[(P::EPC + e) * 32 + lane];
+                float ck, cq;
+                if constexpr (PER_KEY) {
+                    const float4 Lm = st4p[(2 * P::EPC + e) * 32 + lane];
+                    const float ax = K4.x * expf(lp4.x - Lm.x), ay = K4.y * expf(lp4.y - Lm.y);
+                    const float az = K4.z * expf(lp4.z - Lm.z), aw = K4.w * expf(lp4.w - Lm.w);
+                    ck = warp_sum(fmaf(ax, k4.x, fmaf(ay, k4.y, fmaf(az, k4.z, aw * k4.w))));
+                    cq = warp_sum(fmaf(ax, q4.x, fmaf(ay, q4.y, fmaf(az, q4.z, aw * q4.w))));
+                } else {
+                    const float g = expf(lp4.x - reinterpret_cast<const float*>(st + kChunk)[e]);
+                    ck = warp_sum(fmaf(K4.x, k4.x, fmaf(K4.y, k4.y, fmaf(K4.z, k4.z, K4.w * k4.w)))) * g;
+                    cq = warp_sum(fmaf(K4.x, q4.x, fmaf(K4.y, q4.y, fmaf(K4.z, q4.z, K4.w * q4.w)))) * g;
+                }
+                r01 = make_float2(fmaf(ck, U4.x, r01.x), fmaf(ck, U4.y, r01.y));
+                r23 = make_float2(fmaf(ck, U4.z, r23.x), fmaf(ck, U4.w, r23.y));
+                y01 = make_float2(fmaf(cq, U4.x, y01.x), fmaf(cq, U4.y, y01.y));
+                y23 = make_float2(fmaf(cq, U4.z, y23.x), fmaf(cq, U4.w, y23.y));
+            }
+        }
+        __syncwarp();  // every lane is done with the stage
+        if (lane == 0 && it + kRing < NI) issue_item<INT8, PER_KEY>(ws, a, row, hd, L, it + kRing);
     }
 
     // ---- delta correction and output -----------------------------------------
-    const float4 u4 = make_float4(beta * (v4.x - r4.x), beta * (v4.y - r4.y),
-                                  beta * (v4.z - r4.z), beta * (v4.w - r4.w));
-    st4(a.y + ro, make_float4(fmaf(kq, u4.x, y4.x), fmaf(kq, u4.y, y4.y), fmaf(kq, u4.z, y4.z),
-                              fmaf(kq, u4.w, y4.w)));
+    const float4 u4 = make_float4(beta * (v4.x - r01.x), beta * (v4.y - r01.y),
+                                  beta * (v4.z - r23.x), beta * (v4.w - r23.y));
+    st4(a.y + ro, make_float4(fmaf(kq, u4.x, y01.x), fmaf(kq, u4.y, y01.y),
+                              fmaf(kq, u4.z, y23.x), fmaf(kq, u4.w, y23.y)));
 
     // ---- append entry L -------------------------------------------------------
     {
-        const size_t eo = (e0 + L) * kD + 4 * lane;
+        const size_t eo = (hd * static_cast<size_t>(W) + L) * kD + 4 * lane;
         st4(pv.klog + eo, k4);
         st4(pv.ulog + eo, u4);
-        if constexpr (PER_KEY) st4(pv.lamlog + eo, lp4);
-        else if (lane == 0) pv.lamlog[e0 + L] = lp4.x;
+        const size_t lb0 = hd * static_cast<size_t>(pv.lam_stride);
+        if constexpr (PER_KEY) st4(pv.lamlog + lb0 + static_cast<size_t>(L) * kD + 4 * lane, lp4);
+        else if (lane == 0) pv.lamlog[lb0 + L] = lp4.x;
     }
+    if constexpr (PER_KEY) st4(pv.lbar + hd * kD + 4 * lane, lp4);
+    else if (lane == 0) pv.lbar[hd] = lp4.x;
     if (L + 1 < W) {
-        if constexpr (PER_KEY) st4(pv.lbar + hd * kD + 4 * lane, lp4);
-        else if (lane == 0) pv.lbar[hd] = lp4.x;
         if (lane == 0) pv.len[hd] = L + 1;
-        return;
+        return -1;
     }
-    // ---- window end: fold the W entries into the base, start a new window ----
+    *lp_out = lp4.x;
+    return static_cast<long long>(hd);  // window end: the CTA folds the W entries
+}
+
+template <bool INT8, bool PER_KEY>
+__global__ void __launch_bounds__(kThreads, 2) log_step_kernel(const StepArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ long long fold_hd[kWarps];
+    __shared__ float fold_lb[kWarps];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const PoolView& pv = a.pv;
+    const int row = blockIdx.x * kWarps + warp;
+    float lp = 0.0f;
+    long long hd = -1;
+    WarpSmem& ws = reinterpret_cast<WarpSmem*>(smem)[warp];
+    if (lane == 0) ws.bar_live = 0u;
     __syncwarp();
-    fold_warp<INT8, PER_KEY, kFoldCommit>(pv, hd, L + 1, lp_s[warp], lp4.x, nullptr, lane);
-    if constexpr (PER_KEY) st4(pv.lbar + hd * kD + 4 * lane, make_float4(0.f, 0.f, 0.f, 0.f));
-    else if (lane == 0) pv.lbar[hd] = 0.0f;
-    if (lane == 0) pv.len[hd] = 0;
+    if (row < a.batch * pv.H) hd = warp_step<INT8, PER_KEY>(a, ws, row, &lp);
+    if (lane == 0) {
+        fold_hd[warp] = hd;
+        fold_lb[warp] = lp;
+    }
+    // ---- window ends: the whole CTA folds each closed window in turn ----------
+    // (the ring memory is free now and becomes the fold's staging area)
+    if (!__syncthreads_or(hd >= 0)) return;
+    if (lane == 0 && ws.bar_live) {
+#pragma unroll
+        for (int s = 0; s < kRing; ++s) mbar_inval(&ws.bar[s]);
+    }
+    __syncthreads();
+    const FoldSmem fs = fold_smem(smem, INT8);
+    if (threadIdx.x == 0) {
+        mbar_init(fs.bar, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    uint32_t phase = 0;
+    for (int w = 0; w < kWarps; ++w) {
+        const long long h = fold_hd[w];
+        if (h < 0) continue;
+        const size_t st = static_cast<size_t>(h);
+        const bool ok = fold_cta<INT8, PER_KEY, kFoldCommit>(pv, st, pv.W, pv.lbar + st * (PER_KEY ? kD : 1),
+                                                             fold_lb[w], nullptr, fs, phase);
+        phase ^= 1u;
+        __syncthreads();  // every reader of lbar is done
+        if (ok) {
+            if (PER_KEY) {
+                if (threadIdx.x < kD / 4) st4(pv.lbar + st * kD + 4 * threadIdx.x, make_float4(0.f, 0.f, 0.f, 0.f));
+            } else if (threadIdx.x == 0) {
+                pv.lbar[st] = 0.0f;
+            }
+            if (threadIdx.x == 0) pv.len[st] = 0;
+        } else {
+            break;
+        }
+    }
 }
 
 template <typename K>
@@ -336,7 +552,11 @@ cudaError_t prepare_step_kernels() {
     cudaError_t e;
     if ((e = set_smem(eager_step_kernel<false>, eager_smem_bytes())) != cudaSuccess) return e;
     if ((e = set_smem(eager_step_kernel<true>, eager_smem_bytes())) != cudaSuccess) return e;
-    return cudaSuccess;
+    const size_t ls = step_smem_bytes();
+    if ((e = set_smem(log_step_kernel<false, false>, ls)) != cudaSuccess) return e;
+    if ((e = set_smem(log_step_kernel<false, true>, ls)) != cudaSuccess) return e;
+    if ((e = set_smem(log_step_kernel<true, false>, ls)) != cudaSuccess) return e;
+    return set_smem(log_step_kernel<true, true>, ls);
 }
 
 cudaError_t launch_eager_step(const StepArgs& a, bool per_key, cudaStream_t s) {
@@ -351,16 +571,17 @@ cudaError_t launch_eager_step(const StepArgs& a, bool per_key, cudaStream_t s) {
 cudaError_t launch_log_step(const StepArgs& a, bool int8, bool per_key, cudaStream_t s) {
     const int64_t rows = static_cast<int64_t>(a.batch) * a.pv.H;
     const dim3 grid(static_cast<unsigned>((rows + kWarps - 1) / kWarps));
+    const size_t sm = step_smem_bytes();
     if (int8) {
         if (per_key)
-            log_step_kernel<true, true><<<grid, kThreads, 0, s>>>(a);
+            log_step_kernel<true, true><<<grid, kThreads, sm, s>>>(a);
         else
-            log_step_kernel<true, false><<<grid, kThreads, 0, s>>>(a);
+            log_step_kernel<true, false><<<grid, kThreads, sm, s>>>(a);
     } else {
         if (per_key)
-            log_step_kernel<false, true><<<grid, kThreads, 0, s>>>(a);
+            log_step_kernel<false, true><<<grid, kThreads, sm, s>>>(a);
         else
-            log_step_kernel<false, false><<<grid, kThreads, 0, s>>>(a);
+            log_step_kernel<false, false><<<grid, kThreads, sm, s>>>(a);
     }
     return cudaGetLastError();
 }

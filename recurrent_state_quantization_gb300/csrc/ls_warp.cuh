@@ -1,12 +1,11 @@
 // ls_warp.cuh -- warp-per-head building blocks of the deferred and per-window
 // INT8 variants (sm_103a).
 //
-// One warp owns one (slot, head).  The base is stored row-major, S[i][j]
-// (key row i, value column j); lane l owns value columns 4l..4l+3 and, for
-// vectors indexed by key, key rows 4l..4l+3.  A base row is one coalesced
-// warp access (512 B FP32, 128 B INT8), so the GEMVs S^T x reduce over key
-// rows inside each lane, with no cross-lane reduction, and a key row's absmax
-// (the INT8 scale) is a warp reduction.
+// One warp owns one (slot, head).  Lane l owns value columns 4l..4l+3 and, for
+// vectors indexed by key, key rows 4l..4l+3.  The base is row-major (FP32) or
+// in 4x4 quads (INT8, see PoolView), so one warp access covers whole key rows:
+// the GEMVs S^T x reduce over key rows inside each lane (no cross-lane
+// reduction) and a key row's absmax (the INT8 scale) is a warp reduction.
 #pragma once
 
 #include <cstdint>
@@ -30,128 +29,231 @@ __device__ __forceinline__ float4 ldcg4(const float* p) {
     return __ldcg(reinterpret_cast<const float4*>(p));
 }
 
-// 4 INT8 codes (one 32-bit word, little-endian) -> 4 floats.
-__device__ __forceinline__ float4 codes4(uint32_t w) {
-    return make_float4(static_cast<float>(static_cast<int8_t>(w & 0xffu)),
-                       static_cast<float>(static_cast<int8_t>((w >> 8) & 0xffu)),
-                       static_cast<float>(static_cast<int8_t>((w >> 16) & 0xffu)),
-                       static_cast<float>(static_cast<int8_t>(w >> 24)));
+// Symmetric INT8 code of x with scale s, as the low byte of a word.
+__device__ __forceinline__ uint32_t code_byte(float x, float s) {
+    return static_cast<uint32_t>(quant_code(x, s)) & 0xffu;
 }
 
-template <bool INT8>
-struct BaseRows {
-    // Row i of head hd, the lane's 4 columns.
-    static __device__ __forceinline__ float4 stream(const void* base, size_t hd, int i, int lane) {
-        if constexpr (INT8) {
-            const uint32_t* p = reinterpret_cast<const uint32_t*>(base) + hd * (kD * kD / 4) +
-                                i * (kD / 4) + lane;
-            uint32_t w;
-            asm volatile("ld.global.nc.L1::no_allocate.b32 %0, [%1];" : "=r"(w) : "l"(p));
-            return codes4(w);
-        } else {
-            return ld_stream4(reinterpret_cast<const float*>(base) + hd * (kD * kD) + i * kD +
-                              4 * lane);
-        }
-    }
-    static __device__ __forceinline__ float4 coherent(const void* base, size_t hd, int i, int lane) {
-        if constexpr (INT8) {
-            const uint32_t* p = reinterpret_cast<const uint32_t*>(base) + hd * (kD * kD / 4) +
-                                i * (kD / 4) + lane;
-            return codes4(__ldcg(p));
-        } else {
-            return ldcg4(reinterpret_cast<const float*>(base) + hd * (kD * kD) + i * kD + 4 * lane);
-        }
-    }
-};
+// INT8 base, column quads: the 16 bytes of quad (i4, c) hold key rows
+// 4*i4..4*i4+3 of value columns 4*c..4*c+3; word m is column 4*c + m and its
+// byte r is row 4*i4 + r.  quad_index addresses the quad in 16-byte units.
+__device__ __forceinline__ size_t quad_index(size_t hd, int i4, int c) {
+    return hd * (kD * kD / 16) + static_cast<size_t>(i4) * (kD / 4) + c;
+}
 
-// Symmetric INT8 codes of 4 values with a common scale, packed little-endian.
-__device__ __forceinline__ uint32_t pack_codes4(float4 v, float s) {
-    const uint32_t a = static_cast<uint32_t>(quant_code(v.x, s)) & 0xffu;
-    const uint32_t b = static_cast<uint32_t>(quant_code(v.y, s)) & 0xffu;
-    const uint32_t c = static_cast<uint32_t>(quant_code(v.z, s)) & 0xffu;
-    const uint32_t d = static_cast<uint32_t>(quant_code(v.w, s)) & 0xffu;
-    return a | (b << 8) | (c << 16) | (d << 24);
+// Byte r of each of the 4 words of a quad -> the 4 columns of row r.
+__device__ __forceinline__ float4 quad_row(uint4 q, int r) {
+    const int sh = 8 * r;
+    return make_float4(static_cast<float>(static_cast<int8_t>((q.x >> sh) & 0xffu)),
+                       static_cast<float>(static_cast<int8_t>((q.y >> sh) & 0xffu)),
+                       static_cast<float>(static_cast<int8_t>((q.z >> sh) & 0xffu)),
+                       static_cast<float>(static_cast<int8_t>((q.w >> sh) & 0xffu)));
+}
+
+// Codes of 4 rows x 4 columns (rows[r] = the 4 columns of row r, each row
+// with its own scale) packed as one column quad.
+__device__ __forceinline__ uint4 pack_quad(const float4 (&rows)[4], const float (&s)[4]) {
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        w[0] |= code_byte(rows[r].x, s[r]) << (8 * r);
+        w[1] |= code_byte(rows[r].y, s[r]) << (8 * r);
+        w[2] |= code_byte(rows[r].z, s[r]) << (8 * r);
+        w[3] |= code_byte(rows[r].w, s[r]) << (8 * r);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Split x (|x| <= 2^30) into 4 signed base-256 digits, x = sum_d d_d 256^d,
+// d_d in [-128, 127]; digit d is returned in out[d] (low byte significant).
+__device__ __forceinline__ void digits4(int x, int (&out)[4]) {
+#pragma unroll
+    for (int d = 0; d < 3; ++d) {
+        const int lo = ((x + 128) & 0xff) - 128;
+        out[d] = lo;
+        x = (x - lo) >> 8;
+    }
+    out[3] = x;
 }
 
 enum FoldMode : int { kFoldCommit = 0, kFoldRead = 1 };
 
-constexpr int kFoldRows = 8;  // key rows folded per block
-
-// Fold the first `n` log entries of state hd into its base, 8 key rows at a
-// time (a warp holds 8 x 128 accumulators):
+// ---------------------------------------------------------------------------
+// CTA-cooperative fold of one state (256 threads).
+//
+// Folds the first n log entries of state hd into its base:
 //     S[i][:] = exp(lb_i) dequant(B)[i][:] + sum_{l<n} exp(lb_i - Lam_l,i) K_l,i U_l[:]
 // ("DeltaLog: Deferred Materialization of Recurrent States for Linear
 // Attention Decoding", §3.2 eq. 7; eq. 6 when the log holds the current
 // token, whose snapshot equals lb).  lb is the cumulative log-decay the log
-// is folded at: per key row in lb_s (shared memory, per-key gate) or the
-// scalar lb (scalar gate).
+// is folded at: per key row at lbg (per-key gate; GLOBAL memory, read through
+// L2 because the caller may just have written it) or lb_scalar.
 //   kFoldCommit: deferred -> S is the new FP32 base;  INT8 -> per key row
 //     s_i = max_j |S_ij| / 127, codes rint(S / s_i) clamped to [-127, 127]
 //     ("LeapQuant: Efficient Linear Attention with Accurate Recurrent State
 //     Quantization", §3.2 eq. 4, App. B.3) -- written in place;
 //   kFoldRead: S is written to out ([d_k][d_v]) and the pool is unchanged.
+// Work split: warp w owns key rows 16w..16w+15 (so a row's absmax is a warp
+// reduction), lane l value columns 4l..4l+3; 64 FP32 accumulators per
+// thread.  The base tile is staged by bulk asynchronous copies, the log in
+// chunks of kFoldChunk entries with (a, a) pairs a = exp(lb - Lam) K for the
+// paired FMAs.  Returns false after a copy timeout (flagged).
+// ---------------------------------------------------------------------------
+constexpr int kFoldChunk = 16;
+
+struct FoldSmem {
+    unsigned char* tile;  // tile_bytes(INT8)
+    float2* a2;           // [kFoldChunk][kD] (a, a)
+    float4* u4;           // [kFoldChunk][kD / 4]
+    uint64_t* bar;
+};
+
+__host__ __device__ constexpr size_t fold_smem_bytes(bool int8) {
+    return tile_bytes(int8) + size_t(kFoldChunk) * kD * 8 + size_t(kFoldChunk) * kD * 4 + 16;
+}
+
+__device__ __forceinline__ FoldSmem fold_smem(unsigned char* base, bool int8) {
+    FoldSmem f;
+    f.tile = base;
+    f.a2 = reinterpret_cast<float2*>(base + tile_bytes(int8));
+    f.u4 = reinterpret_cast<float4*>(base + tile_bytes(int8) + size_t(kFoldChunk) * kD * 8);
+    f.bar = reinterpret_cast<uint64_t*>(base + tile_bytes(int8) + size_t(kFoldChunk) * kD * 12);
+    return f;
+}
+
 template <bool INT8, bool PER_KEY, int MODE>
-__device__ __forceinline__ void fold_warp(const PoolView& pv, size_t hd, int n,
-                                          const float* lb_s, float lb, float* out, int lane) {
-    const size_t e0 = hd * static_cast<size_t>(pv.W);
-#pragma unroll 1
-    for (int i0 = 0; i0 < kD; i0 += kFoldRows) {
-        float4 acc[kFoldRows];
-        // decayed, dequantized base rows
+__device__ bool fold_cta(const PoolView& pv, size_t hd, int n, const float* lbg, float lb_scalar,
+                         float* out, const FoldSmem& fs, uint32_t phase) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr uint32_t kTile = static_cast<uint32_t>(tile_bytes(INT8));
+    constexpr uint32_t kPart = kTile / 4;
+    if (tid == 0) {
+        const unsigned char* src = reinterpret_cast<const unsigned char*>(pv.base) + hd * kTile;
+        fence_proxy_async();  // the staging area was last used by generic loads and stores
+        mbar_arrive_expect_tx(fs.bar, kTile);
 #pragma unroll
-        for (int r = 0; r < kFoldRows; ++r) {
-            const int i = i0 + r;
-            float e = expf(PER_KEY ? lb_s[i] : lb);
-            if constexpr (INT8) e *= __ldcg(pv.scale + hd * kD + i);
-            const float4 b = BaseRows<INT8>::coherent(pv.base, hd, i, lane);
-            acc[r] = make_float4(e * b.x, e * b.y, e * b.z, e * b.w);
+        for (int i = 0; i < 4; ++i) bulk_g2s(fs.tile + i * kPart, src + i * kPart, kPart, fs.bar);
+    }
+    // decay (and INT8 scale) of the thread's 16 key rows
+    const int i0 = 16 * warp;
+    float e[16];
+#pragma unroll
+    for (int r4 = 0; r4 < 4; ++r4) {
+        float4 lb4 = make_float4(lb_scalar, lb_scalar, lb_scalar, lb_scalar);
+        if constexpr (PER_KEY) lb4 = ldcg4(lbg + i0 + 4 * r4);
+        float4 s4 = make_float4(1.f, 1.f, 1.f, 1.f);
+        if constexpr (INT8) s4 = ldcg4(pv.scale + hd * kD + i0 + 4 * r4);
+        e[4 * r4 + 0] = expf(lb4.x) * s4.x;
+        e[4 * r4 + 1] = expf(lb4.y) * s4.y;
+        e[4 * r4 + 2] = expf(lb4.z) * s4.z;
+        e[4 * r4 + 3] = expf(lb4.w) * s4.w;
+    }
+    const bool ok = mbar_wait_bounded(fs.bar, phase);
+    if (__syncthreads_or(!ok)) {
+        if (tid == 0) {
+            flag_status(pv.status, kDevTimeout);
+            mbar_wait_bounded(fs.bar, phase);
         }
-        // + sum_l exp(lb - Lam_l) K_l U_l^T
-#pragma unroll 1
-        for (int l = 0; l < n; ++l) {
-            const size_t eo = (e0 + l) * kD;
-            const float4 ka = ldcg4(pv.klog + eo + i0);
-            const float4 kb = ldcg4(pv.klog + eo + i0 + 4);
-            const float4 u = ldcg4(pv.ulog + eo + 4 * lane);
-            float a[kFoldRows] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
-            if constexpr (PER_KEY) {
-                const float4 la = ldcg4(pv.lamlog + eo + i0);
-                const float4 lc = ldcg4(pv.lamlog + eo + i0 + 4);
-                const float lm[kFoldRows] = {la.x, la.y, la.z, la.w, lc.x, lc.y, lc.z, lc.w};
+        __syncthreads();
+        return false;
+    }
+    // decayed, dequantized base rows; acc[r] = columns 4l..4l+3 of row i0 + r
+    float2 lo[16], hi[16];
 #pragma unroll
-                for (int r = 0; r < kFoldRows; ++r) a[r] *= expf(lb_s[i0 + r] - lm[r]);
-            } else {
-                const float g = expf(lb - __ldcg(pv.lamlog + e0 + l));
+    for (int qd = 0; qd < 4; ++qd) {
+        if constexpr (INT8) {
+            const uint4 q = reinterpret_cast<const uint4*>(fs.tile)[(i0 / 4 + qd) * (kD / 4) + lane];
 #pragma unroll
-                for (int r = 0; r < kFoldRows; ++r) a[r] *= g;
+            for (int r = 0; r < 4; ++r) {
+                const float4 z = quad_row(q, r);
+                const float ee = e[4 * qd + r];
+                lo[4 * qd + r] = make_float2(ee * z.x, ee * z.y);
+                hi[4 * qd + r] = make_float2(ee * z.z, ee * z.w);
             }
+        } else {
 #pragma unroll
-            for (int r = 0; r < kFoldRows; ++r) {
-                acc[r].x = fmaf(a[r], u.x, acc[r].x);
-                acc[r].y = fmaf(a[r], u.y, acc[r].y);
-                acc[r].z = fmaf(a[r], u.z, acc[r].z);
-                acc[r].w = fmaf(a[r], u.w, acc[r].w);
-            }
-        }
-        // write the block
-#pragma unroll
-        for (int r = 0; r < kFoldRows; ++r) {
-            const int i = i0 + r;
-            if constexpr (MODE == kFoldRead) {
-                st4(out + i * kD + 4 * lane, acc[r]);
-            } else if constexpr (!INT8) {
-                st4(reinterpret_cast<float*>(pv.base) + hd * (kD * kD) + i * kD + 4 * lane, acc[r]);
-            } else {
-                float m = fmaxf(fmaxf(fabsf(acc[r].x), fabsf(acc[r].y)),
-                                fmaxf(fabsf(acc[r].z), fabsf(acc[r].w)));
-                m = warp_max(m);
-                const float s = __fdiv_rn(m, 127.0f);
-                reinterpret_cast<uint32_t*>(pv.base)[hd * (kD * kD / 4) + i * (kD / 4) + lane] =
-                    pack_codes4(acc[r], s);
-                if (lane == 0) pv.scale[hd * kD + i] = s;
+            for (int r = 0; r < 4; ++r) {
+                const int row = 4 * qd + r;
+                const float4 b = reinterpret_cast<const float4*>(fs.tile)[(i0 + row) * (kD / 4) + lane];
+                lo[row] = make_float2(e[row] * b.x, e[row] * b.y);
+                hi[row] = make_float2(e[row] * b.z, e[row] * b.w);
             }
         }
     }
+    // + sum_l exp(lb - Lam_l) K_l U_l^T, kFoldChunk entries at a time
+    const size_t kb = hd * static_cast<size_t>(pv.W);
+    const size_t lb0 = hd * static_cast<size_t>(pv.lam_stride);
+#pragma unroll 1
+    for (int c0 = 0; c0 < n; c0 += kFoldChunk) {
+        const int nl = min(kFoldChunk, n - c0);
+        __syncthreads();  // the previous chunk is consumed
+        for (int idx = tid; idx < nl * (kD / 4); idx += kThreads) {
+            const int l = idx >> 5, q = idx & 31;  // entry, 4-row / 4-column group
+            const size_t eo = (kb + c0 + l) * kD + 4 * q;
+            const float4 K4 = ldcg4(pv.klog + eo);
+            fs.u4[l * (kD / 4) + q] = ldcg4(pv.ulog + eo);
+            float4 g;
+            if constexpr (PER_KEY) {
+                const float4 lm = ldcg4(pv.lamlog + lb0 + static_cast<size_t>(c0 + l) * kD + 4 * q);
+                const float4 lb4 = ldcg4(lbg + 4 * q);
+                g = make_float4(expf(lb4.x - lm.x), expf(lb4.y - lm.y), expf(lb4.z - lm.z),
+                                expf(lb4.w - lm.w));
+            } else {
+                const float gg = expf(lb_scalar - __ldcg(pv.lamlog + lb0 + c0 + l));
+                g = make_float4(gg, gg, gg, gg);
+            }
+            float4* a2 = reinterpret_cast<float4*>(fs.a2 + l * kD + 4 * q);
+            const float ax = g.x * K4.x, ay = g.y * K4.y, az = g.z * K4.z, aw = g.w * K4.w;
+            a2[0] = make_float4(ax, ax, ay, ay);
+            a2[1] = make_float4(az, az, aw, aw);
+        }
+        __syncthreads();
+#pragma unroll 2
+        for (int l = 0; l < nl; ++l) {
+            const float4 u = fs.u4[l * (kD / 4) + lane];
+            const float2 u01 = make_float2(u.x, u.y), u23 = make_float2(u.z, u.w);
+            const float4* ap = reinterpret_cast<const float4*>(fs.a2 + l * kD + i0);
+#pragma unroll
+            for (int r2 = 0; r2 < 8; ++r2) {
+                const float4 aa = ap[r2];  // (a, a) of rows i0 + 2 r2, i0 + 2 r2 + 1
+                const float2 a0 = make_float2(aa.x, aa.y), a1 = make_float2(aa.z, aa.w);
+                lo[2 * r2] = __ffma2_rn(a0, u01, lo[2 * r2]);
+                hi[2 * r2] = __ffma2_rn(a0, u23, hi[2 * r2]);
+                lo[2 * r2 + 1] = __ffma2_rn(a1, u01, lo[2 * r2 + 1]);
+                hi[2 * r2 + 1] = __ffma2_rn(a1, u23, hi[2 * r2 + 1]);
+            }
+        }
+    }
+    // write the 16 rows
+    if constexpr (MODE == kFoldRead) {
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+            st4(out + (i0 + r) * kD + 4 * lane, make_float4(lo[r].x, lo[r].y, hi[r].x, hi[r].y));
+    } else if constexpr (!INT8) {
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+            st4(reinterpret_cast<float*>(pv.base) + hd * (kD * kD) + (i0 + r) * kD + 4 * lane,
+                make_float4(lo[r].x, lo[r].y, hi[r].x, hi[r].y));
+    } else {
+#pragma unroll
+        for (int qd = 0; qd < 4; ++qd) {
+            float sc[4];
+            float4 rows[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int row = 4 * qd + r;
+                rows[r] = make_float4(lo[row].x, lo[row].y, hi[row].x, hi[row].y);
+                float mx = fmaxf(fmaxf(fabsf(rows[r].x), fabsf(rows[r].y)),
+                                 fmaxf(fabsf(rows[r].z), fabsf(rows[r].w)));
+                mx = warp_max(mx);
+                sc[r] = __fdiv_rn(mx, 127.0f);
+            }
+            reinterpret_cast<uint4*>(pv.base)[quad_index(hd, i0 / 4 + qd, lane)] = pack_quad(rows, sc);
+            if (lane == 0)
+                st4(pv.scale + hd * kD + i0 + 4 * qd, make_float4(sc[0], sc[1], sc[2], sc[3]));
+        }
+    }
+    return true;
 }
 
 }  // namespace ls
