@@ -30,12 +30,13 @@
  *   - The delta-rule readout uses the decayed state, S^T (alpha . k), as in
  *     the right-hand sides of [LQ] App. A.
  *   - The output is always the post-update readout y = S_t^T q_t ([LQ] eq. 1).
- *   - INT8 per-window scheme: symmetric INT8 with one FP32 scale per key row,
- *     s_i = max_j |S_ij| / 127, Z = clamp(round-half-even(S/s), -127, 127);
- *     a zero row (or a scale that underflows to 0) gets s = 0 and Z = 0.
- *     The decision (absmax, scale, division, rounding) is taken in FP32 on
- *     the FP32 rounding of the double state, the precision the CUDA kernel
- *     computes in ([LQ] App. B.3 fixes only the "/127" symmetric form).
+ *   - INT8 per-window scheme: symmetric INT8 with one FP32 scale per key row:
+ *     B_i = max_j |S_ij|, Z = clamp(round-half-even(S * (127 / B_i)), -127, 127),
+ *     stored scale s_i = B_i / 127 ([LQ] App. B.3 writes dequant = (Z/127) B);
+ *     a zero row (or one whose factor overflows) gets s = 0 and Z = 0.  The
+ *     decision (absmax, factor, product, rounding) is taken in FP32 on the
+ *     FP32 rounding of the double state, the precision the CUDA kernel
+ *     computes in.
  *   - The window counts tokens from the last boundary (load, commit or
  *     reset); the W-th token's output is read from the unquantized S_W, then
  *     S_W is quantized ([LQ] §3.2 eq. 4).  W = 1 is per-step quantization
@@ -45,6 +46,7 @@
  *   - An explicit commit of a state with an empty log/window leaves it as it
  *     is (nothing to fold, the state is already at a boundary).
  */
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -368,8 +370,15 @@ int orc_deferred_commit(int64_t n, int dk, int dv, int dl, int M,
 /* ------------------------------------------------------------------------ */
 
 /*
- * quant_8 of [LQ] §3.1 / App. B.3 (symmetric, "/127"), one scale per key
- * row.  The decision is taken in FP32 on the FP32 rounding of S.
+ * quant_8 of [LQ] §3.1 / App. B.3, one scale per key row.  App. B.3 writes
+ * the dequantization as (Z / 127) B with B the row's absmax, so the row is
+ * quantized by the factor 127 / B:
+ *     Z_ij = clamp(round-half-even(S_ij * (127 / B_i)), -127, 127),
+ *     stored scale s_i = B_i / 127 (dequant S_ij = s_i Z_ij).
+ * The decision is taken in FP32 on the FP32 rounding of S: B_i, 127 / B_i,
+ * B_i / 127 and the product are each correctly rounded FP32 operations.  A
+ * row whose scale or factor is not a positive finite FP32 number (a zero row,
+ * or one so small that 127 / B overflows) gets s = 0 and Z = 0.
  */
 static void quant_rows(int dk, int dv, const double *S, int8_t *Z, float *s)
 {
@@ -379,12 +388,18 @@ static void quant_rows(int dk, int dv, const double *S, int8_t *Z, float *s)
             const float a = fabsf((float)S[(size_t)i * dv + j]);
             if (a > amax) amax = a;
         }
-        const float sc = amax / 127.0f;
+        float sc = amax / 127.0f;
+        float inv = amax > 0.0f ? 127.0f / amax : 0.0f;
+        if (!(sc > 0.0f) || !(inv <= FLT_MAX)) {
+            sc = 0.0f;
+            inv = 0.0f;
+        }
         s[i] = sc;
         for (int j = 0; j < dv; ++j) {
             int8_t z = 0;
             if (sc > 0.0f) {
-                float t = rintf((float)S[(size_t)i * dv + j] / sc);
+                const float x = (float)S[(size_t)i * dv + j];
+                float t = rintf(x * inv);
                 if (t > 127.0f) t = 127.0f;
                 if (t < -127.0f) t = -127.0f;
                 z = (int8_t)t;

@@ -81,15 +81,16 @@ __global__ void __launch_bounds__(kThreads) load_rows_kernel(const AuxArgs a) {
                 st4(reinterpret_cast<float*>(pv.base) + hd * (kD * kD) + (4 * i4 + m) * kD + 4 * lane,
                     v[m]);
         } else {
-            float sc[4];
+            float f[4];
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 float mx = fmaxf(fmaxf(fabsf(v[m].x), fabsf(v[m].y)), fmaxf(fabsf(v[m].z), fabsf(v[m].w)));
                 mx = warp_max(mx);
-                sc[m] = __fdiv_rn(mx, 127.0f);
-                if (lane == 0) pv.scale[hd * kD + 4 * i4 + m] = sc[m];
+                float sc;
+                row_quant_params(mx, sc, f[m]);
+                if (lane == 0) pv.scale[hd * kD + 4 * i4 + m] = sc;
             }
-            reinterpret_cast<uint4*>(pv.base)[quad_index(hd, i4, lane)] = pack_quad(v, sc);
+            reinterpret_cast<uint4*>(pv.base)[quad_index(hd, i4, lane)] = pack_quad(v, f);
         }
     }
     clear_log(pv, hd);

@@ -146,11 +146,23 @@ __device__ __forceinline__ void gather16(const float* vec, int g, float (&x)[16]
     }
 }
 
-// Symmetric INT8 code of x with scale s (> 0): round half to even, clamp to
-// [-127, 127].  The division is the correctly rounded FP32 one.
-__device__ __forceinline__ int quant_code(float x, float s) {
-    if (!(s > 0.0f)) return 0;
-    int z = __float2int_rn(__fdiv_rn(x, s));
+// Per-key-row INT8 parameters from the row's absmax B: stored scale
+// s = B / 127 and quantization factor f = 127 / B (correctly rounded FP32;
+// LeapQuant App. B.3 writes dequant = (Z / 127) B).  A row whose scale or
+// factor is not a positive finite FP32 number gets s = f = 0 (codes 0).
+__device__ __forceinline__ void row_quant_params(float amax, float& s, float& f) {
+    s = __fdiv_rn(amax, 127.0f);
+    f = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
+    if (!(s > 0.0f) || !(f <= 3.402823466e38f)) {
+        s = 0.0f;
+        f = 0.0f;
+    }
+}
+
+// Symmetric INT8 code of x with factor f: round half to even, clamp to
+// [-127, 127].  f = 0 gives 0.
+__device__ __forceinline__ int quant_code(float x, float f) {
+    int z = __float2int_rn(x * f);
     z = z > 127 ? 127 : z;
     z = z < -127 ? -127 : z;
     return z;

@@ -29,9 +29,10 @@ __device__ __forceinline__ float4 ldcg4(const float* p) {
     return __ldcg(reinterpret_cast<const float4*>(p));
 }
 
-// Symmetric INT8 code of x with scale s, as the low byte of a word.
-__device__ __forceinline__ uint32_t code_byte(float x, float s) {
-    return static_cast<uint32_t>(quant_code(x, s)) & 0xffu;
+// Four codes (ints in [-127, 127]) packed little-endian into one word.
+__device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d) {
+    return __byte_perm(__byte_perm(static_cast<uint32_t>(a), static_cast<uint32_t>(b), 0x0040),
+                       __byte_perm(static_cast<uint32_t>(c), static_cast<uint32_t>(d), 0x0040), 0x5410);
 }
 
 // INT8 base, column quads: the 16 bytes of quad (i4, c) hold key rows
@@ -51,17 +52,36 @@ __device__ __forceinline__ float4 quad_row(uint4 q, int r) {
 }
 
 // Codes of 4 rows x 4 columns (rows[r] = the 4 columns of row r, each row
-// with its own scale) packed as one column quad.
-__device__ __forceinline__ uint4 pack_quad(const float4 (&rows)[4], const float (&s)[4]) {
-    uint32_t w[4] = {0u, 0u, 0u, 0u};
+// with its own factor f[r]) packed as one column quad (word m = column m,
+// byte r = row r).
+__device__ __forceinline__ uint4 pack_quad(const float4 (&rows)[4], const float (&f)[4]) {
+    int z[4][4];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-        w[0] |= code_byte(rows[r].x, s[r]) << (8 * r);
-        w[1] |= code_byte(rows[r].y, s[r]) << (8 * r);
-        w[2] |= code_byte(rows[r].z, s[r]) << (8 * r);
-        w[3] |= code_byte(rows[r].w, s[r]) << (8 * r);
+        z[r][0] = quant_code(rows[r].x, f[r]);
+        z[r][1] = quant_code(rows[r].y, f[r]);
+        z[r][2] = quant_code(rows[r].z, f[r]);
+        z[r][3] = quant_code(rows[r].w, f[r]);
     }
-    return make_uint4(w[0], w[1], w[2], w[3]);
+    return make_uint4(pack4(z[0][0], z[1][0], z[2][0], z[3][0]), pack4(z[0][1], z[1][1], z[2][1], z[3][1]),
+                      pack4(z[0][2], z[1][2], z[2][2], z[3][2]), pack4(z[0][3], z[1][3], z[2][3], z[3][3]));
+}
+
+// Max over the 32 lanes of each of 16 per-lane values v[0..15] (one per key
+// row), by recursive halving: 16 shuffles instead of 80.  Lane l returns the
+// max of row (l >> 1) & 15.
+__device__ __forceinline__ float warp_max16_scatter(float (&v)[16], int lane) {
+#pragma unroll
+    for (int b = 4, h = 8; b >= 1; --b, h >>= 1) {
+        const bool upper = (lane >> b) & 1;
+#pragma unroll
+        for (int r = 0; r < h; ++r) {
+            const float send = upper ? v[r] : v[r + h];
+            const float keep = upper ? v[r + h] : v[r];
+            v[r] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 1 << b));
+        }
+    }
+    return fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], 1));
 }
 
 // Split x (|x| <= 2^30) into 4 signed base-256 digits, x = sum_d d_d 256^d,
@@ -105,19 +125,22 @@ struct FoldSmem {
     unsigned char* tile;  // tile_bytes(INT8)
     float2* a2;           // [kFoldChunk][kD] (a, a)
     float4* u4;           // [kFoldChunk][kD / 4]
+    float* es;            // [kD] exp(lb_i) (* s_i for INT8)
     uint64_t* bar;
 };
 
 __host__ __device__ constexpr size_t fold_smem_bytes(bool int8) {
-    return tile_bytes(int8) + size_t(kFoldChunk) * kD * 8 + size_t(kFoldChunk) * kD * 4 + 16;
+    return tile_bytes(int8) + size_t(kFoldChunk) * kD * 12 + kD * 4 + 16;
 }
 
 __device__ __forceinline__ FoldSmem fold_smem(unsigned char* base, bool int8) {
     FoldSmem f;
+    const size_t t = tile_bytes(int8);
     f.tile = base;
-    f.a2 = reinterpret_cast<float2*>(base + tile_bytes(int8));
-    f.u4 = reinterpret_cast<float4*>(base + tile_bytes(int8) + size_t(kFoldChunk) * kD * 8);
-    f.bar = reinterpret_cast<uint64_t*>(base + tile_bytes(int8) + size_t(kFoldChunk) * kD * 12);
+    f.a2 = reinterpret_cast<float2*>(base + t);
+    f.u4 = reinterpret_cast<float4*>(base + t + size_t(kFoldChunk) * kD * 8);
+    f.es = reinterpret_cast<float*>(base + t + size_t(kFoldChunk) * kD * 12);
+    f.bar = reinterpret_cast<uint64_t*>(base + t + size_t(kFoldChunk) * kD * 12 + kD * 4);
     return f;
 }
 
@@ -134,19 +157,15 @@ __device__ bool fold_cta(const PoolView& pv, size_t hd, int n, const float* lbg,
 #pragma unroll
         for (int i = 0; i < 4; ++i) bulk_g2s(fs.tile + i * kPart, src + i * kPart, kPart, fs.bar);
     }
-    // decay (and INT8 scale) of the thread's 16 key rows
+    // decay (and INT8 scale) of every key row, once per CTA (a scalar-gate
+    // FP32 fold needs one value only)
     const int i0 = 16 * warp;
-    float e[16];
-#pragma unroll
-    for (int r4 = 0; r4 < 4; ++r4) {
-        float4 lb4 = make_float4(lb_scalar, lb_scalar, lb_scalar, lb_scalar);
-        if constexpr (PER_KEY) lb4 = ldcg4(lbg + i0 + 4 * r4);
-        float4 s4 = make_float4(1.f, 1.f, 1.f, 1.f);
-        if constexpr (INT8) s4 = ldcg4(pv.scale + hd * kD + i0 + 4 * r4);
-        e[4 * r4 + 0] = expf(lb4.x) * s4.x;
-        e[4 * r4 + 1] = expf(lb4.y) * s4.y;
-        e[4 * r4 + 2] = expf(lb4.z) * s4.z;
-        e[4 * r4 + 3] = expf(lb4.w) * s4.w;
+    constexpr bool kRowFactors = INT8 || PER_KEY;
+    if (kRowFactors && tid < kD) {
+        const float lb = PER_KEY ? __ldcg(lbg + tid) : lb_scalar;
+        float ee = expf(lb);
+        if constexpr (INT8) ee *= __ldcg(pv.scale + hd * kD + tid);
+        fs.es[tid] = ee;
     }
     const bool ok = mbar_wait_bounded(fs.bar, phase);
     if (__syncthreads_or(!ok)) {
@@ -158,6 +177,21 @@ __device__ bool fold_cta(const PoolView& pv, size_t hd, int n, const float* lbg,
         return false;
     }
     // decayed, dequantized base rows; acc[r] = columns 4l..4l+3 of row i0 + r
+    float e[16];
+#pragma unroll
+    for (int r4 = 0; r4 < 4; ++r4) {
+        float4 v;
+        if constexpr (kRowFactors) {
+            v = reinterpret_cast<const float4*>(fs.es)[i0 / 4 + r4];
+        } else {
+            const float g = expf(lb_scalar);
+            v = make_float4(g, g, g, g);
+        }
+        e[4 * r4 + 0] = v.x;
+        e[4 * r4 + 1] = v.y;
+        e[4 * r4 + 2] = v.z;
+        e[4 * r4 + 3] = v.w;
+    }
     float2 lo[16], hi[16];
 #pragma unroll
     for (int qd = 0; qd < 4; ++qd) {
@@ -235,22 +269,26 @@ __device__ bool fold_cta(const PoolView& pv, size_t hd, int n, const float* lbg,
             st4(reinterpret_cast<float*>(pv.base) + hd * (kD * kD) + (i0 + r) * kD + 4 * lane,
                 make_float4(lo[r].x, lo[r].y, hi[r].x, hi[r].y));
     } else {
+        // per-row absmax over the 128 columns (warp-wide), one division pair
+        // per row in the lane that holds it, factors broadcast back
+        float mx[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+            mx[r] = fmaxf(fmaxf(fabsf(lo[r].x), fabsf(lo[r].y)), fmaxf(fabsf(hi[r].x), fabsf(hi[r].y)));
+        float s_mine, f_mine;
+        row_quant_params(warp_max16_scatter(mx, lane), s_mine, f_mine);
+        if ((lane & 1) == 0) pv.scale[hd * kD + i0 + (lane >> 1)] = s_mine;
 #pragma unroll
         for (int qd = 0; qd < 4; ++qd) {
-            float sc[4];
+            float f[4];
             float4 rows[4];
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const int row = 4 * qd + r;
+                f[r] = __shfl_sync(0xffffffffu, f_mine, 2 * row);
                 rows[r] = make_float4(lo[row].x, lo[row].y, hi[row].x, hi[row].y);
-                float mx = fmaxf(fmaxf(fabsf(rows[r].x), fabsf(rows[r].y)),
-                                 fmaxf(fabsf(rows[r].z), fabsf(rows[r].w)));
-                mx = warp_max(mx);
-                sc[r] = __fdiv_rn(mx, 127.0f);
             }
-            reinterpret_cast<uint4*>(pv.base)[quad_index(hd, i0 / 4 + qd, lane)] = pack_quad(rows, sc);
-            if (lane == 0)
-                st4(pv.scale + hd * kD + i0 + 4 * qd, make_float4(sc[0], sc[1], sc[2], sc[3]));
+            reinterpret_cast<uint4*>(pv.base)[quad_index(hd, i0 / 4 + qd, lane)] = pack_quad(rows, f);
         }
     }
     return true;

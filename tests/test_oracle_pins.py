@@ -243,8 +243,14 @@ def test_quantizer_bounds_and_idempotence(oracle_mod):
     assert Z.min() >= -127 and Z.max() <= 127
     Sf = S.astype(np.float32).astype(np.float64)
     deq = oracle_mod.dequantize_rows(Z, s)
-    bound = s.astype(np.float64)[..., None] * 0.5 * (1 + 2.0 ** -20) + np.abs(Sf) * 2.0 ** -22
+    # half a step, plus the FP32 rounding of the factor 127 / absmax and of the
+    # product (at most 128 * 2^-23 of a step) and of S itself
+    sd = s.astype(np.float64)[..., None]
+    bound = sd * (0.5 + 128 * 2.0 ** -22) + np.abs(Sf) * 2.0 ** -22
     assert np.all(np.abs(deq - Sf) <= bound)
+    # never more than half a step plus rounding: a wrong rounding direction
+    # would cost a whole step
+    assert np.all(np.abs(deq - Sf) <= 0.51 * sd + 1e-30)
     nz = np.abs(S).max(axis=-1) > 0
     assert np.all(np.abs(Z).max(axis=-1)[nz] == 127)
     assert s[1, 3] == 0 and np.all(Z[1, 3] == 0)
@@ -258,6 +264,16 @@ def test_quantizer_rounds_half_to_even(oracle_mod):
     Z, s = oracle_mod.quantize_rows(row[None, :])
     assert s[0] == 1.0
     assert list(Z[0]) == [127, 2, 4, -2, -4, 0, 2, 0, 126, 0]
+    # absmax 254: factor 127/254 = 0.5 exactly, so 5.0 -> 2.5 -> 2 and 7.0 -> 3.5 -> 4
+    Z, s = oracle_mod.quantize_rows(np.array([[254.0, 5.0, 7.0, -5.0, 1.0]]))
+    assert s[0] == np.float32(254.0) / np.float32(127.0)
+    assert list(Z[0]) == [127, 2, 4, -2, 0]
+
+
+def test_quantizer_degenerate_rows(oracle_mod):
+    tiny = np.float32(1e-38) / np.float32(1e4)  # subnormal: 127 / absmax overflows FP32
+    Z, s = oracle_mod.quantize_rows(np.array([[0.0, 0.0, 0.0], [tiny, -tiny, 0.0]]))
+    assert np.all(s == 0) and np.all(Z == 0)
 
 
 # --------------------------------------------------------------------------
