@@ -93,7 +93,8 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int prepare_all() {
     // Idempotent per device; cheap enough to repeat at every pool creation.
-    if (ls::prepare_step_kernels() != cudaSuccess) return LS_ERR_CUDA;
+    if (ls::prepare_eager_step_kernels() != cudaSuccess) return LS_ERR_CUDA;
+    if (ls::prepare_log_step_kernels() != cudaSuccess) return LS_ERR_CUDA;
     if (ls::prepare_fold_kernels() != cudaSuccess) return LS_ERR_CUDA;
     if (ls::prepare_aux_kernels() != cudaSuccess) return LS_ERR_CUDA;
     return LS_OK;

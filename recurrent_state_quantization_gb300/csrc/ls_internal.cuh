@@ -85,7 +85,8 @@ __host__ __device__ constexpr size_t eager_smem_bytes() {
 __host__ __device__ constexpr size_t transpose_smem_bytes() { return size_t(kD) * (kD + 1) * 4; }
 
 // ---- launchers (each in its own translation unit) -------------------------
-cudaError_t prepare_step_kernels();
+cudaError_t prepare_eager_step_kernels();
+cudaError_t prepare_log_step_kernels();
 cudaError_t prepare_fold_kernels();
 cudaError_t prepare_aux_kernels();
 
