@@ -90,7 +90,13 @@ __global__ void __launch_bounds__(kThreads) load_rows_kernel(const AuxArgs a) {
                 row_quant_params(mx, sc, f[m]);
                 if (lane == 0) pv.scale[hd * kD + 4 * i4 + m] = sc;
             }
-            reinterpret_cast<uint4*>(pv.base)[quad_index(hd, i4, lane)] = pack_quad(v, f);
+            float2 lo[4], hi[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                lo[m] = make_float2(v[m].x, v[m].y);
+                hi[m] = make_float2(v[m].z, v[m].w);
+            }
+            reinterpret_cast<uint4*>(pv.base)[quad_index(hd, i4, lane)] = pack_quad(lo, hi, 0, f);
         }
     }
     clear_log(pv, hd);

@@ -159,15 +159,6 @@ __device__ __forceinline__ void row_quant_params(float amax, float& s, float& f)
     }
 }
 
-// Symmetric INT8 code of x with factor f: round half to even, clamp to
-// [-127, 127].  f = 0 gives 0.
-__device__ __forceinline__ int quant_code(float x, float f) {
-    int z = __float2int_rn(x * f);
-    z = z > 127 ? 127 : z;
-    z = z < -127 ? -127 : z;
-    return z;
-}
-
 __device__ __forceinline__ void flag_status(int32_t* status, int32_t bit) {
     atomicOr(status, bit);
 }

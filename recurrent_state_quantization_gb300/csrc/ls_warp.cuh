@@ -29,10 +29,35 @@ __device__ __forceinline__ float4 ldcg4(const float* p) {
     return __ldcg(reinterpret_cast<const float4*>(p));
 }
 
-// Four codes (ints in [-127, 127]) packed little-endian into one word.
-__device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d) {
-    return __byte_perm(__byte_perm(static_cast<uint32_t>(a), static_cast<uint32_t>(b), 0x0040),
-                       __byte_perm(static_cast<uint32_t>(c), static_cast<uint32_t>(d), 0x0040), 0x5410);
+// Exact INT8 <-> FP32 conversions on the FMA and integer pipes.
+// Dequantize: a code n (two's complement byte) biased to u = n + 128 in
+// [1, 255] is the low mantissa byte of the FP32 number 2^23 + u; subtracting
+// 2^23 + 128 leaves n exactly.
+// Quantize: a product t = fl(x f) with |t| < 2^22, plus 1.5 * 2^23, rounds to
+// rint(t) (half to even) and leaves it in the low mantissa bits in two's
+// complement, so the low byte is the code.  With f = fl(127 / B) and |x| <= B
+// (B the row's absmax) |t| < 127.5, so no clamp is needed.
+constexpr float kCodeBias = 8388736.0f;     // 2^23 + 128
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
+
+// Byte r of two biased code words (word ^ 0x80808080) as exact FP32 codes.
+__device__ __forceinline__ float2 code_values(uint32_t wa, uint32_t wb, int r) {
+    const uint32_t sel = 0x7650u | static_cast<uint32_t>(r);
+    const float2 b = make_float2(__uint_as_float(__byte_perm(wa, 0x4B000000u, sel)),
+                                 __uint_as_float(__byte_perm(wb, 0x4B000000u, sel)));
+    return __fadd2_rn(b, make_float2(-kCodeBias, -kCodeBias));
+}
+
+// Codes of two values sharing the factor f, as FP32 words whose low byte is
+// the code.
+__device__ __forceinline__ float2 code_words(float2 x, float f) {
+    return __fadd2_rn(__fmul2_rn(x, make_float2(f, f)), make_float2(kRoundMagic, kRoundMagic));
+}
+
+// Low bytes of four words packed little-endian into one word.
+__device__ __forceinline__ uint32_t pack_low_bytes(float a, float b, float c, float d) {
+    return __byte_perm(__byte_perm(__float_as_uint(a), __float_as_uint(b), 0x0040),
+                       __byte_perm(__float_as_uint(c), __float_as_uint(d), 0x0040), 0x5410);
 }
 
 // INT8 base, column quads: the 16 bytes of quad (i4, c) hold key rows
@@ -42,29 +67,27 @@ __device__ __forceinline__ size_t quad_index(size_t hd, int i4, int c) {
     return hd * (kD * kD / 16) + static_cast<size_t>(i4) * (kD / 4) + c;
 }
 
-// Byte r of each of the 4 words of a quad -> the 4 columns of row r.
-__device__ __forceinline__ float4 quad_row(uint4 q, int r) {
-    const int sh = 8 * r;
-    return make_float4(static_cast<float>(static_cast<int8_t>((q.x >> sh) & 0xffu)),
-                       static_cast<float>(static_cast<int8_t>((q.y >> sh) & 0xffu)),
-                       static_cast<float>(static_cast<int8_t>((q.z >> sh) & 0xffu)),
-                       static_cast<float>(static_cast<int8_t>((q.w >> sh) & 0xffu)));
+// Row r of a quad, dequantized with the factor e: (columns 0, 1), (2, 3).
+__device__ __forceinline__ void quad_row(uint4 qb, int r, float e, float2& lo, float2& hi) {
+    const float2 ee = make_float2(e, e);
+    lo = __fmul2_rn(code_values(qb.x, qb.y, r), ee);
+    hi = __fmul2_rn(code_values(qb.z, qb.w, r), ee);
 }
 
-// Codes of 4 rows x 4 columns (rows[r] = the 4 columns of row r, each row
-// with its own factor f[r]) packed as one column quad (word m = column m,
-// byte r = row r).
-__device__ __forceinline__ uint4 pack_quad(const float4 (&rows)[4], const float (&f)[4]) {
-    int z[4][4];
+// Codes of rows r0..r0+3 x 4 columns (row r = (lo[r], hi[r]) = columns
+// 0..3, with its own factor f[r - r0]) packed as one column quad (word m =
+// column m, byte r - r0 = row r).
+template <int N>
+__device__ __forceinline__ uint4 pack_quad(const float2 (&lo)[N], const float2 (&hi)[N], int r0,
+                                           const float (&f)[4]) {
+    float2 a[4], b[4];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-        z[r][0] = quant_code(rows[r].x, f[r]);
-        z[r][1] = quant_code(rows[r].y, f[r]);
-        z[r][2] = quant_code(rows[r].z, f[r]);
-        z[r][3] = quant_code(rows[r].w, f[r]);
+        a[r] = code_words(lo[r0 + r], f[r]);
+        b[r] = code_words(hi[r0 + r], f[r]);
     }
-    return make_uint4(pack4(z[0][0], z[1][0], z[2][0], z[3][0]), pack4(z[0][1], z[1][1], z[2][1], z[3][1]),
-                      pack4(z[0][2], z[1][2], z[2][2], z[3][2]), pack4(z[0][3], z[1][3], z[2][3], z[3][3]));
+    return make_uint4(pack_low_bytes(a[0].x, a[1].x, a[2].x, a[3].x), pack_low_bytes(a[0].y, a[1].y, a[2].y, a[3].y),
+                      pack_low_bytes(b[0].x, b[1].x, b[2].x, b[3].x), pack_low_bytes(b[0].y, b[1].y, b[2].y, b[3].y));
 }
 
 // Max over the 32 lanes of each of 16 per-lane values v[0..15] (one per key
@@ -196,14 +219,13 @@ __device__ bool fold_cta(const PoolView& pv, size_t hd, int n, const float* lbg,
 #pragma unroll
     for (int qd = 0; qd < 4; ++qd) {
         if constexpr (INT8) {
-            const uint4 q = reinterpret_cast<const uint4*>(fs.tile)[(i0 / 4 + qd) * (kD / 4) + lane];
+            uint4 q = reinterpret_cast<const uint4*>(fs.tile)[(i0 / 4 + qd) * (kD / 4) + lane];
+            q.x ^= 0x80808080u;
+            q.y ^= 0x80808080u;
+            q.z ^= 0x80808080u;
+            q.w ^= 0x80808080u;
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const float4 z = quad_row(q, r);
-                const float ee = e[4 * qd + r];
-                lo[4 * qd + r] = make_float2(ee * z.x, ee * z.y);
-                hi[4 * qd + r] = make_float2(ee * z.z, ee * z.w);
-            }
+            for (int r = 0; r < 4; ++r) quad_row(q, r, e[4 * qd + r], lo[4 * qd + r], hi[4 * qd + r]);
         } else {
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
@@ -281,14 +303,9 @@ __device__ bool fold_cta(const PoolView& pv, size_t hd, int n, const float* lbg,
 #pragma unroll
         for (int qd = 0; qd < 4; ++qd) {
             float f[4];
-            float4 rows[4];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int row = 4 * qd + r;
-                f[r] = __shfl_sync(0xffffffffu, f_mine, 2 * row);
-                rows[r] = make_float4(lo[row].x, lo[row].y, hi[row].x, hi[row].y);
-            }
-            reinterpret_cast<uint4*>(pv.base)[quad_index(hd, i0 / 4 + qd, lane)] = pack_quad(rows, f);
+            for (int r = 0; r < 4; ++r) f[r] = __shfl_sync(0xffffffffu, f_mine, 2 * (4 * qd + r));
+            reinterpret_cast<uint4*>(pv.base)[quad_index(hd, i0 / 4 + qd, lane)] = pack_quad(lo, hi, 4 * qd, f);
         }
     }
     return true;
