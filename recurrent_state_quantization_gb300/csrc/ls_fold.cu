@@ -40,16 +40,19 @@ __global__ void __launch_bounds__(kThreads, 2) fold_kernel(const AuxArgs a) {
     const FoldSmem fs = fold_smem(smem, INT8);
     if (threadIdx.x == 0) {
         mbar_init(fs.bar, 1);
+        mbar_init(fs.lbar, 1);
         mbar_fence_init();
     }
     __syncthreads();
-    // per-key gate: lbar is read row by row from global memory (it is reset
-    // only after the fold); scalar gate: one value
+    // per-key gate: lbar is read row by row from global memory by the fold
+    // (it is reset only after the fold); scalar gate: one value
     const float lb = PER_KEY ? 0.0f : pv.lbar[hd];
     float* out = nullptr;
     if constexpr (MODE == kFoldRead) out = a.state_out + (static_cast<size_t>(n) * H + h) * (kD * kD);
+    const TokenIn none{nullptr, nullptr, nullptr, nullptr, 0.0f, nullptr, 0};
+    FoldPipe pp;
     const bool ok = fold_cta<INT8, PER_KEY, MODE>(pv, hd, L, pv.lbar + hd * (PER_KEY ? kD : 1), lb,
-                                                  out, fs, 0u);
+                                                  out, fs, pp, none, -1, 0);
     if (MODE == kFoldCommit && ok) {
         __syncthreads();  // every reader of lbar is done
         if (PER_KEY) {

@@ -62,7 +62,8 @@ struct WarpSmem {
     uint32_t pad;
 };
 static_assert(sizeof(WarpSmem) % 16 == 0, "per-warp shared block must keep 16-byte alignment");
-static_assert(kWarps * sizeof(WarpSmem) >= fold_smem_bytes(false),
+static_assert(kWarps * sizeof(WarpSmem) >= fold_smem_bytes(false) &&
+                  kWarps * sizeof(WarpSmem) >= fold_smem_bytes(true),
               "the window-end fold reuses the rings as staging");
 
 constexpr size_t step_smem_bytes() { return kWarps * sizeof(WarpSmem); }
@@ -119,9 +120,16 @@ __device__ __forceinline__ void issue_item(WarpSmem& ws, const StepArgs& a, int 
     }
 }
 
-// One warp decodes one (request, head).  Returns the state index hd when this
-// token closed the head's window (its W entries still have to be folded into
-// the base), -1 otherwise; *lp_out receives the scalar-gate log-decay.
+// One warp decodes one (request, head) and returns -1, or the state index hd
+// when the token closes the head's window (L + 1 == W) and the CTA has work
+// left on it:
+//   FP32 base: the warp leaves the token to the CTA, which decodes it in one
+//     pass over the state (the fold's kFoldStep); *lp_out = lbar + lambda;
+//   INT8 base: the warp decodes and appends it like any other token, and the
+//     CTA folds the W entries into the base and requantizes; *lp_out = lbar
+//     after the token.  The base and log the CTA re-reads were just streamed
+//     by the warp and are mostly still in L2, while the per-warp GEMV keeps
+//     the integer arithmetic of every other token.
 template <bool INT8, bool PER_KEY>
 __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, int row,
                                                float* lp_out) {
@@ -145,6 +153,10 @@ __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, 
         if (lane == 0) flag_status(pv.status, kDevBadState);
         st4(a.y + ro, nan4);
         return -1;
+    }
+    if (!INT8 && L + 1 == W) {
+        if constexpr (!PER_KEY) *lp_out = pv.lbar[hd] + __ldg(a.lam + row);
+        return static_cast<long long>(hd);
     }
     const int NI = 1 + P::NT + (L + P::EPC - 1) / P::EPC;
     if (lane == 0) {
@@ -283,11 +295,11 @@ __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, 
                 }
             } else {
 #pragma unroll
-                for (int g = 0; g < P::ROWS / 4; ++g) {
+                for (int gr = 0; gr < P::ROWS / 4; ++gr) {
 #pragma unroll
                     for (int m = 0; m < 4; ++m) {
-                        const float4 v = st4p[(4 * g + m) * 32 + lane];
-                        const float4 x = ws.xkq[row0 + 4 * g + m];  // (xk, xk, xq, xq)
+                        const float4 v = st4p[(4 * gr + m) * 32 + lane];
+                        const float4 x = ws.xkq[row0 + 4 * gr + m];  // (xk, xk, xq, xq)
                         const float2 xk = make_float2(x.x, x.y), xq = make_float2(x.z, x.w);
                         const float2 v01 = make_float2(v.x, v.y), v23 = make_float2(v.z, v.w);
                         r01 = __ffma2_rn(v01, xk, r01);
@@ -334,9 +346,9 @@ __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, 
 
     // ---- append entry L -------------------------------------------------------
     {
-        const size_t eo = (hd * static_cast<size_t>(W) + L) * kD + 4 * lane;
-        st4(pv.klog + eo, k4);
-        st4(pv.ulog + eo, u4);
+        const size_t eo = (hd * static_cast<size_t>(W) + L) * kD;
+        st4(pv.klog + eo + 4 * lane, k4);
+        st4(pv.ulog + eo + 4 * lane, u4);
         const size_t lb0 = hd * static_cast<size_t>(pv.lam_stride);
         if constexpr (PER_KEY) st4(pv.lamlog + lb0 + static_cast<size_t>(L) * kD + 4 * lane, lp4);
         else if (lane == 0) pv.lamlog[lb0 + L] = lp4.x;
@@ -348,7 +360,7 @@ __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, 
         return -1;
     }
     *lp_out = lp4.x;
-    return static_cast<long long>(hd);  // window end: the CTA folds the W entries
+    return static_cast<long long>(hd);  // INT8 window end: the CTA folds the W entries
 }
 
 template <bool INT8, bool PER_KEY>
@@ -369,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 2) log_step_kernel(const StepArgs a)
         fold_hd[warp] = hd;
         fold_lb[warp] = lp;
     }
-    // ---- window ends: the whole CTA folds each closed window in turn ----------
+    // ---- window ends: the whole CTA decodes each closing head in turn ----------
     // (the ring memory is free now and becomes the fold's staging area)
     if (!__syncthreads_or(hd >= 0)) return;
     if (lane == 0 && ws.bar_live) {
@@ -380,18 +392,30 @@ __global__ void __launch_bounds__(kThreads, 2) log_step_kernel(const StepArgs a)
     const FoldSmem fs = fold_smem(smem, INT8);
     if (threadIdx.x == 0) {
         mbar_init(fs.bar, 1);
+        mbar_init(fs.lbar, 1);
         mbar_fence_init();
     }
     __syncthreads();
-    uint32_t phase = 0;
+    FoldPipe pp;
+    bool ok = true;
     for (int w = 0; w < kWarps; ++w) {
         const long long h = fold_hd[w];
         if (h < 0) continue;
+        const int r = blockIdx.x * kWarps + w;
         const size_t st = static_cast<size_t>(h);
-        const bool ok = fold_cta<INT8, PER_KEY, kFoldCommit>(pv, st, pv.W, pv.lbar + st * (PER_KEY ? kD : 1),
-                                                             fold_lb[w], nullptr, fs, phase);
-        phase ^= 1u;
-        __syncthreads();  // every reader of lbar is done
+        if (ok) {
+            long long next = -1;
+            for (int w2 = w + 1; w2 < kWarps && next < 0; ++w2) next = fold_hd[w2];
+            const TokenIn tok{a.k, a.q, a.v, a.lam, __ldg(a.beta + r), a.y, static_cast<size_t>(r) * kD};
+            const float* lbg = pv.lbar + st * (PER_KEY ? kD : 1);
+            if constexpr (INT8)
+                ok = fold_cta<INT8, PER_KEY, kFoldCommit>(pv, st, pv.W, lbg, fold_lb[w], nullptr, fs, pp, tok,
+                                                          next, pv.W);
+            else
+                ok = fold_cta<INT8, PER_KEY, kFoldStep>(pv, st, pv.W - 1, lbg, fold_lb[w], nullptr, fs, pp,
+                                                        tok, next, pv.W - 1);
+            __syncthreads();  // every reader of lbar is done
+        }
         if (ok) {
             if (PER_KEY) {
                 if (threadIdx.x < kD / 4) st4(pv.lbar + st * kD + 4 * threadIdx.x, make_float4(0.f, 0.f, 0.f, 0.f));
@@ -399,8 +423,8 @@ __global__ void __launch_bounds__(kThreads, 2) log_step_kernel(const StepArgs a)
                 pv.lbar[st] = 0.0f;
             }
             if (threadIdx.x == 0) pv.len[st] = 0;
-        } else {
-            break;
+        } else if (!INT8 && threadIdx.x < kD) {  // after a copy timeout (flagged): no output
+            a.y[static_cast<size_t>(r) * kD + threadIdx.x] = __int_as_float(0x7fc00000);
         }
     }
 }

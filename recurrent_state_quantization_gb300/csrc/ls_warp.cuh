@@ -62,9 +62,11 @@ __device__ __forceinline__ uint32_t pack_low_bytes(float a, float b, float c, fl
 
 // INT8 base, column quads: the 16 bytes of quad (i4, c) hold key rows
 // 4*i4..4*i4+3 of value columns 4*c..4*c+3; word m is column 4*c + m and its
-// byte r is row 4*i4 + r.  quad_index addresses the quad in 16-byte units.
+// byte r is row 4*i4 + r.  quad_slot / quad_index address the quad in 16-byte
+// units.
+__host__ __device__ __forceinline__ int quad_slot(int i4, int c) { return i4 * (kD / 4) + c; }
 __device__ __forceinline__ size_t quad_index(size_t hd, int i4, int c) {
-    return hd * (kD * kD / 16) + static_cast<size_t>(i4) * (kD / 4) + c;
+    return hd * (kD * kD / 16) + static_cast<size_t>(quad_slot(i4, c));
 }
 
 // Row r of a quad, dequantized with the factor e: (columns 0, 1), (2, 3).
@@ -119,7 +121,19 @@ __device__ __forceinline__ void digits4(int x, int (&out)[4]) {
     out[3] = x;
 }
 
-enum FoldMode : int { kFoldCommit = 0, kFoldRead = 1 };
+enum FoldMode : int { kFoldCommit = 0, kFoldRead = 1, kFoldStep = 2 };
+
+// The current token of one (request, head) for kFoldStep: k, q, v, lambda at
+// ro = row * 128 (lambda: per-key gate only), beta, and the output row.
+struct TokenIn {
+    const float* k;
+    const float* q;
+    const float* v;
+    const float* lam;
+    float beta;
+    float* y;
+    size_t ro;
+};
 
 // ---------------------------------------------------------------------------
 // CTA-cooperative fold of one state (256 threads).
@@ -132,73 +146,180 @@ enum FoldMode : int { kFoldCommit = 0, kFoldRead = 1 };
 // is folded at: per key row at lbg (per-key gate; GLOBAL memory, read through
 // L2 because the caller may just have written it) or lb_scalar.
 //   kFoldCommit: deferred -> S is the new FP32 base;  INT8 -> per key row
-//     s_i = max_j |S_ij| / 127, codes rint(S / s_i) clamped to [-127, 127]
+//     B_i = max_j |S_ij|, s_i = B_i / 127, codes rint(S_ij * (127 / B_i))
 //     ("LeapQuant: Efficient Linear Attention with Accurate Recurrent State
 //     Quantization", §3.2 eq. 4, App. B.3) -- written in place;
-//   kFoldRead: S is written to out ([d_k][d_v]) and the pool is unchanged.
+//   kFoldRead: S is written to out ([d_k][d_v]) and the pool is unchanged;
+//   kFoldStep: the token that closes the window, in one pass over the state.
+//     lb = lbar + lambda (lambda per key row from tok.lam, or already in
+//     lb_scalar), so S = Diag(alpha) S_{t-1} with S_{t-1} the logical state
+//     of the n = W - 1 stored entries.  Then r = S^T k, y0 = S^T q,
+//     u = beta (v - r), y = y0 + (k.q) u (LeapQuant App. A; y from the
+//     unquantized state), S += k u^T, and S is committed as in kFoldCommit:
+//     the merge of DeltaLog eq. 6 and the window end of LeapQuant eq. 4
+//     without writing the current token to the log.
 // Work split: warp w owns key rows 16w..16w+15 (so a row's absmax is a warp
 // reduction), lane l value columns 4l..4l+3; 64 FP32 accumulators per
 // thread.  The base tile is staged by bulk asynchronous copies, the log in
 // chunks of kFoldChunk entries with (a, a) pairs a = exp(lb - Lam) K for the
-// paired FMAs.  Returns false after a copy timeout (flagged).
+// paired FMAs.  Returns false after a copy timeout (flagged; nothing of this
+// call is left in flight).
 // ---------------------------------------------------------------------------
 constexpr int kFoldChunk = 16;
 
 struct FoldSmem {
     unsigned char* tile;  // tile_bytes(INT8)
-    float2* a2;           // [kFoldChunk][kD] (a, a)
+    float2* a2;           // [kFoldChunk][kD] (a, a); kFoldStep: then partial sums
     float4* u4;           // [kFoldChunk][kD / 4]
     float* es;            // [kD] exp(lb_i) (* s_i for INT8)
-    uint64_t* bar;
+    float* lp;            // [kD] lb_i (per-key gate)
+    float* kv;            // [kD] k, q, v, u of the token (kFoldStep)
+    float* qv;
+    float* vv;
+    float* uv;
+    float* misc;          // [4] partial k.q
+    float4* rk;           // INT8: raw log chunk K [kFoldChunk][kD], U, Lambda
+    float4* ru;           //   (per key row, or kFoldChunk scalars)
+    float4* rl;
+    uint64_t* bar;        // tile copies
+    uint64_t* lbar;       // INT8: log chunk copies
 };
 
+// INT8 stages its log chunks by bulk copies too (room for them next to the
+// 16 KiB tile); FP32 loads them per thread.
+__host__ __device__ constexpr size_t fold_raw_bytes(bool int8) {
+    return int8 ? size_t(3) * kFoldChunk * kD * 4 : 0;
+}
+
 __host__ __device__ constexpr size_t fold_smem_bytes(bool int8) {
-    return tile_bytes(int8) + size_t(kFoldChunk) * kD * 12 + kD * 4 + 16;
+    return tile_bytes(int8) + size_t(kFoldChunk) * kD * 12 + 6 * kD * 4 + 16 + fold_raw_bytes(int8) + 16;
 }
 
 __device__ __forceinline__ FoldSmem fold_smem(unsigned char* base, bool int8) {
     FoldSmem f;
-    const size_t t = tile_bytes(int8);
-    f.tile = base;
-    f.a2 = reinterpret_cast<float2*>(base + t);
-    f.u4 = reinterpret_cast<float4*>(base + t + size_t(kFoldChunk) * kD * 8);
-    f.es = reinterpret_cast<float*>(base + t + size_t(kFoldChunk) * kD * 12);
-    f.bar = reinterpret_cast<uint64_t*>(base + t + size_t(kFoldChunk) * kD * 12 + kD * 4);
+    unsigned char* p = base;
+    f.tile = p;
+    p += tile_bytes(int8);
+    f.a2 = reinterpret_cast<float2*>(p);
+    p += size_t(kFoldChunk) * kD * 8;
+    f.u4 = reinterpret_cast<float4*>(p);
+    p += size_t(kFoldChunk) * kD * 4;
+    float* v = reinterpret_cast<float*>(p);
+    f.es = v;
+    f.lp = v + kD;
+    f.kv = v + 2 * kD;
+    f.qv = v + 3 * kD;
+    f.vv = v + 4 * kD;
+    f.uv = v + 5 * kD;
+    f.misc = v + 6 * kD;
+    p = reinterpret_cast<unsigned char*>(v + 6 * kD + 4);
+    f.rk = reinterpret_cast<float4*>(p);
+    f.ru = f.rk + kFoldChunk * (kD / 4);
+    f.rl = f.ru + kFoldChunk * (kD / 4);
+    p += fold_raw_bytes(int8);
+    f.bar = reinterpret_cast<uint64_t*>(p);
+    f.lbar = f.bar + 1;
     return f;
 }
 
-template <bool INT8, bool PER_KEY, int MODE>
-__device__ bool fold_cta(const PoolView& pv, size_t hd, int n, const float* lbg, float lb_scalar,
-                         float* out, const FoldSmem& fs, uint32_t phase) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// Copy state of the fold's two staging pipelines across the states a CTA
+// folds in turn: the completed phases of the tile and log barriers, and
+// whether the next state's tile / first log chunk is already in flight.
+struct FoldPipe {
+    uint32_t tile_phase = 0;
+    uint32_t log_phase = 0;
+    bool tile_issued = false;
+    bool log_issued = false;
+};
+
+// Stage the base tile of state hd into fs.tile (thread 0 only); completes
+// one phase of fs.bar.
+template <bool INT8>
+__device__ __forceinline__ void fold_issue_tile(const PoolView& pv, size_t hd, const FoldSmem& fs) {
     constexpr uint32_t kTile = static_cast<uint32_t>(tile_bytes(INT8));
     constexpr uint32_t kPart = kTile / 4;
-    if (tid == 0) {
-        const unsigned char* src = reinterpret_cast<const unsigned char*>(pv.base) + hd * kTile;
-        fence_proxy_async();  // the staging area was last used by generic loads and stores
-        mbar_arrive_expect_tx(fs.bar, kTile);
+    const unsigned char* src = reinterpret_cast<const unsigned char*>(pv.base) + hd * kTile;
+    fence_proxy_async();  // the staging area was last used by generic loads and stores
+    mbar_arrive_expect_tx(fs.bar, kTile);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) bulk_g2s(fs.tile + i * kPart, src + i * kPart, kPart, fs.bar);
+    for (int i = 0; i < 4; ++i) bulk_g2s(fs.tile + i * kPart, src + i * kPart, kPart, fs.bar);
+}
+
+// Stage log entries c0 .. c0 + nl - 1 (nl <= kFoldChunk, c0 a multiple of
+// kFoldChunk) of state hd into the raw area (thread 0 only, INT8); completes
+// one phase of fs.lbar.  Scalar-gate snapshots are copied in whole 16-byte
+// groups; the padded snapshot stride keeps them inside the state's row.
+template <bool PER_KEY>
+__device__ __forceinline__ void fold_issue_log(const PoolView& pv, size_t hd, int c0, int nl,
+                                               const FoldSmem& fs) {
+    const size_t eo = (hd * static_cast<size_t>(pv.W) + c0) * kD;
+    const uint32_t part = static_cast<uint32_t>(nl) * kVecBytes;
+    const size_t lb0 = hd * static_cast<size_t>(pv.lam_stride);
+    const uint32_t lam_bytes = PER_KEY ? part : static_cast<uint32_t>((nl + 3) / 4 * 16);
+    fence_proxy_async();
+    mbar_arrive_expect_tx(fs.lbar, 2 * part + lam_bytes);
+    bulk_g2s(fs.rk, pv.klog + eo, part, fs.lbar);
+    bulk_g2s(fs.ru, pv.ulog + eo, part, fs.lbar);
+    if constexpr (PER_KEY)
+        bulk_g2s(fs.rl, pv.lamlog + lb0 + static_cast<size_t>(c0) * kD, part, fs.lbar);
+    else
+        bulk_g2s(fs.rl, pv.lamlog + lb0 + c0, lam_bytes, fs.lbar);
+}
+
+// pp: the pipelines' state (see FoldPipe).  next_hd >= 0: once this state's
+// tile is in registers the tile of next_hd is staged, and (INT8) once its
+// last log chunk is staged the first next_n log entries of next_hd, so their
+// latency hides behind this fold.
+template <bool INT8, bool PER_KEY, int MODE>
+__device__ bool fold_cta(const PoolView& pv, size_t hd, int n, const float* lbg, float lb_scalar,
+                         float* out, const FoldSmem& fs, FoldPipe& pp, const TokenIn& tok,
+                         long long next_hd, int next_n) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) {
+        if (!pp.tile_issued) fold_issue_tile<INT8>(pv, hd, fs);
+        if constexpr (INT8) {
+            if (!pp.log_issued && n > 0) fold_issue_log<PER_KEY>(pv, hd, 0, min(kFoldChunk, n), fs);
+        }
     }
+    pp.tile_issued = false;
+    const bool log_in_flight = INT8 && n > 0;  // this state's first chunk
+    pp.log_issued = false;
     // decay (and INT8 scale) of every key row, once per CTA (a scalar-gate
-    // FP32 fold needs one value only)
+    // FP32 fold needs one value only); the token's vectors for kFoldStep
     const int i0 = 16 * warp;
     constexpr bool kRowFactors = INT8 || PER_KEY;
-    if (kRowFactors && tid < kD) {
-        const float lb = PER_KEY ? __ldcg(lbg + tid) : lb_scalar;
-        float ee = expf(lb);
-        if constexpr (INT8) ee *= __ldcg(pv.scale + hd * kD + tid);
-        fs.es[tid] = ee;
+    if (tid < kD) {
+        float lb = lb_scalar;
+        if constexpr (PER_KEY) {
+            lb = __ldcg(lbg + tid);
+            if constexpr (MODE == kFoldStep) lb += __ldg(tok.lam + tok.ro + tid);
+            fs.lp[tid] = lb;
+        }
+        if constexpr (kRowFactors) {
+            float ee = expf(lb);
+            if constexpr (INT8) ee *= __ldcg(pv.scale + hd * kD + tid);
+            fs.es[tid] = ee;
+        }
+        if constexpr (MODE == kFoldStep) {
+            const float ki = __ldg(tok.k + tok.ro + tid), qi = __ldg(tok.q + tok.ro + tid);
+            fs.kv[tid] = ki;
+            fs.qv[tid] = qi;
+            fs.vv[tid] = __ldg(tok.v + tok.ro + tid);
+            const float kq = warp_sum(ki * qi);
+            if (lane == 0) fs.misc[warp] = kq;
+        }
     }
-    const bool ok = mbar_wait_bounded(fs.bar, phase);
+    const bool ok = mbar_wait_bounded(fs.bar, pp.tile_phase);
     if (__syncthreads_or(!ok)) {
         if (tid == 0) {
             flag_status(pv.status, kDevTimeout);
-            mbar_wait_bounded(fs.bar, phase);
+            mbar_wait_bounded(fs.bar, pp.tile_phase);
+            if (log_in_flight) mbar_wait_bounded(fs.lbar, pp.log_phase);
         }
         __syncthreads();
         return false;
     }
+    pp.tile_phase ^= 1u;
     // decayed, dequantized base rows; acc[r] = columns 4l..4l+3 of row i0 + r
     float e[16];
 #pragma unroll
@@ -219,7 +340,7 @@ __device__ bool fold_cta(const PoolView& pv, size_t hd, int n, const float* lbg,
 #pragma unroll
     for (int qd = 0; qd < 4; ++qd) {
         if constexpr (INT8) {
-            uint4 q = reinterpret_cast<const uint4*>(fs.tile)[(i0 / 4 + qd) * (kD / 4) + lane];
+            uint4 q = reinterpret_cast<const uint4*>(fs.tile)[quad_slot(i0 / 4 + qd, lane)];
             q.x ^= 0x80808080u;
             q.y ^= 0x80808080u;
             q.z ^= 0x80808080u;
@@ -236,6 +357,11 @@ __device__ bool fold_cta(const PoolView& pv, size_t hd, int n, const float* lbg,
             }
         }
     }
+    if (next_hd >= 0) {
+        __syncthreads();  // the tile is in registers
+        if (tid == 0) fold_issue_tile<INT8>(pv, static_cast<size_t>(next_hd), fs);
+        pp.tile_issued = true;
+    }
     // + sum_l exp(lb - Lam_l) K_l U_l^T, kFoldChunk entries at a time
     const size_t kb = hd * static_cast<size_t>(pv.W);
     const size_t lb0 = hd * static_cast<size_t>(pv.lam_stride);
@@ -243,27 +369,73 @@ __device__ bool fold_cta(const PoolView& pv, size_t hd, int n, const float* lbg,
     for (int c0 = 0; c0 < n; c0 += kFoldChunk) {
         const int nl = min(kFoldChunk, n - c0);
         __syncthreads();  // the previous chunk is consumed
-        for (int idx = tid; idx < nl * (kD / 4); idx += kThreads) {
-            const int l = idx >> 5, q = idx & 31;  // entry, 4-row / 4-column group
-            const size_t eo = (kb + c0 + l) * kD + 4 * q;
-            const float4 K4 = ldcg4(pv.klog + eo);
-            fs.u4[l * (kD / 4) + q] = ldcg4(pv.ulog + eo);
-            float4 g;
-            if constexpr (PER_KEY) {
-                const float4 lm = ldcg4(pv.lamlog + lb0 + static_cast<size_t>(c0 + l) * kD + 4 * q);
-                const float4 lb4 = ldcg4(lbg + 4 * q);
-                g = make_float4(expf(lb4.x - lm.x), expf(lb4.y - lm.y), expf(lb4.z - lm.z),
-                                expf(lb4.w - lm.w));
-            } else {
-                const float gg = expf(lb_scalar - __ldcg(pv.lamlog + lb0 + c0 + l));
-                g = make_float4(gg, gg, gg, gg);
+        if constexpr (INT8) {
+            // raw chunk (bulk copies) -> (a, a) pairs and U; then the next
+            // chunk, or the next state's first one, is staged behind it
+            const bool lok = mbar_wait_bounded(fs.lbar, pp.log_phase);
+            if (__syncthreads_or(!lok)) {
+                if (tid == 0) {
+                    flag_status(pv.status, kDevTimeout);
+                    mbar_wait_bounded(fs.lbar, pp.log_phase);
+                    if (pp.tile_issued) mbar_wait_bounded(fs.bar, pp.tile_phase);
+                }
+                __syncthreads();
+                pp.tile_issued = false;
+                return false;
             }
-            float4* a2 = reinterpret_cast<float4*>(fs.a2 + l * kD + 4 * q);
-            const float ax = g.x * K4.x, ay = g.y * K4.y, az = g.z * K4.z, aw = g.w * K4.w;
-            a2[0] = make_float4(ax, ax, ay, ay);
-            a2[1] = make_float4(az, az, aw, aw);
+            pp.log_phase ^= 1u;
+            for (int idx = tid; idx < nl * (kD / 4); idx += kThreads) {
+                const int l = idx >> 5, q = idx & 31;  // entry, 4-row / 4-column group
+                const float4 K4 = fs.rk[idx];
+                fs.u4[idx] = fs.ru[idx];
+                float4 g;
+                if constexpr (PER_KEY) {
+                    const float4 lm = fs.rl[idx];
+                    const float4 lb4 = reinterpret_cast<const float4*>(fs.lp)[q];
+                    g = make_float4(expf(lb4.x - lm.x), expf(lb4.y - lm.y), expf(lb4.z - lm.z),
+                                    expf(lb4.w - lm.w));
+                } else {
+                    const float gg = expf(lb_scalar - reinterpret_cast<const float*>(fs.rl)[l]);
+                    g = make_float4(gg, gg, gg, gg);
+                }
+                float4* a2 = reinterpret_cast<float4*>(fs.a2 + l * kD + 4 * q);
+                const float ax = g.x * K4.x, ay = g.y * K4.y, az = g.z * K4.z, aw = g.w * K4.w;
+                a2[0] = make_float4(ax, ax, ay, ay);
+                a2[1] = make_float4(az, az, aw, aw);
+            }
+            __syncthreads();
+            const bool more = c0 + kFoldChunk < n;
+            const bool next = !more && next_hd >= 0 && next_n > 0;
+            if (tid == 0) {
+                if (more)
+                    fold_issue_log<PER_KEY>(pv, hd, c0 + kFoldChunk, min(kFoldChunk, n - c0 - kFoldChunk), fs);
+                else if (next)
+                    fold_issue_log<PER_KEY>(pv, static_cast<size_t>(next_hd), 0, min(kFoldChunk, next_n), fs);
+            }
+            pp.log_issued = next;
+        } else {
+            for (int idx = tid; idx < nl * (kD / 4); idx += kThreads) {
+                const int l = idx >> 5, q = idx & 31;  // entry, 4-row / 4-column group
+                const size_t eo = (kb + c0 + l) * kD + 4 * q;
+                const float4 K4 = ldcg4(pv.klog + eo);
+                fs.u4[l * (kD / 4) + q] = ldcg4(pv.ulog + eo);
+                float4 g;
+                if constexpr (PER_KEY) {
+                    const float4 lm = ldcg4(pv.lamlog + lb0 + static_cast<size_t>(c0 + l) * kD + 4 * q);
+                    const float4 lb4 = reinterpret_cast<const float4*>(fs.lp)[q];
+                    g = make_float4(expf(lb4.x - lm.x), expf(lb4.y - lm.y), expf(lb4.z - lm.z),
+                                    expf(lb4.w - lm.w));
+                } else {
+                    const float gg = expf(lb_scalar - __ldcg(pv.lamlog + lb0 + c0 + l));
+                    g = make_float4(gg, gg, gg, gg);
+                }
+                float4* a2 = reinterpret_cast<float4*>(fs.a2 + l * kD + 4 * q);
+                const float ax = g.x * K4.x, ay = g.y * K4.y, az = g.z * K4.z, aw = g.w * K4.w;
+                a2[0] = make_float4(ax, ax, ay, ay);
+                a2[1] = make_float4(az, az, aw, aw);
+            }
+            __syncthreads();
         }
-        __syncthreads();
 #pragma unroll 2
         for (int l = 0; l < nl; ++l) {
             const float4 u = fs.u4[l * (kD / 4) + lane];
@@ -277,6 +449,60 @@ __device__ bool fold_cta(const PoolView& pv, size_t hd, int n, const float* lbg,
                 hi[2 * r2] = __ffma2_rn(a0, u23, hi[2 * r2]);
                 lo[2 * r2 + 1] = __ffma2_rn(a1, u01, lo[2 * r2 + 1]);
                 hi[2 * r2 + 1] = __ffma2_rn(a1, u23, hi[2 * r2 + 1]);
+            }
+        }
+    }
+    if constexpr (MODE == kFoldStep) {
+        // r = S^T k and y0 = S^T q: per-thread partials over its 16 rows,
+        // summed over the 8 warps in shared memory (the staged chunks are
+        // consumed; their area holds the partials)
+        __syncthreads();
+        float2 pk01 = make_float2(0.f, 0.f), pk23 = pk01, pq01 = pk01, pq23 = pk01;
+#pragma unroll
+        for (int r4 = 0; r4 < 4; ++r4) {
+            const float4 k4 = reinterpret_cast<const float4*>(fs.kv)[i0 / 4 + r4];
+            const float4 q4 = reinterpret_cast<const float4*>(fs.qv)[i0 / 4 + r4];
+            const float kk[4] = {k4.x, k4.y, k4.z, k4.w}, qq[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int row = 4 * r4 + r;
+                const float2 k2 = make_float2(kk[r], kk[r]), q2 = make_float2(qq[r], qq[r]);
+                pk01 = __ffma2_rn(lo[row], k2, pk01);
+                pk23 = __ffma2_rn(hi[row], k2, pk23);
+                pq01 = __ffma2_rn(lo[row], q2, pq01);
+                pq23 = __ffma2_rn(hi[row], q2, pq23);
+            }
+        }
+        float4* red = reinterpret_cast<float4*>(fs.a2);  // [2][8 warps][128 columns]
+        red[warp * 32 + lane] = make_float4(pk01.x, pk01.y, pk23.x, pk23.y);
+        red[(kWarps + warp) * 32 + lane] = make_float4(pq01.x, pq01.y, pq23.x, pq23.y);
+        __syncthreads();
+        if (tid < kD) {
+            const float* rf = reinterpret_cast<const float*>(fs.a2);
+            float r = 0.0f, y0 = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                r += rf[w * kD + tid];
+                y0 += rf[(kWarps + w) * kD + tid];
+            }
+            const float kq = (fs.misc[0] + fs.misc[1]) + (fs.misc[2] + fs.misc[3]);
+            const float u = tok.beta * (fs.vv[tid] - r);
+            fs.uv[tid] = u;
+            tok.y[tok.ro + tid] = fmaf(kq, u, y0);
+        }
+        __syncthreads();
+        // S += k u^T
+        const float4 u = reinterpret_cast<const float4*>(fs.uv)[lane];
+        const float2 u01 = make_float2(u.x, u.y), u23 = make_float2(u.z, u.w);
+#pragma unroll
+        for (int r4 = 0; r4 < 4; ++r4) {
+            const float4 k4 = reinterpret_cast<const float4*>(fs.kv)[i0 / 4 + r4];
+            const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const float2 k2 = make_float2(kk[r], kk[r]);
+                lo[4 * r4 + r] = __ffma2_rn(k2, u01, lo[4 * r4 + r]);
+                hi[4 * r4 + r] = __ffma2_rn(k2, u23, hi[4 * r4 + r]);
             }
         }
     }
