@@ -65,6 +65,29 @@ def dist_setup(args):
     return rank, world, local
 
 
+def barrier(world: int) -> None:
+    """Barrier over the ranks (no-op on one rank)."""
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(value: float, world: int, device) -> float:
+    """Max of a per-rank scalar over all ranks (the timed interval)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: int, world: int, max_ms: float) -> float:
+    """Whole-job rate: the units every rank processed over the slowest rank's time."""
+    return units_per_rank * world / (max_ms * 1e-3)
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -222,8 +245,7 @@ def run_native(args, rank, world, local):
     for t in range(args.warmup):
         one_step(t)
     torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
+    barrier(world)
     torch.cuda.synchronize()
 
     clocks = Clocks(local)
@@ -238,14 +260,9 @@ def run_native(args, rank, world, local):
     stop.record(stream)
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
+    barrier(world)
     clk = clocks.stop()
-    elapsed_ms = start.elapsed_time(stop)
-    if world > 1:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = reduce_max(start.elapsed_time(stop), world, dev)
 
     hbm_peak, peak_kind = peaks()
     per_variant = {}
@@ -258,8 +275,7 @@ def run_native(args, rank, world, local):
                           "head_steps_per_s": hs / (ms * 1e-3),
                           "algorithmic_bytes_per_head_step": bm.variant_bytes(n, w.gate, W),
                           "achieved_gbs": gbs, "frac_of_" + peak_kind + "_hbm": gbs / hbm_peak}
-    total_hs = heads * w.pools * len(variants) * args.steps * world
-    value = total_hs / (elapsed_ms * 1e-3)
+    value = job_throughput(heads * w.pools * len(variants) * args.steps, world, elapsed_ms)
     # one kernel launch per decode call (the window fold runs inside the step kernel)
     launches_per_step = w.pools * len(variants)
 
@@ -294,7 +310,7 @@ def run_native(args, rank, world, local):
     if not args.no_extras:
         out["int8_window_sweep"] = window_sweep(w, slot_idx, masks, inputs, ring, dev, hbm_peak,
                                                 peak_kind, pools["eager"])
-        out["e2e"] = e2e(w, variants, pools, slot_idx, dev)
+        out["e2e"] = e2e(w, variants, pools, slot_idx, dev, world)
         if rank == 0:
             out["cpu_baseline"] = cpu_baseline(w, variants, budget_s=6.0)
     return out
@@ -336,7 +352,7 @@ def window_sweep(w, slot_idx, masks, inputs, ring, dev, peak, peak_kind, eager_p
     return res
 
 
-def e2e(w, variants, pools, slot_idx, dev, tokens=24):
+def e2e(w, variants, pools, slot_idx, dev, world=1, tokens=24):
     """The same step through ls_decode_step_host: inputs copied from pinned host
     memory and y copied back inside the timed region, every call."""
     import torch
@@ -360,15 +376,16 @@ def e2e(w, variants, pools, slot_idx, dev, tokens=24):
 
     for t in range(2):
         step(t)
+    barrier(world)
     t0 = time.perf_counter()
     for t in range(tokens):
         step(t)
-    dt = time.perf_counter() - t0
+    dt = reduce_max(time.perf_counter() - t0, world, dev)
     heads = w.batch * w.heads
     calls = len(variants) * w.pools
     h2d = calls * (4 * w.batch + 4 * heads * (w.d_k * 2 + w.d_v + w.dl + 1))
     d2h = calls * 4 * heads * w.d_v
-    return {"value": heads * calls * tokens / dt, "unit": UNIT, "tokens": tokens,
+    return {"value": job_throughput(heads * calls * tokens, world, dt * 1e3), "unit": UNIT, "tokens": tokens,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "api": "ls_decode_step_host (pinned host buffers, cudaMemcpyAsync inside the "
                    "library, host synchronizes on y every token)"}
@@ -425,7 +442,7 @@ def run_reference(args):
     res = cpu_baseline(w, variants, steps=args.steps)
     wall = time.perf_counter() - t0
     value = res["value"]
-    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * (w.heads * len(variants)) / value,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
