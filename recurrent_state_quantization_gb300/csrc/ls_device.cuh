@@ -159,6 +159,16 @@ __device__ __forceinline__ void row_quant_params(float amax, float& s, float& f)
     }
 }
 
+// Programmatic dependent launch: let the next kernel on the stream be
+// scheduled as soon as every CTA of this one has started, then wait until
+// the previous kernel has completed and its memory is visible.  Called first
+// thing in a step kernel, before any global memory access; a no-op when the
+// launch carries no programmatic dependency.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void flag_status(int32_t* status, int32_t bit) {
     atomicOr(status, bit);
 }

@@ -66,6 +66,7 @@ __device__ __forceinline__ bool wait_quarter(uint64_t* bars, int r, int32_t* sta
 template <bool PER_KEY>
 __global__ void __launch_bounds__(kThreads, 3) eager_step_kernel(const StepArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
+    pdl_enter();
     unsigned char* tile = smem;
     float* xk_s = reinterpret_cast<float*>(smem + tile_bytes(false));
     float* xq_s = xk_s + kD;
@@ -163,11 +164,8 @@ cudaError_t prepare_eager_step_kernels() {
 
 cudaError_t launch_eager_step(const StepArgs& a, bool per_key, cudaStream_t s) {
     const dim3 grid(static_cast<unsigned>(a.batch) * static_cast<unsigned>(a.pv.H));
-    if (per_key)
-        eager_step_kernel<true><<<grid, kThreads, eager_smem_bytes(), s>>>(a);
-    else
-        eager_step_kernel<false><<<grid, kThreads, eager_smem_bytes(), s>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(per_key ? eager_step_kernel<true> : eager_step_kernel<false>, grid,
+                            eager_smem_bytes(), s, a);
 }
 
 }  // namespace ls

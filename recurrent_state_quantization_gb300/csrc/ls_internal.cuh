@@ -7,6 +7,8 @@
 
 #include <cuda_runtime.h>
 
+#include <utility>
+
 namespace ls {
 
 constexpr int kD = 128;         // d_k = d_v
@@ -85,6 +87,25 @@ __host__ __device__ constexpr size_t eager_smem_bytes() {
 __host__ __device__ constexpr size_t transpose_smem_bytes() { return size_t(kD) * (kD + 1) * 4; }
 
 // ---- launchers (each in its own translation unit) -------------------------
+// Launch a step kernel with programmatic stream serialization allowed, so it
+// may be scheduled while the previous kernel on the stream drains (the
+// kernel itself waits for that kernel before touching memory).
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, size_t smem, cudaStream_t s,
+                             Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 cudaError_t prepare_eager_step_kernels();
 cudaError_t prepare_log_step_kernels();
 cudaError_t prepare_fold_kernels();

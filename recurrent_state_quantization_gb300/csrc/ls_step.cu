@@ -368,6 +368,7 @@ __global__ void __launch_bounds__(kThreads, 2) log_step_kernel(const StepArgs a)
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ long long fold_hd[kWarps];
     __shared__ float fold_lb[kWarps];
+    pdl_enter();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const PoolView& pv = a.pv;
     const int row = blockIdx.x * kWarps + warp;
@@ -450,18 +451,9 @@ cudaError_t launch_log_step(const StepArgs& a, bool int8, bool per_key, cudaStre
     const int64_t rows = static_cast<int64_t>(a.batch) * a.pv.H;
     const dim3 grid(static_cast<unsigned>((rows + kWarps - 1) / kWarps));
     const size_t sm = step_smem_bytes();
-    if (int8) {
-        if (per_key)
-            log_step_kernel<true, true><<<grid, kThreads, sm, s>>>(a);
-        else
-            log_step_kernel<true, false><<<grid, kThreads, sm, s>>>(a);
-    } else {
-        if (per_key)
-            log_step_kernel<false, true><<<grid, kThreads, sm, s>>>(a);
-        else
-            log_step_kernel<false, false><<<grid, kThreads, sm, s>>>(a);
-    }
-    return cudaGetLastError();
+    if (int8)
+        return launch_dependent(per_key ? log_step_kernel<true, true> : log_step_kernel<true, false>, grid, sm, s, a);
+    return launch_dependent(per_key ? log_step_kernel<false, true> : log_step_kernel<false, false>, grid, sm, s, a);
 }
 
 }  // namespace ls
