@@ -384,25 +384,24 @@ __device__ bool fold_cta(const PoolView& pv, size_t hd, int n, const float* lbg,
                 return false;
             }
             pp.log_phase ^= 1u;
-            for (int idx = tid; idx < nl * (kD / 4); idx += kThreads) {
-                const int l = idx >> 5, q = idx & 31;  // entry, 4-row / 4-column group
-                const float4 K4 = fs.rk[idx];
-                fs.u4[idx] = fs.ru[idx];
-                float4 g;
+            // (entry, key-row pair) items: each lane stores one float4 of
+            // (a, a) pairs, consecutive lanes consecutive addresses
+            for (int idx = tid; idx < nl * (kD / 2); idx += kThreads) {
+                const int l = idx >> 6, p = idx & 63;
+                const float2 K2 = reinterpret_cast<const float2*>(fs.rk)[idx];
+                float2 g;
                 if constexpr (PER_KEY) {
-                    const float4 lm = fs.rl[idx];
-                    const float4 lb4 = reinterpret_cast<const float4*>(fs.lp)[q];
-                    g = make_float4(expf(lb4.x - lm.x), expf(lb4.y - lm.y), expf(lb4.z - lm.z),
-                                    expf(lb4.w - lm.w));
+                    const float2 lm = reinterpret_cast<const float2*>(fs.rl)[idx];
+                    const float2 lb2 = reinterpret_cast<const float2*>(fs.lp)[p];
+                    g = make_float2(expf(lb2.x - lm.x), expf(lb2.y - lm.y));
                 } else {
                     const float gg = expf(lb_scalar - reinterpret_cast<const float*>(fs.rl)[l]);
-                    g = make_float4(gg, gg, gg, gg);
+                    g = make_float2(gg, gg);
                 }
-                float4* a2 = reinterpret_cast<float4*>(fs.a2 + l * kD + 4 * q);
-                const float ax = g.x * K4.x, ay = g.y * K4.y, az = g.z * K4.z, aw = g.w * K4.w;
-                a2[0] = make_float4(ax, ax, ay, ay);
-                a2[1] = make_float4(az, az, aw, aw);
+                const float a0 = g.x * K2.x, a1 = g.y * K2.y;
+                reinterpret_cast<float4*>(fs.a2)[idx] = make_float4(a0, a0, a1, a1);
             }
+            for (int idx = tid; idx < nl * (kD / 4); idx += kThreads) fs.u4[idx] = fs.ru[idx];
             __syncthreads();
             const bool more = c0 + kFoldChunk < n;
             const bool next = !more && next_hd >= 0 && next_n > 0;
