@@ -1,0 +1,152 @@
+"""Drift report: how far the INT8 trajectory moves from the FP32 one, and how
+close the deferred FP32 trajectory stays to the eager one, per 1024-token
+block, on the GPU (every head) and in the oracle (sampled heads).
+
+Three pools (eager, deferred with the workload's merge interval, INT8 with
+window W) and three oracles run the same seeded tokens, free-running (no
+restarts).  At the end of every block:
+
+- state: ||S_int8 - S_fp32||_F / ||S_fp32||_F over the logical states
+  (ls_pool_read), S_fp32 the eager trajectory;
+- y: the relative L2 of y_int8 - y_fp32 over the block's tokens;
+- deferred: max over heads of max|S_def - S_eager| / max|S_eager|, and for
+  y the per-head max|y_def - y_eager| over the block over max|y_eager| over
+  the block.
+
+The INT8 trajectories of GPU and oracle separate through legitimate one-LSB
+rounding flips, so they are compared statistically: on the sampled heads the
+GPU's INT8-vs-FP32 divergence, summed over the run, must not exceed the
+oracle's own by more than a quarter.  One JSON line per workload is printed
+("drift-report ...").
+"""
+import json
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+BLOCK = 1024
+
+
+def _harness():
+    import _harness as H  # noqa: WPS433 (tests dir is on sys.path)
+    return H
+
+
+def _rows_view(S, pair):
+    """[num_slots, H, 128, 128] -> the sampled rows' states, as float64 numpy."""
+    w, s = pair.w, pair.sample
+    slots_b = pair.slot_idx.cpu().numpy()[s.rows // w.heads]
+    idx = torch.as_tensor(slots_b * w.heads + s.rows % w.heads, device=S.device)
+    return S.reshape(-1, 128, 128).index_select(0, idx).double().cpu().numpy()
+
+
+def _head_relmax(a, b):
+    """max over heads of max|a - b| / max|b| (torch, [n, ...])."""
+    n = a.shape[0]
+    num = (a - b).abs().reshape(n, -1).amax(dim=1)
+    den = b.abs().reshape(n, -1).amax(dim=1).clamp_min(1e-30)
+    return float((num / den).max())
+
+
+class _HeadMax:
+    """Per-head running max|a - b| and max|b| over a block of tokens; the
+    ratio is the y error over the head's trajectory, not per token (a token
+    whose y nearly cancels would otherwise dominate)."""
+
+    def __init__(self):
+        self.num = self.den = None
+
+    def add(self, a, b):
+        n = (a - b).abs().amax(dim=-1)
+        d = b.abs().amax(dim=-1)
+        self.num = n if self.num is None else torch.maximum(self.num, n)
+        self.den = d if self.den is None else torch.maximum(self.den, d)
+
+    def value(self):
+        return float((self.num / self.den.clamp_min(1e-30)).max())
+
+
+@pytest.mark.parametrize("wi,window,n_sample", [(4, 32, 4), (1, 64, 8), (2, 32, 8)])
+def test_drift_report(wi, window, n_sample):
+    from recurrent_state_quantization_gb300 import workloads as wl
+    H = _harness()
+    w = wl.WORKLOADS[wi]
+    pe = H.Pair(w, "eager", 0, n_sample=n_sample)
+    pd = H.Pair(w, "deferred", w.merge_interval, n_sample=n_sample)
+    pi = H.Pair(w, "int8", window, n_sample=n_sample)
+    all_slots = torch.arange(w.num_slots, dtype=torch.int32, device=pe.dev)
+    blocks = []
+    run = {k: 0.0 for k in ("g_s_num", "g_s_den", "o_s_num", "o_s_den", "g_y_num", "g_y_den",
+                            "o_y_num", "o_y_den")}
+    acc = None
+    for t in range(w.tokens):
+        if acc is None:
+            acc = {k: 0.0 for k in ("gy_num", "gy_den", "gys_num", "oy_num", "oy_den")}
+            acc["gdy"], acc["ody"] = _HeadMax(), _HeadMax()
+        ye, yoe = pe.step(t)
+        yd, yod = pd.step(t)
+        yi, yoi = pi.step(t)
+        acc["gy_num"] += float(((yi - ye) ** 2).sum())
+        acc["gy_den"] += float((ye ** 2).sum())
+        rows = torch.as_tensor(pi.sample.rows, device=pi.dev)
+        ysi = yi.reshape(-1, 128).index_select(0, rows).double().cpu().numpy()
+        yse = ye.reshape(-1, 128).index_select(0, rows).double().cpu().numpy()
+        acc["gys_num"] += float(((ysi - yse) ** 2).sum())
+        acc["oy_num"] += float(((yoi - yoe) ** 2).sum())
+        acc["oy_den"] += float((yoe ** 2).sum())
+        acc["gdy"].add(yd.reshape(-1, 128), ye.reshape(-1, 128))
+        acc["ody"].add(torch.from_numpy(yod), torch.from_numpy(yoe))
+        if (t + 1) % BLOCK == 0 or t + 1 == w.tokens:
+            Se = pe.pool.read(all_slots)
+            Sd = pd.pool.read(all_slots)
+            Si = pi.pool.read(all_slots)
+            g_s = float((Si - Se).norm() / Se.norm())
+            g_d = _head_relmax(Sd.reshape(-1, 128, 128), Se.reshape(-1, 128, 128))
+            gse, gsi = _rows_view(Se, pe), _rows_view(Si, pi)
+            oe = pe.orc.logical(pe.sample.state_idx)
+            od = pd.orc.logical(pd.sample.state_idx)
+            oi = pi.orc.logical(pi.sample.state_idx)
+            o_s = H.rel_l2(oi, oe)
+            o_d = max(H.relmax(od[n], oe[n]) for n in range(len(oe)))
+            blk = {"tokens": t + 1,
+                   "gpu": {"state_int8_vs_fp32": g_s,
+                           "state_int8_vs_fp32_sampled": H.rel_l2(gsi, gse),
+                           "y_int8_vs_fp32": (acc["gy_num"] / acc["gy_den"]) ** 0.5,
+                           "deferred_vs_eager_state_relmax": g_d,
+                           "deferred_vs_eager_y_relmax": acc["gdy"].value()},
+                   "oracle": {"state_int8_vs_fp32": o_s,
+                              "y_int8_vs_fp32": (acc["oy_num"] / acc["oy_den"]) ** 0.5,
+                              "deferred_vs_eager_state_relmax": o_d,
+                              "deferred_vs_eager_y_relmax": acc["ody"].value()}}
+            blocks.append(blk)
+            run["g_s_num"] += float(((gsi - gse) ** 2).sum())
+            run["g_s_den"] += float((gse ** 2).sum())
+            run["o_s_num"] += float(((oi - oe) ** 2).sum())
+            run["o_s_den"] += float((oe ** 2).sum())
+            run["g_y_num"] += acc["gys_num"]
+            run["o_y_num"] += acc["oy_num"]
+            run["o_y_den"] += acc["oy_den"]
+            acc = None
+    report = {"workload": w.name, "int8_window": window, "deferred_merge_interval": w.merge_interval,
+              "sampled_heads": int(len(pi.sample.rows)), "blocks": blocks}
+    print("drift-report " + json.dumps(report))
+    for p in (pe, pd, pi):
+        assert p.pool.status() == 0
+    # deferred FP32 stays on the eager trajectory (both are FP32 recurrences
+    # of the same state), on the GPU and in the oracle
+    for b in blocks:
+        assert b["gpu"]["deferred_vs_eager_state_relmax"] <= 2e-4, b
+        assert b["oracle"]["deferred_vs_eager_state_relmax"] <= 1e-9, b
+        assert b["gpu"]["deferred_vs_eager_y_relmax"] <= 2e-4, b
+    # INT8 drifts from FP32 on the GPU as it does in the oracle (same heads)
+    g_s = (run["g_s_num"] / run["g_s_den"]) ** 0.5
+    o_s = (run["o_s_num"] / run["o_s_den"]) ** 0.5
+    g_y = (run["g_y_num"] / run["o_y_den"]) ** 0.5
+    o_y = (run["o_y_num"] / run["o_y_den"]) ** 0.5
+    assert g_s <= 1.25 * o_s + 1e-6, (g_s, o_s)
+    assert g_y <= 1.25 * o_y + 1e-6, (g_y, o_y)
+    assert o_s > 0.0 and np.isfinite(g_s)
