@@ -44,15 +44,19 @@ def _load():
         lib.orc_deferred_commit.argtypes = [I64, I32, I32, I32, I32, P, P, P, P, P, P, P]
         lib.orc_quantize_rows.argtypes = [I64, I32, I32, P, P, P]
         lib.orc_dequantize_rows.argtypes = [I64, I32, I32, P, P, P]
-        lib.orc_window_step.argtypes = [I64, I32, I32, I32, I32, P, P, P, P, P, P, P,
-                                        P, P, P, P, P, P, P, I32]
-        lib.orc_window_commit.argtypes = [I64, I32, I32, P, P, P, P, P]
-        lib.orc_window_load.argtypes = [I64, I32, I32, P, P, P, P, P, P]
-        lib.orc_window_unrolled.argtypes = [I64, I32, I32, I32, I32, P, P, P, P, P, P, P, P]
-        lib.orc_window_readout.argtypes = [I64, I32, I32, I32, I32, P, P, P, P, P, P, P,
-                                           P, P]
+        lib.orc_quantize_cols.argtypes = [I64, I32, I32, P, P, P, P]
+        lib.orc_dequantize_cols.argtypes = [I64, I32, I32, P, P, P, P]
+        lib.orc_window_step.argtypes = [I64, I32, I32, I32, I32, I32, P, P, P, P, P, P,
+                                        P, P, P, P, P, P, P, P, P, I32]
+        lib.orc_window_commit.argtypes = [I64, I32, I32, I32, P, P, P, P, P, P]
+        lib.orc_window_load.argtypes = [I64, I32, I32, I32, P, P, P, P, P, P, P]
+        lib.orc_window_unrolled.argtypes = [I64, I32, I32, I32, I32, I32, P, P, P, P, P, P,
+                                            P, P, P]
+        lib.orc_window_readout.argtypes = [I64, I32, I32, I32, I32, I32, P, P, P, P, P, P,
+                                           P, P, P, P]
         for name in ("orc_eager_step", "orc_deferred_step", "orc_deferred_logical",
                      "orc_deferred_commit", "orc_quantize_rows", "orc_dequantize_rows",
+                     "orc_quantize_cols", "orc_dequantize_cols",
                      "orc_window_step", "orc_window_commit", "orc_window_load",
                      "orc_window_unrolled", "orc_window_readout"):
             getattr(lib, name).restype = I32
@@ -194,15 +198,21 @@ class DeferredOracle(_Base):
 
 
 class WindowInt8Oracle(_Base):
-    """Per-window INT8 scheme, LeapQuant §3.2 eq. 3-4, window W."""
+    """Per-window INT8 scheme, LeapQuant §3.2 eq. 3-4, window W.
 
-    def __init__(self, nstates, dk, dv, dl, W, nthreads=0):
+    col_scales=False: one FP32 scale per key row.  col_scales=True: the
+    smoothed per-value-column format of LeapQuant §3.4 eq. 7 / App. B.3
+    (row factors = smoothing vector c, column factors = scales b)."""
+
+    def __init__(self, nstates, dk, dv, dl, W, nthreads=0, col_scales=False):
         super().__init__(nstates, dk, dv, dl, nthreads)
         if W < 1:
             raise ValueError("W >= 1")
         self.W = int(W)
+        self.mode = 1 if col_scales else 0
         self.Z = np.zeros((self.n, dk, dv), dtype=np.int8)
         self.s = np.zeros((self.n, dk), dtype=np.float32)
+        self.fc = np.zeros((self.n, dv), dtype=np.float32)
         self.Sw = np.zeros((self.n, dk, dv), dtype=np.float64)
         self.rl = np.zeros((self.n, self.W, dl), dtype=np.float64)
         self.rk = np.zeros((self.n, self.W, dk), dtype=np.float64)
@@ -213,8 +223,9 @@ class WindowInt8Oracle(_Base):
         idx = self._idx(idx)
         q, k, v, lam, beta = self._inputs(idx, q, k, v, lam, beta)
         y = np.zeros((idx.size, self.dv), dtype=np.float64)
-        _check(_load().orc_window_step(idx.size, self.dk, self.dv, self.dl, self.W,
-                                       _p(self.Z), _p(self.s), _p(self.Sw), _p(self.rl),
+        _check(_load().orc_window_step(idx.size, self.mode, self.dk, self.dv, self.dl, self.W,
+                                       _p(self.Z), _p(self.s), _p(self.fc), _p(self.Sw),
+                                       _p(self.rl),
                                        _p(self.rk), _p(self.ru), _p(self.cnt), _p(idx),
                                        _p(q), _p(k), _p(v), _p(lam), _p(beta), _p(y),
                                        self.nthreads), "window step")
@@ -225,20 +236,27 @@ class WindowInt8Oracle(_Base):
         return self.Sw[self._idx(idx)].copy()
 
     def codes(self, idx):
+        """(Z, row factors): per-key-row scales, or the smoothing vector c."""
         idx = self._idx(idx)
         return self.Z[idx].copy(), self.s[idx].copy()
 
+    def col_factors(self, idx):
+        """The per-value-column scales b (smoothed format; zeros otherwise)."""
+        return self.fc[self._idx(idx)].copy()
+
     def commit(self, idx):
         idx = self._idx(idx)
-        _check(_load().orc_window_commit(idx.size, self.dk, self.dv, _p(self.Z), _p(self.s),
-                                         _p(self.Sw), _p(self.cnt), _p(idx)), "window commit")
+        _check(_load().orc_window_commit(idx.size, self.mode, self.dk, self.dv, _p(self.Z),
+                                         _p(self.s), _p(self.fc), _p(self.Sw), _p(self.cnt),
+                                         _p(idx)), "window commit")
 
     def load(self, idx, S):
         idx = self._idx(idx)
         S = np.ascontiguousarray(np.asarray(S, dtype=np.float64).reshape(idx.size, self.dk,
                                                                           self.dv))
-        _check(_load().orc_window_load(idx.size, self.dk, self.dv, _p(S), _p(self.Z),
-                                       _p(self.s), _p(self.Sw), _p(self.cnt), _p(idx)),
+        _check(_load().orc_window_load(idx.size, self.mode, self.dk, self.dv, _p(S),
+                                       _p(self.Z), _p(self.s), _p(self.fc), _p(self.Sw),
+                                       _p(self.cnt), _p(idx)),
                "window load")
 
     def reset(self, idx):
@@ -248,8 +266,9 @@ class WindowInt8Oracle(_Base):
         """S_l rebuilt from the boundary state and the buffered records (eq. 4)."""
         idx = self._idx(idx)
         out = np.zeros((idx.size, self.dk, self.dv), dtype=np.float64)
-        _check(_load().orc_window_unrolled(idx.size, self.dk, self.dv, self.dl, self.W,
-                                           _p(self.Z), _p(self.s), _p(self.rl), _p(self.rk),
+        _check(_load().orc_window_unrolled(idx.size, self.mode, self.dk, self.dv, self.dl,
+                                           self.W, _p(self.Z), _p(self.s), _p(self.fc),
+                                           _p(self.rl), _p(self.rk),
                                            _p(self.ru), _p(self.cnt), _p(idx), _p(out)),
                "window unrolled")
         return out
@@ -259,8 +278,9 @@ class WindowInt8Oracle(_Base):
         idx = self._idx(idx)
         x = np.ascontiguousarray(np.asarray(x, dtype=np.float64).reshape(idx.size, self.dk))
         out = np.zeros((idx.size, self.dv), dtype=np.float64)
-        _check(_load().orc_window_readout(idx.size, self.dk, self.dv, self.dl, self.W,
-                                          _p(self.Z), _p(self.s), _p(self.rl), _p(self.rk),
+        _check(_load().orc_window_readout(idx.size, self.mode, self.dk, self.dv, self.dl,
+                                          self.W, _p(self.Z), _p(self.s), _p(self.fc),
+                                          _p(self.rl), _p(self.rk),
                                           _p(self.ru), _p(self.cnt), _p(idx), _p(x), _p(out)),
                "window readout")
         return out
@@ -289,5 +309,31 @@ def dequantize_rows(Z, s):
     return S
 
 
+def quantize_cols(S):
+    """Smoothed per-value-column INT8 (LeapQuant §3.4 eq. 7, App. B.3):
+    returns (Z, c, b) with S ~ c_i Z_ij b_j."""
+    S = np.ascontiguousarray(np.asarray(S, dtype=np.float64))
+    lead = S.shape[:-2]
+    dk, dv = S.shape[-2:]
+    n = int(np.prod(lead)) if lead else 1
+    Z = np.zeros(S.shape, dtype=np.int8)
+    c = np.zeros(lead + (dk,), dtype=np.float32)
+    b = np.zeros(lead + (dv,), dtype=np.float32)
+    _check(_load().orc_quantize_cols(n, dk, dv, _p(S), _p(Z), _p(c), _p(b)), "quantize cols")
+    return Z, c, b
+
+
+def dequantize_cols(Z, c, b):
+    Z = np.ascontiguousarray(np.asarray(Z, dtype=np.int8))
+    c = np.ascontiguousarray(np.asarray(c, dtype=np.float32))
+    b = np.ascontiguousarray(np.asarray(b, dtype=np.float32))
+    lead = Z.shape[:-2]
+    dk, dv = Z.shape[-2:]
+    n = int(np.prod(lead)) if lead else 1
+    S = np.zeros(Z.shape, dtype=np.float64)
+    _check(_load().orc_dequantize_cols(n, dk, dv, _p(Z), _p(c), _p(b), _p(S)), "dequantize cols")
+    return S
+
+
 __all__ = ["EagerOracle", "DeferredOracle", "WindowInt8Oracle", "quantize_rows",
-           "dequantize_rows", "max_threads", "build_oracle"]
+           "dequantize_rows", "quantize_cols", "dequantize_cols", "max_threads", "build_oracle"]

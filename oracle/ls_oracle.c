@@ -418,6 +418,96 @@ static void dequant_rows(int dk, int dv, const int8_t *Z, const float *s,
             S[(size_t)i * dv + j] = (double)s[i] * (double)Z[(size_t)i * dv + j];
 }
 
+/*
+ * The smoothed, per-value-column format of [LQ] §3.4 eq. 7 and App. B.3.
+ * The residual (here the whole boundary state) is divided row by row by the
+ * smoothing vector c, with c_i the square root of key row i's mean absolute
+ * value and a small positive floor, and the result is quantized with one
+ * symmetric INT8 scale per value column j: dequant = (Z / 127) B, so
+ * S ~ C (Z / 127) B.  Decisions in FP32 on the FP32 rounding of S:
+ *     m_i = fl(sum_j |S_ij|) / dv  (sum formed in double, then rounded)
+ *     c_i = max(sqrt_fp32(m_i), 2^-20)
+ *     g_i = fl(1 / c_i),  R_ij = fl(S_ij * g_i)               (C^-1 S)
+ *     B_j = max_i |R_ij|,  b_j = fl(B_j / 127),  f_j = fl(127 / B_j)
+ *     Z_ij = round-half-even(fl(R_ij * f_j))
+ * A column whose b or f is not a positive finite FP32 number gets b = 0 and
+ * Z = 0.  |R_ij f_j| < 127.5, so no clamp acts.  Stored: Z, c (row
+ * factors), b (column factors); dequant S_ij = c_i Z_ij b_j.
+ */
+#define SMOOTH_FLOOR 9.5367431640625e-07f /* 2^-20 */
+
+static void quant_cols(int dk, int dv, const double *S, int8_t *Z, float *c,
+                       float *b)
+{
+    float R[1024];
+    float B[1024];
+    for (int j = 0; j < dv; ++j) B[j] = 0.0f;
+    for (int i = 0; i < dk; ++i) {
+        double sum = 0.0;
+        for (int j = 0; j < dv; ++j) sum += fabs((double)(float)S[(size_t)i * dv + j]);
+        const float m = (float)sum / (float)dv;
+        float ci = sqrtf(m);
+        if (!(ci >= SMOOTH_FLOOR)) ci = SMOOTH_FLOOR;
+        c[i] = ci;
+        const float g = 1.0f / ci;
+        for (int j = 0; j < dv; ++j) {
+            const float r = (float)S[(size_t)i * dv + j] * g;
+            const float a = fabsf(r);
+            if (a > B[j]) B[j] = a;
+        }
+    }
+    for (int j = 0; j < dv; ++j) {
+        float bj = B[j] / 127.0f;
+        float fj = B[j] > 0.0f ? 127.0f / B[j] : 0.0f;
+        if (!(bj > 0.0f) || !(fj <= FLT_MAX)) {
+            bj = 0.0f;
+            fj = 0.0f;
+        }
+        b[j] = bj;
+        R[j] = fj;  /* reuse R as the factors */
+    }
+    for (int i = 0; i < dk; ++i) {
+        const float g = 1.0f / c[i];
+        for (int j = 0; j < dv; ++j) {
+            int8_t z = 0;
+            if (b[j] > 0.0f) {
+                const float r = (float)S[(size_t)i * dv + j] * g;
+                float t = rintf(r * R[j]);
+                if (t > 127.0f) t = 127.0f;
+                if (t < -127.0f) t = -127.0f;
+                z = (int8_t)t;
+            }
+            Z[(size_t)i * dv + j] = z;
+        }
+    }
+}
+
+/* S_ij = c_i * Z_ij * b_j, in double. */
+static void dequant_cols(int dk, int dv, const int8_t *Z, const float *c,
+                         const float *b, double *S)
+{
+    for (int i = 0; i < dk; ++i)
+        for (int j = 0; j < dv; ++j)
+            S[(size_t)i * dv + j] =
+                (double)c[i] * (double)Z[(size_t)i * dv + j] * (double)b[j];
+}
+
+/* The scheme's two formats: mode 0 = per key row (fr = s, fc unused),
+ * mode 1 = smoothed per value column (fr = c, fc = b). */
+static void quant_mode(int mode, int dk, int dv, const double *S, int8_t *Z,
+                       float *fr, float *fc)
+{
+    if (mode == 1) quant_cols(dk, dv, S, Z, fr, fc);
+    else quant_rows(dk, dv, S, Z, fr);
+}
+
+static void dequant_mode(int mode, int dk, int dv, const int8_t *Z,
+                         const float *fr, const float *fc, double *S)
+{
+    if (mode == 1) dequant_cols(dk, dv, Z, fr, fc, S);
+    else dequant_rows(dk, dv, Z, fr, S);
+}
+
 int orc_quantize_rows(int64_t n, int dk, int dv, const double *S, int8_t *Z,
                       float *s)
 {
@@ -440,6 +530,28 @@ int orc_dequantize_rows(int64_t n, int dk, int dv, const int8_t *Z,
     return ORC_OK;
 }
 
+int orc_quantize_cols(int64_t n, int dk, int dv, const double *S, int8_t *Z,
+                      float *c, float *b)
+{
+    if (n < 0 || dk <= 0 || dv <= 0 || dv > 1024) return ORC_ERR_ARG;
+#pragma omp parallel for schedule(static)
+    for (int64_t h = 0; h < n; ++h)
+        quant_cols(dk, dv, S + (size_t)h * dk * dv, Z + (size_t)h * dk * dv,
+                   c + (size_t)h * dk, b + (size_t)h * dv);
+    return ORC_OK;
+}
+
+int orc_dequantize_cols(int64_t n, int dk, int dv, const int8_t *Z,
+                        const float *c, const float *b, double *S)
+{
+    if (n < 0 || dk <= 0 || dv <= 0) return ORC_ERR_ARG;
+#pragma omp parallel for schedule(static)
+    for (int64_t h = 0; h < n; ++h)
+        dequant_cols(dk, dv, Z + (size_t)h * dk * dv, c + (size_t)h * dk,
+                     b + (size_t)h * dv, S + (size_t)h * dk * dv);
+    return ORC_OK;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Per-window INT8 scheme                                                    */
 /* ------------------------------------------------------------------------ */
@@ -447,7 +559,9 @@ int orc_dequantize_rows(int64_t n, int dk, int dv, const int8_t *Z,
 /*
  * Per-state arrays of the per-window scheme ([LQ] §3.2):
  *   Z    [dk*dv] int8   quantized boundary state (payload of S-hat_0)
- *   s    [dk]    float  its per-key-row scales
+ *   s    [dk]    float  its row factors: per-key-row scales (mode 0) or the
+ *                       smoothing vector c (mode 1, [LQ] §3.4)
+ *   fc   [dv]    float  mode 1: per-value-column scales b (unused in mode 0)
  *   Sw   [dk*dv] double the exact state S_i reached from dequant(S-hat_0)
  *                       by the window's records so far (eq. 3)
  *   rl   [W*dl]  double buffered log-decays  (alpha_i = exp(rl_i))
@@ -461,9 +575,10 @@ int orc_dequantize_rows(int64_t n, int dk, int dv, const int8_t *Z,
  *     y_i = S_i^T q_i                       (read before any quantization)
  *     buffer (alpha_i, k_i, u_i)
  *     at the W-th record: S-hat <- quant_8(S_W), S_W <- dequant(S-hat),
- *     empty the buffer.
+ *     empty the buffer (quant_8 / dequant of the pool's format, `mode`).
  */
-static void window_one(int dk, int dv, int dl, int W, int8_t *Z, float *s,
+static void window_one(int mode, int dk, int dv, int dl, int W, int8_t *Z,
+                       float *s, float *fc,
                        double *Sw, double *rl, double *rk, double *ru,
                        int32_t *cntp, const float *q, const float *k,
                        const float *v, const float *lam, float beta,
@@ -476,26 +591,30 @@ static void window_one(int dk, int dv, int dl, int W, int8_t *Z, float *s,
     for (int i = 0; i < dk; ++i) rk[(size_t)c * dk + i] = (double)k[i];
     for (int j = 0; j < dv; ++j) ru[(size_t)c * dv + j] = u[j];
     if (c + 1 == W) {
-        quant_rows(dk, dv, Sw, Z, s);
-        dequant_rows(dk, dv, Z, s, Sw);
+        quant_mode(mode, dk, dv, Sw, Z, s, fc);
+        dequant_mode(mode, dk, dv, Z, s, fc, Sw);
         *cntp = 0;
     } else {
         *cntp = c + 1;
     }
 }
 
-static int window_args_ok(int dk, int dv, int dl, int W)
+static int window_args_ok(int mode, int dk, int dv, int dl, int W)
 {
-    return valid_dims(dk, dv, dl) && W >= 1 && dk <= 1024 && dv <= 1024;
+    return valid_dims(dk, dv, dl) && W >= 1 && dk <= 1024 && dv <= 1024 &&
+           (mode == 0 || mode == 1);
 }
 
-int orc_window_step(int64_t n, int dk, int dv, int dl, int W, int8_t *Z,
-                    float *s, double *Sw, double *rl, double *rk, double *ru,
+/* fc: the column factors ([n_states][dv]); may be NULL in mode 0. */
+int orc_window_step(int64_t n, int mode, int dk, int dv, int dl, int W,
+                    int8_t *Z, float *s, float *fc, double *Sw, double *rl,
+                    double *rk, double *ru,
                     int32_t *cnt, const int64_t *idx, const float *q,
                     const float *k, const float *v, const float *lam,
                     const float *beta, double *y, int nthreads)
 {
-    if (n < 0 || !window_args_ok(dk, dv, dl, W)) return ORC_ERR_ARG;
+    if (n < 0 || !window_args_ok(mode, dk, dv, dl, W)) return ORC_ERR_ARG;
+    if (mode == 1 && fc == NULL) return ORC_ERR_ARG;
     if (n == 0) return ORC_OK;
     set_threads(nthreads);
     int err = 0;
@@ -509,8 +628,9 @@ int orc_window_step(int64_t n, int dk, int dv, int dl, int W, int8_t *Z,
 #pragma omp for schedule(dynamic, 4)
             for (int64_t row = 0; row < n; ++row) {
                 const int64_t h = idx[row];
-                window_one(dk, dv, dl, W, Z + (size_t)h * dk * dv,
-                           s + (size_t)h * dk, Sw + (size_t)h * dk * dv,
+                window_one(mode, dk, dv, dl, W, Z + (size_t)h * dk * dv,
+                           s + (size_t)h * dk, mode ? fc + (size_t)h * dv : NULL,
+                           Sw + (size_t)h * dk * dv,
                            rl + (size_t)h * W * dl, rk + (size_t)h * W * dk,
                            ru + (size_t)h * W * dv, cnt + h, q + row * dk,
                            k + row * dk, v + row * dv, lam + row * dl,
@@ -523,17 +643,21 @@ int orc_window_step(int64_t n, int dk, int dv, int dl, int W, int8_t *Z,
 }
 
 /* Close the current window early: quantize S_i, start a new window. */
-int orc_window_commit(int64_t n, int dk, int dv, int8_t *Z, float *s,
-                      double *Sw, int32_t *cnt, const int64_t *idx)
+int orc_window_commit(int64_t n, int mode, int dk, int dv, int8_t *Z,
+                      float *s, float *fc, double *Sw, int32_t *cnt,
+                      const int64_t *idx)
 {
-    if (n < 0 || dk <= 0 || dv <= 0) return ORC_ERR_ARG;
+    if (n < 0 || dk <= 0 || dv <= 0 || dv > 1024 || (mode != 0 && mode != 1) ||
+        (mode == 1 && fc == NULL))
+        return ORC_ERR_ARG;
 #pragma omp parallel for schedule(static)
     for (int64_t row = 0; row < n; ++row) {
         const int64_t h = idx[row];
         if (cnt[h] == 0) continue;
-        quant_rows(dk, dv, Sw + (size_t)h * dk * dv, Z + (size_t)h * dk * dv,
-                   s + (size_t)h * dk);
-        dequant_rows(dk, dv, Z + (size_t)h * dk * dv, s + (size_t)h * dk,
+        float *fch = mode ? fc + (size_t)h * dv : NULL;
+        quant_mode(mode, dk, dv, Sw + (size_t)h * dk * dv, Z + (size_t)h * dk * dv,
+                   s + (size_t)h * dk, fch);
+        dequant_mode(mode, dk, dv, Z + (size_t)h * dk * dv, s + (size_t)h * dk, fch,
                      Sw + (size_t)h * dk * dv);
         cnt[h] = 0;
     }
@@ -541,16 +665,20 @@ int orc_window_commit(int64_t n, int dk, int dv, int8_t *Z, float *s,
 }
 
 /* Start a window from a given state: S-hat_0 = quant_8(S). */
-int orc_window_load(int64_t n, int dk, int dv, const double *S, int8_t *Z,
-                    float *s, double *Sw, int32_t *cnt, const int64_t *idx)
+int orc_window_load(int64_t n, int mode, int dk, int dv, const double *S,
+                    int8_t *Z, float *s, float *fc, double *Sw, int32_t *cnt,
+                    const int64_t *idx)
 {
-    if (n < 0 || dk <= 0 || dv <= 0) return ORC_ERR_ARG;
+    if (n < 0 || dk <= 0 || dv <= 0 || dv > 1024 || (mode != 0 && mode != 1) ||
+        (mode == 1 && fc == NULL))
+        return ORC_ERR_ARG;
 #pragma omp parallel for schedule(static)
     for (int64_t row = 0; row < n; ++row) {
         const int64_t h = idx[row];
-        quant_rows(dk, dv, S + (size_t)row * dk * dv, Z + (size_t)h * dk * dv,
-                   s + (size_t)h * dk);
-        dequant_rows(dk, dv, Z + (size_t)h * dk * dv, s + (size_t)h * dk,
+        float *fch = mode ? fc + (size_t)h * dv : NULL;
+        quant_mode(mode, dk, dv, S + (size_t)row * dk * dv, Z + (size_t)h * dk * dv,
+                   s + (size_t)h * dk, fch);
+        dequant_mode(mode, dk, dv, Z + (size_t)h * dk * dv, s + (size_t)h * dk, fch,
                      Sw + (size_t)h * dk * dv);
         cnt[h] = 0;
     }
@@ -564,12 +692,13 @@ int orc_window_load(int64_t n, int dk, int dv, const double *S, int8_t *Z,
  *   Gamma_{a:b} = Diag(alpha_b) ... Diag(alpha_a), identity when a > b.
  * The diagonal products are accumulated as sums of log-decays.
  */
-int orc_window_unrolled(int64_t n, int dk, int dv, int dl, int W,
-                        const int8_t *Z, const float *s, const double *rl,
-                        const double *rk, const double *ru,
+int orc_window_unrolled(int64_t n, int mode, int dk, int dv, int dl, int W,
+                        const int8_t *Z, const float *s, const float *fc,
+                        const double *rl, const double *rk, const double *ru,
                         const int32_t *cnt, const int64_t *idx, double *S_out)
 {
-    if (n < 0 || !window_args_ok(dk, dv, dl, W)) return ORC_ERR_ARG;
+    if (n < 0 || !window_args_ok(mode, dk, dv, dl, W)) return ORC_ERR_ARG;
+    if (mode == 1 && fc == NULL) return ORC_ERR_ARG;
 #pragma omp parallel for schedule(dynamic, 2)
     for (int64_t row = 0; row < n; ++row) {
         const int64_t h = idx[row];
@@ -578,7 +707,8 @@ int orc_window_unrolled(int64_t n, int dk, int dv, int dl, int W,
         const double *RK = rk + (size_t)h * W * dk;
         const double *RU = ru + (size_t)h * W * dv;
         double *S = S_out + (size_t)row * dk * dv;
-        dequant_rows(dk, dv, Z + (size_t)h * dk * dv, s + (size_t)h * dk, S);
+        dequant_mode(mode, dk, dv, Z + (size_t)h * dk * dv, s + (size_t)h * dk,
+                     mode ? fc + (size_t)h * dv : NULL, S);
         for (int i = 0; i < dk; ++i) {
             double g = 0.0; /* log of Gamma_{1:l}, row i */
             for (int t = 0; t < l; ++t) g += dlam_at(RL + (size_t)t * dl, dl, i);
@@ -600,16 +730,19 @@ int orc_window_unrolled(int64_t n, int dk, int dv, int dl, int W,
 }
 
 /*
- * Window readout without forming the state, [LQ] App. B.2 eq. 9:
+ * Window readout without forming the state, [LQ] App. B.2 eq. 9 (mode 1:
+ * App. B.3 eq. 10, the boundary term B Z^T C Gamma x / 127):
  *   S_l^T x = S-hat_0^T Gamma_{1:l} x + sum_j u_j (k_j^T Gamma_{j+1:l} x).
  * x is [n][dk]; out is [n][dv].
  */
-int orc_window_readout(int64_t n, int dk, int dv, int dl, int W,
-                       const int8_t *Z, const float *s, const double *rl,
-                       const double *rk, const double *ru, const int32_t *cnt,
-                       const int64_t *idx, const double *x, double *out)
+int orc_window_readout(int64_t n, int mode, int dk, int dv, int dl, int W,
+                       const int8_t *Z, const float *s, const float *fc,
+                       const double *rl, const double *rk, const double *ru,
+                       const int32_t *cnt, const int64_t *idx, const double *x,
+                       double *out)
 {
-    if (n < 0 || !window_args_ok(dk, dv, dl, W)) return ORC_ERR_ARG;
+    if (n < 0 || !window_args_ok(mode, dk, dv, dl, W)) return ORC_ERR_ARG;
+    if (mode == 1 && fc == NULL) return ORC_ERR_ARG;
 #pragma omp parallel for schedule(dynamic, 2)
     for (int64_t row = 0; row < n; ++row) {
         const int64_t h = idx[row];
@@ -619,6 +752,7 @@ int orc_window_readout(int64_t n, int dk, int dv, int dl, int W,
         const double *RU = ru + (size_t)h * W * dv;
         const int8_t *Zh = Z + (size_t)h * dk * dv;
         const float *sh = s + (size_t)h * dk;
+        const float *bh = mode ? fc + (size_t)h * dv : NULL;
         const double *xr = x + (size_t)row * dk;
         double *o = out + (size_t)row * dv;
         for (int j = 0; j < dv; ++j) o[j] = 0.0;
@@ -626,8 +760,10 @@ int orc_window_readout(int64_t n, int dk, int dv, int dl, int W,
             double g = 0.0;
             for (int t = 0; t < l; ++t) g += dlam_at(RL + (size_t)t * dl, dl, i);
             const double gx = exp(g) * xr[i];
+            /* [LQ] App. B.3 eq. 10: B Z^T C Gamma x for mode 1 */
             for (int j = 0; j < dv; ++j)
-                o[j] += (double)sh[i] * (double)Zh[(size_t)i * dv + j] * gx;
+                o[j] += (double)sh[i] * (double)Zh[(size_t)i * dv + j] * gx *
+                        (bh ? (double)bh[j] : 1.0);
         }
         for (int jj = 0; jj < l; ++jj) {
             double c = 0.0;
