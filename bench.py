@@ -174,9 +174,10 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def make_pools(w, variant, window, dev):
+def make_pools(w, variant, window, dev, col_scales=False):
     from recurrent_state_quantization_gb300 import StatePool
-    return [StatePool(w.num_slots, w.heads, variant, w.gate, window, device=dev)
+    return [StatePool(w.num_slots, w.heads, variant, w.gate, window, device=dev,
+                      col_scales=col_scales)
             for _ in range(w.pools)]
 
 
@@ -318,15 +319,16 @@ def run_native(args, rank, world, local):
 
 def window_sweep(w, slot_idx, masks, inputs, ring, dev, peak, peak_kind, eager_pools):
     """INT8 head-steps/s and achieved algorithmic GB/s for each window W (a
-    whole number of windows, 4 pools, warmed states)."""
+    whole number of windows, 4 pools, warmed states), and for W = 16 in the
+    smoothed per-value-column format."""
     import torch
     from recurrent_state_quantization_gb300 import bytemodel as bm
     all_slots = torch.arange(w.num_slots, dtype=torch.int32, device=dev)
     res = []
     stream = torch.cuda.current_stream()
     heads = w.batch * w.heads
-    for W in SWEEP_W:
-        pools = make_pools(w, "int8", W, dev)
+    for W, cols in [(W_, False) for W_ in SWEEP_W] + [(16, True)]:
+        pools = make_pools(w, "int8", W, dev, col_scales=cols)
         for p in range(w.pools):
             pools[p].load(all_slots, eager_pools[p].read(all_slots))
         y = torch.empty(w.batch, w.heads, w.d_v, device=dev)
@@ -344,8 +346,9 @@ def window_sweep(w, slot_idx, masks, inputs, ring, dev, peak, peak_kind, eager_p
         torch.cuda.synchronize()
         ms = a.elapsed_time(b)
         hs = heads * w.pools * tokens
-        gbs = bm.int8_bytes(w.gate, W) * hs / (ms * 1e-3) / 1e9
-        res.append({"window": W, "tokens": tokens, "head_steps_per_s": hs / (ms * 1e-3),
+        gbs = bm.int8_bytes(w.gate, W, col_scales=cols) * hs / (ms * 1e-3) / 1e9
+        res.append({"window": W, "format": "smoothed per-value-column" if cols else "per-key-row",
+                    "tokens": tokens, "head_steps_per_s": hs / (ms * 1e-3),
                     "achieved_gbs": gbs, "frac_of_" + peak_kind + "_hbm": gbs / peak})
         del pools
         torch.cuda.empty_cache()

@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define LS_ABI_VERSION 1
+#define LS_ABI_VERSION 2
 
 /* status codes */
 #define LS_OK 0
@@ -87,6 +87,19 @@ typedef enum {
 /* Largest `window` (W for LS_WINDOW_INT8, M for LS_DEFERRED_FP32). */
 #define LS_MAX_WINDOW 256
 
+/*
+ * ls_pool_desc.flags.  LS_INT8_COLUMN_SCALES (LS_WINDOW_INT8 only): store the
+ * window-boundary state in the smoothed per-value-column format of
+ * "LeapQuant: Efficient Linear Attention with Accurate Recurrent State
+ * Quantization", §3.4 eq. 7 and App. B.3: each key row i is divided by its
+ * smoothing factor c_i = max(sqrt(mean_j |S_ij|), 2^-20), and the result is
+ * quantized with one symmetric INT8 scale b_j = B_j / 127 per value column
+ * (B_j the column's absmax, codes rint(R_ij * (127 / B_j))), so that
+ * S_ij ~ c_i Z_ij b_j; reads use eq. 10 (B Z^T C Gamma x / 127).  Without
+ * the flag, one scale s_i = B_i / 127 per key row: S_ij ~ s_i Z_ij.
+ */
+#define LS_INT8_COLUMN_SCALES 1u
+
 typedef struct {
     int32_t num_slots; /* P >= 1: states (requests) the pool holds            */
     int32_t num_heads; /* H >= 1                                                */
@@ -96,7 +109,7 @@ typedef struct {
     int32_t gate;      /* ls_gate                                              */
     int32_t window;    /* W (INT8) or M (deferred), 1..LS_MAX_WINDOW; ignored
                           (may be 0) for LS_EAGER_FP32                          */
-    uint32_t flags;    /* reserved, must be 0                                   */
+    uint32_t flags;    /* 0, or LS_INT8_COLUMN_SCALES for LS_WINDOW_INT8       */
 } ls_pool_desc;
 
 /* Human-readable name of a status code.  Never NULL. */
@@ -215,12 +228,23 @@ int ls_pool_read(const ls_pool *pool, const int32_t *d_slots, int32_t n,
 
 /*
  * LS_WINDOW_INT8 only: the current base of `n` slots as codes
- * d_codes [n, H, d_k, d_v] (int8, logical layout, 16-byte aligned) and
- * scales d_scales [n, H, d_k] (FP32): dequant(S)[i][j] = scales[i] * codes[i][j].
- * Errors as ls_pool_load, and LS_ERR_INVALID for the other variants.
+ * d_codes [n, H, d_k, d_v] (int8, logical layout, 16-byte aligned) and the
+ * key-row factors d_scales [n, H, d_k] (FP32): the per-row scales s_i, so
+ * dequant(S)[i][j] = s_i * codes[i][j]; with LS_INT8_COLUMN_SCALES the
+ * smoothing factors c_i (see ls_pool_read_int8_col_scales).  Errors as
+ * ls_pool_load, and LS_ERR_INVALID for the other variants.
  */
 int ls_pool_read_int8(const ls_pool *pool, const int32_t *d_slots, int32_t n,
                       int8_t *d_codes, float *d_scales, void *stream);
+
+/*
+ * LS_WINDOW_INT8 with LS_INT8_COLUMN_SCALES only: the per-value-column
+ * scales b_j of `n` slots into d_col_scales [n, H, d_v] (FP32), so that
+ * dequant(S)[i][j] = c_i * codes[i][j] * b_j (LeapQuant App. B.3).  Errors
+ * as ls_pool_load, and LS_ERR_INVALID for other pools.
+ */
+int ls_pool_read_int8_col_scales(const ls_pool *pool, const int32_t *d_slots,
+                                 int32_t n, float *d_col_scales, void *stream);
 
 /*
  * Deferred / INT8 only: the live log length of every (slot, head) into

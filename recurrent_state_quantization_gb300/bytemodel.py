@@ -15,7 +15,9 @@ written; the roofline fraction divides them by a measured kernel time.
   with C_entry = p_K d_k + p_U d_v + 4 dl and C_decay = 4 dl.
 * Per-window INT8 with window W ("LeapQuant: Efficient Linear Attention with
   Accurate Recurrent State Quantization", §3.2): the same cycle with an INT8
-  base plus one FP32 scale per key row in place of the FP32 base.
+  base plus one FP32 scale per key row in place of the FP32 base; the
+  smoothed per-value-column format (§3.4 eq. 7, App. B.3) adds one FP32
+  scale per value column to that base.
 """
 from __future__ import annotations
 
@@ -38,8 +40,8 @@ def state_bytes_fp32(d_k: int = 128, d_v: int = 128) -> int:
     return 4 * d_k * d_v
 
 
-def state_bytes_int8(d_k: int = 128, d_v: int = 128) -> int:
-    return d_k * d_v + 4 * d_k
+def state_bytes_int8(d_k: int = 128, d_v: int = 128, col_scales: bool = False) -> int:
+    return d_k * d_v + 4 * d_k + (4 * d_v if col_scales else 0)
 
 
 def eager_bytes(gate: str, d_k: int = 128, d_v: int = 128) -> float:
@@ -57,8 +59,8 @@ def deferred_bytes(gate: str, M: int, d_k: int = 128, d_v: int = 128) -> float:
     return log_cycle_bytes(state_bytes_fp32(d_k, d_v), gate, M, d_k, d_v)
 
 
-def int8_bytes(gate: str, W: int, d_k: int = 128, d_v: int = 128) -> float:
-    return log_cycle_bytes(state_bytes_int8(d_k, d_v), gate, W, d_k, d_v)
+def int8_bytes(gate: str, W: int, d_k: int = 128, d_v: int = 128, col_scales: bool = False) -> float:
+    return log_cycle_bytes(state_bytes_int8(d_k, d_v, col_scales), gate, W, d_k, d_v)
 
 
 def variant_bytes(variant: str, gate: str, window: int = 1) -> float:

@@ -29,14 +29,15 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 bool is_log_variant(int32_t v) { return v == LS_DEFERRED_FP32 || v == LS_WINDOW_INT8; }
 
 struct Layout {
-    size_t status, base, scale, lbar, len, klog, ulog, lamlog, total;
+    size_t status, base, scale, colf, lbar, len, klog, ulog, lamlog, total;
 };
 
 // Checks a descriptor; fills the layout when it is valid.
 int make_layout(const ls_pool_desc* d, Layout* L) {
     if (d == nullptr || L == nullptr) return LS_ERR_INVALID;
-    if (d->flags != 0) return LS_ERR_INVALID;
     if (d->variant < LS_EAGER_FP32 || d->variant > LS_WINDOW_INT8) return LS_ERR_INVALID;
+    if ((d->flags & ~LS_INT8_COLUMN_SCALES) != 0) return LS_ERR_INVALID;
+    if ((d->flags & LS_INT8_COLUMN_SCALES) && d->variant != LS_WINDOW_INT8) return LS_ERR_INVALID;
     if (d->gate != LS_GATE_SCALAR && d->gate != LS_GATE_PER_KEY) return LS_ERR_INVALID;
     if (d->num_slots < 1 || d->num_heads < 1) return LS_ERR_INVALID;
     if (d->d_k != kD || d->d_v != kD) return LS_ERR_SIZE;
@@ -54,6 +55,8 @@ int make_layout(const ls_pool_desc* d, Layout* L) {
     off = align_up(off + nh * kD * kD * (int8 ? 1 : 4));
     L->scale = off;
     off = align_up(off + (int8 ? nh * kD * 4 : 0));
+    L->colf = off;  // per-value-column scales (LS_INT8_COLUMN_SCALES)
+    off = align_up(off + ((d->flags & LS_INT8_COLUMN_SCALES) ? nh * kD * 4 : 0));
     L->lbar = off;
     off = align_up(off + (log ? nh * dl * 4 : 0));
     L->len = off;
@@ -76,6 +79,7 @@ ls::PoolView make_view(const ls_pool_desc& d, const Layout& L, unsigned char* m)
     v.status = reinterpret_cast<int32_t*>(m + L.status);
     v.base = m + L.base;
     v.scale = d.variant == LS_WINDOW_INT8 ? reinterpret_cast<float*>(m + L.scale) : nullptr;
+    v.colf = (d.flags & LS_INT8_COLUMN_SCALES) ? reinterpret_cast<float*>(m + L.colf) : nullptr;
     v.lbar = log ? reinterpret_cast<float*>(m + L.lbar) : nullptr;
     v.len = log ? reinterpret_cast<int32_t*>(m + L.len) : nullptr;
     v.klog = log ? reinterpret_cast<float*>(m + L.klog) : nullptr;
@@ -337,6 +341,18 @@ int ls_pool_read_int8(const ls_pool* pool, const int32_t* d_slots, int32_t n, in
     a.codes_out = d_codes;
     a.scales_out = d_scales;
     return cuda_status(ls::launch_read_int8(a, static_cast<cudaStream_t>(stream)));
+}
+
+int ls_pool_read_int8_col_scales(const ls_pool* pool, const int32_t* d_slots, int32_t n,
+                                 float* d_col_scales, void* stream) {
+    int rc = check_slot_list(pool, d_slots, n);
+    if (rc != LS_OK || n == 0) return rc;
+    if (pool->view.colf == nullptr) return LS_ERR_INVALID;
+    if (d_col_scales == nullptr) return LS_ERR_INVALID;
+    if (!aligned(d_col_scales, 4)) return LS_ERR_ALIGN;
+    ls::AuxArgs a = aux_args(pool, d_slots, n);
+    a.scales_out = d_col_scales;
+    return cuda_status(ls::launch_read_colf(a, static_cast<cudaStream_t>(stream)));
 }
 
 int ls_pool_read_log_meta(const ls_pool* pool, const int32_t* d_slots, int32_t n, int32_t* d_len,

@@ -102,6 +102,32 @@ __global__ void __launch_bounds__(kThreads) load_rows_kernel(const AuxArgs a) {
     clear_log(pv, hd);
 }
 
+// INT8, smoothed per-value-column format: state_in[n][h] -> codes, smoothing
+// factors c and column scales b, with the window end's own quantization
+// ("LeapQuant: Efficient Linear Attention with Accurate Recurrent State
+// Quantization", §3.4 eq. 7); warp w holds key rows 16w..16w+15.
+__global__ void __launch_bounds__(kThreads) load_cols_kernel(const AuxArgs a) {
+    __shared__ __align__(16) float red[kWarps * kD];
+    __shared__ __align__(16) float fcol[kD];
+    const PoolView& pv = a.pv;
+    const int H = pv.H;
+    const int n = blockIdx.x / H, h = blockIdx.x - n * H;
+    int slot;
+    if (!slot_of(a, n, &slot)) return;  // uniform over the CTA
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const size_t hd = static_cast<size_t>(slot) * H + h;
+    const float* in = a.state_in + (static_cast<size_t>(n) * H + h) * (kD * kD);
+    float2 lo[16], hi[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        const float4 v = ldg4(in + (16 * warp + r) * kD + 4 * lane);
+        lo[r] = make_float2(v.x, v.y);
+        hi[r] = make_float2(v.z, v.w);
+    }
+    quantize_cols_cta(lo, hi, pv.base, hd, pv.scale + hd * kD, pv.colf + hd * kD, red, fcol);
+    clear_log(pv, hd);
+}
+
 template <bool INT8>
 __global__ void __launch_bounds__(kThreads) reset_kernel(const AuxArgs a) {
     const PoolView& pv = a.pv;
@@ -115,7 +141,12 @@ __global__ void __launch_bounds__(kThreads) reset_kernel(const AuxArgs a) {
     const int n4 = static_cast<int>(tile_bytes(INT8) / 16);
     for (int idx = threadIdx.x; idx < n4; idx += kThreads) base[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
     if constexpr (INT8) {
-        if (threadIdx.x < kD) pv.scale[hd * kD + threadIdx.x] = 0.0f;
+        // a zero state: per-row scales 0, or (column-scale format) floored
+        // smoothing factors and zero column scales
+        if (threadIdx.x < kD) {
+            pv.scale[hd * kD + threadIdx.x] = pv.colf != nullptr ? kSmoothFloor : 0.0f;
+            if (pv.colf != nullptr) pv.colf[hd * kD + threadIdx.x] = 0.0f;
+        }
     }
     clear_log(pv, hd);
 }
@@ -144,6 +175,17 @@ __global__ void __launch_bounds__(kThreads) read_int8_kernel(const AuxArgs a) {
     if (threadIdx.x < kD) a.scales_out[o * kD + threadIdx.x] = pv.scale[hd * kD + threadIdx.x];
 }
 
+__global__ void __launch_bounds__(128) read_colf_kernel(const AuxArgs a) {
+    const PoolView& pv = a.pv;
+    const int H = pv.H;
+    const int n = blockIdx.x / H, h = blockIdx.x - n * H;
+    int slot;
+    if (!slot_of(a, n, &slot)) return;
+    const size_t hd = static_cast<size_t>(slot) * H + h;
+    const size_t o = static_cast<size_t>(n) * H + h;
+    a.scales_out[o * kD + threadIdx.x] = pv.colf[hd * kD + threadIdx.x];
+}
+
 __global__ void __launch_bounds__(128) read_log_meta_kernel(const AuxArgs a) {
     const PoolView& pv = a.pv;
     const int H = pv.H;
@@ -168,6 +210,8 @@ cudaError_t launch_load(const AuxArgs& a, bool int8, bool has_log, cudaStream_t 
     const dim3 grid(static_cast<unsigned>(a.n) * static_cast<unsigned>(a.pv.H));
     if (!has_log)
         load_eager_kernel<<<grid, kThreads, transpose_smem_bytes(), s>>>(a);
+    else if (int8 && a.pv.colf != nullptr)
+        load_cols_kernel<<<grid, kThreads, 0, s>>>(a);
     else if (int8)
         load_rows_kernel<true><<<grid, kThreads, 0, s>>>(a);
     else
@@ -187,6 +231,12 @@ cudaError_t launch_reset(const AuxArgs& a, bool int8, bool /*has_log*/, cudaStre
 cudaError_t launch_read_int8(const AuxArgs& a, cudaStream_t s) {
     const dim3 grid(static_cast<unsigned>(a.n) * static_cast<unsigned>(a.pv.H));
     read_int8_kernel<<<grid, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_read_colf(const AuxArgs& a, cudaStream_t s) {
+    const dim3 grid(static_cast<unsigned>(a.n) * static_cast<unsigned>(a.pv.H));
+    read_colf_kernel<<<grid, kD, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -39,7 +39,10 @@ constexpr int32_t kDevBadState = 4;
 struct PoolView {
     int32_t* status;       // [1] LS_DEV_* bits
     void* base;            // FP32 or INT8 base states (see above)
-    float* scale;          // INT8: [P*H][d_k] per-key-row scales
+    float* scale;          // INT8: [P*H][d_k] key-row factors: per-row scales s,
+                           //   or the smoothing factors c (column-scale format)
+    float* colf;           // INT8 column-scale format: [P*H][d_v] value-column
+                           //   scales b; nullptr for per-row scales
     float* lbar;           // log variants: [P*H][dl] cumulative log-decay
     int32_t* len;          // log variants: [P*H] live log length
     float* klog;           // [P*H][W][d_k]  key factors k
@@ -120,6 +123,7 @@ cudaError_t launch_eager_read(const AuxArgs& a, cudaStream_t s);
 cudaError_t launch_load(const AuxArgs& a, bool int8, bool has_log, cudaStream_t s);
 cudaError_t launch_reset(const AuxArgs& a, bool int8, bool has_log, cudaStream_t s);
 cudaError_t launch_read_int8(const AuxArgs& a, cudaStream_t s);
+cudaError_t launch_read_colf(const AuxArgs& a, cudaStream_t s);
 cudaError_t launch_read_log_meta(const AuxArgs& a, cudaStream_t s);
 
 }  // namespace ls

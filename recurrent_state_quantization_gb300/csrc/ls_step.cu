@@ -86,7 +86,9 @@ __device__ __forceinline__ void issue_item(WarpSmem& ws, const StepArgs& a, int 
     fence_proxy_async();  // the stage's previous contents were read by the generic proxy
     if (it == 0) {
         const size_t ro = static_cast<size_t>(row) * kD;
-        uint32_t bytes = 3 * kVecBytes + (PER_KEY ? 2 * kVecBytes : 0) + (INT8 ? kVecBytes : 0);
+        const bool cols = INT8 && pv.colf != nullptr;
+        uint32_t bytes = 3 * kVecBytes + (PER_KEY ? 2 * kVecBytes : 0) + (INT8 ? kVecBytes : 0) +
+                         (cols ? kVecBytes : 0);
         mbar_arrive_expect_tx(bar, bytes);
         bulk_g2s(dst, a.k + ro, kVecBytes, bar);
         bulk_g2s(dst + kVecBytes, a.q + ro, kVecBytes, bar);
@@ -97,7 +99,10 @@ __device__ __forceinline__ void issue_item(WarpSmem& ws, const StepArgs& a, int 
             bulk_g2s(dst + off + kVecBytes, pv.lbar + hd * kD, kVecBytes, bar);
             off += 2 * kVecBytes;
         }
-        if constexpr (INT8) bulk_g2s(dst + off, pv.scale + hd * kD, kVecBytes, bar);
+        if constexpr (INT8) {
+            bulk_g2s(dst + off, pv.scale + hd * kD, kVecBytes, bar);
+            if (cols) bulk_g2s(dst + off + kVecBytes, pv.colf + hd * kD, kVecBytes, bar);
+        }
     } else if (it <= P::NT) {
         mbar_arrive_expect_tx(bar, kChunk);
         bulk_g2s(dst, reinterpret_cast<const unsigned char*>(pv.base) + hd * tile_bytes(INT8) +
@@ -172,6 +177,7 @@ __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, 
     __syncwarp();
 
     float4 k4, q4, v4, lp4;
+    float4 colf4 = make_float4(1.f, 1.f, 1.f, 1.f);  // INT8 column-scale format: b of my columns
     float kq = 0.0f;
     float2 r01 = make_float2(0.f, 0.f), r23 = r01, y01 = r01, y23 = r01;
     // INT8: exact integer GEMVs.  xk (and xq) are written in fixed point
@@ -218,8 +224,11 @@ __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, 
             }
             float4 es = make_float4(expf(lp4.x), expf(lp4.y), expf(lp4.z), expf(lp4.w));
             if constexpr (INT8) {
+                // key-row factors: per-row scales, or the smoothing factors c
+                // (LeapQuant App. B.3: C Gamma x is the read vector)
                 const float4 s4 = st4p[off + lane];
                 es = make_float4(es.x * s4.x, es.y * s4.y, es.z * s4.z, es.w * s4.w);
+                if (pv.colf != nullptr) colf4 = st4p[off + 32 + lane];
             }
             const float xk[4] = {es.x * k4.x, es.y * k4.y, es.z * k4.z, es.w * k4.w};
             const float xq[4] = {es.x * q4.x, es.y * q4.y, es.z * q4.z, es.w * q4.w};
@@ -288,6 +297,10 @@ __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, 
                                      fmaf(static_cast<float>(tq), 256.0f,
                                           static_cast<float>(accq[m][0]))) * cq;
                     }
+                    // column-scale format: B Z^T (C Gamma x) / 127, the column
+                    // scales applied after the integer sums (eq. 10)
+                    rk[0] *= colf4.x, rk[1] *= colf4.y, rk[2] *= colf4.z, rk[3] *= colf4.w;
+                    rq[0] *= colf4.x, rq[1] *= colf4.y, rq[2] *= colf4.z, rq[3] *= colf4.w;
                     r01 = make_float2(rk[0], rk[1]);
                     r23 = make_float2(rk[2], rk[3]);
                     y01 = make_float2(rq[0], rq[1]);

@@ -54,6 +54,11 @@ __device__ __forceinline__ float2 code_words(float2 x, float f) {
     return __fadd2_rn(__fmul2_rn(x, make_float2(f, f)), make_float2(kRoundMagic, kRoundMagic));
 }
 
+// Codes of two values with their own factors (value columns of one row).
+__device__ __forceinline__ float2 code_words2(float2 x, float2 f) {
+    return __fadd2_rn(__fmul2_rn(x, f), make_float2(kRoundMagic, kRoundMagic));
+}
+
 // Low bytes of four words packed little-endian into one word.
 __device__ __forceinline__ uint32_t pack_low_bytes(float a, float b, float c, float d) {
     return __byte_perm(__byte_perm(__float_as_uint(a), __float_as_uint(b), 0x0040),
@@ -76,6 +81,14 @@ __device__ __forceinline__ void quad_row(uint4 qb, int r, float e, float2& lo, f
     hi = __fmul2_rn(code_values(qb.z, qb.w, r), ee);
 }
 
+// The same with per-column factors b01 (columns 0, 1) and b23 (2, 3) too.
+__device__ __forceinline__ void quad_row_cols(uint4 qb, int r, float e, float2 b01, float2 b23, float2& lo,
+                                              float2& hi) {
+    const float2 ee = make_float2(e, e);
+    lo = __fmul2_rn(__fmul2_rn(code_values(qb.x, qb.y, r), b01), ee);
+    hi = __fmul2_rn(__fmul2_rn(code_values(qb.z, qb.w, r), b23), ee);
+}
+
 // Codes of rows r0..r0+3 x 4 columns (row r = (lo[r], hi[r]) = columns
 // 0..3, with its own factor f[r - r0]) packed as one column quad (word m =
 // column m, byte r - r0 = row r).
@@ -92,10 +105,26 @@ __device__ __forceinline__ uint4 pack_quad(const float2 (&lo)[N], const float2 (
                       pack_low_bytes(b[0].x, b[1].x, b[2].x, b[3].x), pack_low_bytes(b[0].y, b[1].y, b[2].y, b[3].y));
 }
 
-// Max over the 32 lanes of each of 16 per-lane values v[0..15] (one per key
-// row), by recursive halving: 16 shuffles instead of 80.  Lane l returns the
-// max of row (l >> 1) & 15.
-__device__ __forceinline__ float warp_max16_scatter(float (&v)[16], int lane) {
+// Codes of rows r0..r0+3 x 4 columns with one factor per value column (f01 =
+// columns 0, 1; f23 = columns 2, 3), packed as one column quad.
+template <int N>
+__device__ __forceinline__ uint4 pack_quad_cols(const float2 (&lo)[N], const float2 (&hi)[N], int r0,
+                                                float2 f01, float2 f23) {
+    float2 a[4], b[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        a[r] = code_words2(lo[r0 + r], f01);
+        b[r] = code_words2(hi[r0 + r], f23);
+    }
+    return make_uint4(pack_low_bytes(a[0].x, a[1].x, a[2].x, a[3].x), pack_low_bytes(a[0].y, a[1].y, a[2].y, a[3].y),
+                      pack_low_bytes(b[0].x, b[1].x, b[2].x, b[3].x), pack_low_bytes(b[0].y, b[1].y, b[2].y, b[3].y));
+}
+
+// Reduction over the 32 lanes of each of 16 per-lane values v[0..15] (one
+// per key row), by recursive halving: 16 shuffles instead of 80.  Lane l
+// returns the result for row (l >> 1) & 15.  SUM: sum, otherwise max.
+template <bool SUM>
+__device__ __forceinline__ float warp_reduce16_scatter(float (&v)[16], int lane) {
 #pragma unroll
     for (int b = 4, h = 8; b >= 1; --b, h >>= 1) {
         const bool upper = (lane >> b) & 1;
@@ -103,10 +132,15 @@ __device__ __forceinline__ float warp_max16_scatter(float (&v)[16], int lane) {
         for (int r = 0; r < h; ++r) {
             const float send = upper ? v[r] : v[r + h];
             const float keep = upper ? v[r + h] : v[r];
-            v[r] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 1 << b));
+            const float got = __shfl_xor_sync(0xffffffffu, send, 1 << b);
+            v[r] = SUM ? keep + got : fmaxf(keep, got);
         }
     }
-    return fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], 1));
+    const float got = __shfl_xor_sync(0xffffffffu, v[0], 1);
+    return SUM ? v[0] + got : fmaxf(v[0], got);
+}
+__device__ __forceinline__ float warp_max16_scatter(float (&v)[16], int lane) {
+    return warp_reduce16_scatter<false>(v, lane);
 }
 
 // Split x (|x| <= 2^30) into 4 signed base-256 digits, x = sum_d d_d 256^d,
@@ -119,6 +153,58 @@ __device__ __forceinline__ void digits4(int x, int (&out)[4]) {
         x = (x - lo) >> 8;
     }
     out[3] = x;
+}
+
+// Smoothed per-value-column quantization ("LeapQuant: Efficient Linear
+// Attention with Accurate Recurrent State Quantization", §3.4 eq. 7, App.
+// B.3) of the 128 x 128 state a CTA holds in the fold layout: warp w has key
+// rows 16w..16w+15, lane l value columns 4l..4l+3 (lo = columns 4l, 4l+1,
+// hi = 4l+2, 4l+3).  Per key row, c = max(sqrt(mean |S|), 2^-20) (row sums
+// by a reduce-scatter), g = 1 / c, R = S g; per value column, the absmax of R
+// over all rows (shared memory across warps) gives b = B / 127 and the
+// factor f = 127 / B; codes rint(R f).  Writes the codes of state hd, c to
+// rowf[128] and b to colf[128].  red: kWarps * kD floats, fcol: kD floats of
+// shared memory.  lo / hi are overwritten with R.
+constexpr float kSmoothFloor = 9.5367431640625e-07f;  // 2^-20
+
+__device__ __forceinline__ void quantize_cols_cta(float2 (&lo)[16], float2 (&hi)[16], void* base, size_t hd,
+                                                  float* rowf, float* colf, float* red, float* fcol) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int i0 = 16 * warp;
+    float v[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r)
+        v[r] = (fabsf(lo[r].x) + fabsf(lo[r].y)) + (fabsf(hi[r].x) + fabsf(hi[r].y));
+    float c = sqrtf(warp_reduce16_scatter<true>(v, lane) * (1.0f / kD));
+    if (!(c >= kSmoothFloor)) c = kSmoothFloor;
+    const float g = __fdiv_rn(1.0f, c);
+    if ((lane & 1) == 0) rowf[i0 + (lane >> 1)] = c;
+    float4 cm = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        const float gr = __shfl_sync(0xffffffffu, g, 2 * r);
+        lo[r] = __fmul2_rn(lo[r], make_float2(gr, gr));
+        hi[r] = __fmul2_rn(hi[r], make_float2(gr, gr));
+        cm = make_float4(fmaxf(cm.x, fabsf(lo[r].x)), fmaxf(cm.y, fabsf(lo[r].y)), fmaxf(cm.z, fabsf(hi[r].x)),
+                         fmaxf(cm.w, fabsf(hi[r].y)));
+    }
+    reinterpret_cast<float4*>(red)[warp * (kD / 4) + lane] = cm;
+    __syncthreads();
+    if (tid < kD) {
+        float B = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) B = fmaxf(B, red[w * kD + tid]);
+        float b, f;
+        row_quant_params(B, b, f);
+        colf[tid] = b;
+        fcol[tid] = f;
+    }
+    __syncthreads();
+    const float4 f4 = reinterpret_cast<const float4*>(fcol)[lane];
+#pragma unroll
+    for (int qd = 0; qd < 4; ++qd)
+        reinterpret_cast<uint4*>(base)[quad_index(hd, i0 / 4 + qd, lane)] =
+            pack_quad_cols(lo, hi, 4 * qd, make_float2(f4.x, f4.y), make_float2(f4.z, f4.w));
 }
 
 enum FoldMode : int { kFoldCommit = 0, kFoldRead = 1, kFoldStep = 2 };
@@ -345,8 +431,16 @@ __device__ bool fold_cta(const PoolView& pv, size_t hd, int n, const float* lbg,
             q.y ^= 0x80808080u;
             q.z ^= 0x80808080u;
             q.w ^= 0x80808080u;
+            if (pv.colf != nullptr) {
+                const float4 b4 = ldcg4(pv.colf + hd * kD + 4 * lane);
+                const float2 b01 = make_float2(b4.x, b4.y), b23 = make_float2(b4.z, b4.w);
 #pragma unroll
-            for (int r = 0; r < 4; ++r) quad_row(q, r, e[4 * qd + r], lo[4 * qd + r], hi[4 * qd + r]);
+                for (int r = 0; r < 4; ++r)
+                    quad_row_cols(q, r, e[4 * qd + r], b01, b23, lo[4 * qd + r], hi[4 * qd + r]);
+            } else {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) quad_row(q, r, e[4 * qd + r], lo[4 * qd + r], hi[4 * qd + r]);
+            }
         } else {
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
@@ -515,6 +609,10 @@ __device__ bool fold_cta(const PoolView& pv, size_t hd, int n, const float* lbg,
         for (int r = 0; r < 16; ++r)
             st4(reinterpret_cast<float*>(pv.base) + hd * (kD * kD) + (i0 + r) * kD + 4 * lane,
                 make_float4(lo[r].x, lo[r].y, hi[r].x, hi[r].y));
+    } else if (pv.colf != nullptr) {
+        __syncthreads();  // the staged chunks are consumed: their area holds the column maxima
+        quantize_cols_cta(lo, hi, pv.base, hd, pv.scale + hd * kD, pv.colf + hd * kD,
+                          reinterpret_cast<float*>(fs.a2), fs.kv);
     } else {
         // per-row absmax over the 128 columns (warp-wide), one division pair
         // per row in the lane that holds it, factors broadcast back

@@ -40,9 +40,10 @@ def _need(t: torch.Tensor, name: str, dtype, device, shape=None):
 
 
 def required_bytes(num_slots, num_heads, variant="eager", gate="scalar", window=0,
-                   d_k=128, d_v=128) -> int:
+                   d_k=128, d_v=128, col_scales=False) -> int:
     lib = N.load()
-    d = N.LsDesc(num_slots, num_heads, d_k, d_v, VARIANTS[variant], GATES[gate], window, 0)
+    d = N.LsDesc(num_slots, num_heads, d_k, d_v, VARIANTS[variant], GATES[gate], window,
+                 N.LS_INT8_COLUMN_SCALES if col_scales else 0)
     out = C.c_size_t(0)
     N.check(lib.ls_pool_required_bytes(C.byref(d), C.byref(out)), "ls_pool_required_bytes")
     return int(out.value)
@@ -52,13 +53,15 @@ class StatePool:
     """``num_slots`` x ``num_heads`` recurrent states of one layer on one GPU.
 
     variant: "eager" (dense FP32), "deferred" (FP32 base + log, merge interval
-    ``window``) or "int8" (INT8 base with per-key-row scales, window ``window``).
+    ``window``) or "int8" (INT8 base, window ``window``).
     gate: "scalar" (Gated DeltaNet) or "per_key" (KDA).
+    col_scales (int8): the smoothed per-value-column format (LeapQuant §3.4
+    eq. 7, App. B.3) instead of one scale per key row.
     """
 
     def __init__(self, num_slots: int, num_heads: int, variant: str = "eager",
                  gate: str = "scalar", window: int = 0, d_k: int = 128, d_v: int = 128,
-                 device=None, stream=None):
+                 device=None, stream=None, col_scales: bool = False):
         self.lib = N.load()
         self.variant, self.gate = variant, gate
         self.P, self.H, self.d_k, self.d_v = int(num_slots), int(num_heads), int(d_k), int(d_v)
@@ -70,8 +73,9 @@ class StatePool:
         if dev.index is None:
             dev = torch.device("cuda", torch.cuda.current_device())
         self.device = dev
+        self.col_scales = bool(col_scales)
         self.desc = N.LsDesc(self.P, self.H, self.d_k, self.d_v, VARIANTS[variant], GATES[gate],
-                             self.window, 0)
+                             self.window, N.LS_INT8_COLUMN_SCALES if self.col_scales else 0)
         nbytes = C.c_size_t(0)
         N.check(self.lib.ls_pool_required_bytes(C.byref(self.desc), C.byref(nbytes)),
                 "ls_pool_required_bytes")
@@ -181,7 +185,8 @@ class StatePool:
                                              C.c_void_p(_stream(stream))), "ls_pool_reset_slots")
 
     def read_int8(self, slots, stream=None):
-        """(codes [n, H, d_k, d_v] int8, scales [n, H, d_k] float32) of the INT8 base."""
+        """(codes [n, H, d_k, d_v] int8, key-row factors [n, H, d_k] float32) of
+        the INT8 base: per-row scales, or the smoothing factors c (col_scales)."""
         slots = self._slots(slots)
         n = int(slots.numel())
         codes = torch.empty(n, self.H, self.d_k, self.d_v, dtype=torch.int8, device=self.device)
@@ -190,6 +195,16 @@ class StatePool:
                                            _ptr(scales), C.c_void_p(_stream(stream))),
                 "ls_pool_read_int8")
         return codes, scales
+
+    def read_int8_col_scales(self, slots, stream=None):
+        """col_scales pools: the per-value-column scales b [n, H, d_v] float32."""
+        slots = self._slots(slots)
+        n = int(slots.numel())
+        b = torch.empty(n, self.H, self.d_v, dtype=torch.float32, device=self.device)
+        N.check(self.lib.ls_pool_read_int8_col_scales(self.handle, _ptr(slots), n, _ptr(b),
+                                                      C.c_void_p(_stream(stream))),
+                "ls_pool_read_int8_col_scales")
+        return b
 
     def read_log_meta(self, slots, stream=None):
         """(live log length [n, H] int32, cumulative log-decay [n, H, dl] float32)."""

@@ -14,13 +14,13 @@ from recurrent_state_quantization_gb300 import workloads as wl
 D = 128
 
 
-def make_oracle(variant, nstates, dl, window, nthreads=0):
+def make_oracle(variant, nstates, dl, window, nthreads=0, col_scales=False):
     if variant == "eager":
         return oracle.EagerOracle(nstates, D, D, dl, nthreads)
     if variant == "deferred":
         return oracle.DeferredOracle(nstates, D, D, dl, window, nthreads)
     if variant == "int8":
-        return oracle.WindowInt8Oracle(nstates, D, D, dl, window, nthreads)
+        return oracle.WindowInt8Oracle(nstates, D, D, dl, window, nthreads, col_scales=col_scales)
     raise ValueError(variant)
 
 
@@ -68,11 +68,14 @@ class Pair:
     """A GPU pool and an oracle stepped together over a workload."""
 
     def __init__(self, w: wl.Workload, variant: str, window: int, n_sample=None, device="cuda",
-                 seed=0, nthreads=0):
+                 seed=0, nthreads=0, col_scales=False):
         self.w, self.variant, self.window = w, variant, window
+        self.col_scales = bool(col_scales)
         self.dev = torch.device(device)
-        self.pool = StatePool(w.num_slots, w.heads, variant, w.gate, window, device=self.dev)
-        self.orc = make_oracle(variant, w.num_slots * w.heads, w.dl, window, nthreads)
+        self.pool = StatePool(w.num_slots, w.heads, variant, w.gate, window, device=self.dev,
+                              col_scales=col_scales)
+        self.orc = make_oracle(variant, w.num_slots * w.heads, w.dl, window, nthreads,
+                               col_scales=col_scales)
         self.slot_idx = wl.slot_index(w, self.dev)
         self.sample = sample_rows(w, self.slot_idx, n_sample, seed)
         self.masks = wl.static_masks(w, self.dev)
@@ -142,6 +145,31 @@ class Pair:
         for n_, r in enumerate(s.rows):
             g = S[pos[int(slots_b[n_])], r % w.heads]
             worst = max(worst, relmax(g, So[n_]))
+        return worst
+
+    def factor_err(self):
+        """INT8: max relative error of the key-row factors (scales or smoothing
+        factors c) and, for the column format, of the column scales b, over
+        the sampled heads."""
+        w, s = self.w, self.sample
+        slots_b = self.slot_idx.cpu().numpy()[s.rows // w.heads]
+        uniq = np.unique(slots_b)
+        ut = torch.as_tensor(uniq, dtype=torch.int32, device=self.dev)
+        _, fr = self.pool.read_int8(ut)
+        fr = fr.cpu().numpy()
+        fc = self.pool.read_int8_col_scales(ut).cpu().numpy() if self.col_scales else None
+        pos = {int(x): i for i, x in enumerate(uniq)}
+        _, fro = self.orc.codes(s.state_idx)
+        fco = self.orc.col_factors(s.state_idx)
+        worst = 0.0
+        for n_, r in enumerate(s.rows):
+            g = fr[pos[int(slots_b[n_])], r % w.heads].astype(np.float64)
+            o = fro[n_].astype(np.float64)
+            worst = max(worst, float(np.max(np.abs(g - o) / np.maximum(np.abs(o), 1e-30))))
+            if fc is not None:
+                g = fc[pos[int(slots_b[n_])], r % w.heads].astype(np.float64)
+                o = fco[n_].astype(np.float64)
+                worst = max(worst, float(np.max(np.abs(g - o) / np.maximum(np.abs(o), 1e-30))))
         return worst
 
     def code_mismatch(self):

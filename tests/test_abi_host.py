@@ -75,10 +75,25 @@ def test_required_bytes_layout(lib):
 @pytest.mark.parametrize("field,value,code", [
     ("d_k", 64, -5), ("d_v", 256, -5), ("window", 0, -5), ("window", 257, -5),
     ("variant", 3, -1), ("gate", 2, -1), ("num_slots", 0, -1), ("num_heads", -1, -1),
-    ("flags", 1, -1)])
+    ("flags", 2, -1), ("flags", 0x80000000, -1)])
 def test_bad_descriptors(lib, field, value, code):
     rc, _ = _bytes(lib, _desc(**{field: value}))
     assert rc == code
+
+
+def test_column_scale_flag(lib):
+    """LS_INT8_COLUMN_SCALES: INT8 pools only; one more [P*H][d_v] FP32 array
+    (the value-column scales) after the key-row factors."""
+    from recurrent_state_quantization_gb300 import _native as N
+    P, Hh = 4, 2
+    nh = P * Hh
+    al = lambda x: (x + 255) // 256 * 256
+    rc0, b0 = _bytes(lib, _desc())
+    rc1, b1 = _bytes(lib, _desc(flags=N.LS_INT8_COLUMN_SCALES))
+    assert rc0 == 0 and rc1 == 0 and b1 == b0 + al(nh * 128 * 4)
+    for variant in (N.LS_EAGER_FP32, N.LS_DEFERRED_FP32):
+        rc, _ = _bytes(lib, _desc(variant=variant, flags=N.LS_INT8_COLUMN_SCALES))
+        assert rc == N.LS_ERR_INVALID
 
 
 def test_eager_ignores_window(lib):
@@ -107,7 +122,8 @@ def test_error_strings(lib):
     for code in (0, -1, -2, -3, -4, -5, -99):
         s = lib.ls_error_string(code)
         assert isinstance(s, bytes) and len(s) > 0
-    assert lib.ls_abi_version() == 1
+    from recurrent_state_quantization_gb300 import _native as N
+    assert lib.ls_abi_version() == N.LS_ABI_VERSION == 2
 
 
 def test_product_path_does_not_import_the_oracle():

@@ -48,6 +48,12 @@ def check_fp32(p, where=""):
     return ye, se
 
 
+# key-row / column factors at a window end are functions (absmax, row mean)
+# of each side's own end-of-window state, which agree within the FP32
+# tolerance; at a restart both sides quantize the same FP32 state
+FACTOR_TOL = FP32_TOL
+
+
 def run_lockstep(p, tokens, pool_id=0, code_checks=None):
     """Step every token; for INT8 restart each window from the oracle's state
     on both sides and check the codes at its end."""
@@ -61,6 +67,8 @@ def run_lockstep(p, tokens, pool_id=0, code_checks=None):
                 code_checks.append((t, frac, mx))
             assert mx <= 1, f"token {t}: codes differ by {mx} LSB"
             assert frac <= CODE_FRAC_TOL, f"token {t}: {frac:.3g} of codes differ"
+            fe = p.factor_err()
+            assert fe <= FACTOR_TOL, f"token {t}: scale / smoothing factors rel err {fe:.3g}"
 
 
 def check_int8(p):
@@ -96,14 +104,15 @@ CASES = [("eager", 0), ("deferred", 1), ("deferred", 3), ("deferred", 16),
 
 
 @pytest.mark.parametrize("gate", ["scalar", "per_key"])
-@pytest.mark.parametrize("variant,window", CASES)
-def test_small_ragged(gate, variant, window):
+@pytest.mark.parametrize("variant,window,cols", [c + (False,) for c in CASES] +
+                         [("int8", 1, True), ("int8", 3, True), ("int8", 16, True)])
+def test_small_ragged(gate, variant, window, cols):
     from recurrent_state_quantization_gb300 import workloads as wl
     H = _harness()
     w = wl.custom("ragged", gate=gate, batch=5, heads=3, tokens=37, num_slots=7,
                   windows=(max(window, 1),), merge_interval=max(window, 1), permute_slots=True,
                   seed=11 + window, lam_scale=0.3)
-    p = H.Pair(w, variant, window)
+    p = H.Pair(w, variant, window, col_scales=cols)
     run_lockstep(p, w.tokens)
     if variant == "int8":
         check_int8(p)
@@ -119,14 +128,14 @@ def test_small_ragged(gate, variant, window):
 # full-size workloads, sampled heads
 # ---------------------------------------------------------------------------
 
-def _full(wi, variant, window, n_sample, tokens=None, pools=1, prewarm=None):
+def _full(wi, variant, window, n_sample, tokens=None, pools=1, prewarm=None, cols=False):
     from recurrent_state_quantization_gb300 import workloads as wl
     H = _harness()
     w = wl.WORKLOADS[wi]
     T = w.tokens if tokens is None else tokens
     results = []
     for pool_id in range(pools):
-        p = H.Pair(w, variant, window, n_sample=n_sample, seed=pool_id)
+        p = H.Pair(w, variant, window, n_sample=n_sample, seed=pool_id, col_scales=cols)
         if prewarm is not None:
             prewarm(p, pool_id)
         checks = []
@@ -137,6 +146,7 @@ def _full(wi, variant, window, n_sample, tokens=None, pools=1, prewarm=None):
             if variant == "int8" and (t + 1) % window == 0:
                 frac, mx = p.code_mismatch()
                 checks.append((t, frac, mx))
+                assert p.factor_err() <= FACTOR_TOL, t
         results.append((p, checks))
     return results
 
@@ -157,9 +167,10 @@ def test_gdn_pool_b64_h48_t1024_outliers(variant, window):
     _assert_full(_full(1, variant, window, n_sample=24), variant)
 
 
-@pytest.mark.parametrize("variant,window", [("eager", 0), ("deferred", 16), ("int8", 32)])
-def test_kda_b128_h32_t512_longlived(variant, window):
-    _assert_full(_full(2, variant, window, n_sample=16), variant)
+@pytest.mark.parametrize("variant,window,cols", [("eager", 0, False), ("deferred", 16, False),
+                                                 ("int8", 32, False), ("int8", 32, True)])
+def test_kda_b128_h32_t512_longlived(variant, window, cols):
+    _assert_full(_full(2, variant, window, n_sample=16, cols=cols), variant)
 
 
 def _prewarm_factory(tokens):
@@ -184,13 +195,14 @@ def _prewarm_factory(tokens):
     return prewarm
 
 
-@pytest.mark.parametrize("variant,window", [("eager", 0), ("deferred", 16), ("int8", 8),
-                                            ("int8", 16), ("int8", 32), ("int8", 64),
-                                            ("int8", 128)])
-def test_gdn_serving_b256_h48_4pools(variant, window):
+@pytest.mark.parametrize("variant,window,cols", [("eager", 0, False), ("deferred", 16, False),
+                                                 ("int8", 8, False), ("int8", 16, False),
+                                                 ("int8", 32, False), ("int8", 64, False),
+                                                 ("int8", 128, False), ("int8", 16, True)])
+def test_gdn_serving_b256_h48_4pools(variant, window, cols):
     from recurrent_state_quantization_gb300 import workloads as wl
     w = wl.WORKLOADS[3]
-    _assert_full(_full(3, variant, window, n_sample=6, pools=w.pools,
+    _assert_full(_full(3, variant, window, n_sample=6, pools=w.pools, cols=cols,
                        prewarm=_prewarm_factory(w.prewarm_tokens)), variant)
 
 
