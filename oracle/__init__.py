@@ -45,18 +45,19 @@ def _load():
         lib.orc_quantize_rows.argtypes = [I64, I32, I32, P, P, P]
         lib.orc_dequantize_rows.argtypes = [I64, I32, I32, P, P, P]
         lib.orc_quantize_cols.argtypes = [I64, I32, I32, P, P, P, P]
+        lib.orc_fit_compensators.argtypes = [I64, I32, I32, I32, P, P, P, I32]
         lib.orc_dequantize_cols.argtypes = [I64, I32, I32, P, P, P, P]
-        lib.orc_window_step.argtypes = [I64, I32, I32, I32, I32, I32, P, P, P, P, P, P,
-                                        P, P, P, P, P, P, P, P, P, I32]
-        lib.orc_window_commit.argtypes = [I64, I32, I32, I32, P, P, P, P, P, P]
-        lib.orc_window_load.argtypes = [I64, I32, I32, I32, P, P, P, P, P, P, P]
-        lib.orc_window_unrolled.argtypes = [I64, I32, I32, I32, I32, I32, P, P, P, P, P, P,
-                                            P, P, P]
-        lib.orc_window_readout.argtypes = [I64, I32, I32, I32, I32, I32, P, P, P, P, P, P,
-                                           P, P, P, P]
+        lib.orc_window_step.argtypes = [I64, I32, I32, I32, I32, I32, I32, P, P, P, P, P,
+                                        P, P, P, P, P, P, P, P, P, P, P, P, I32]
+        lib.orc_window_commit.argtypes = [I64, I32, I32, I32, I32, P, P, P, P, P, P, P, P]
+        lib.orc_window_load.argtypes = [I64, I32, I32, I32, I32, P, P, P, P, P, P, P, P, P]
+        lib.orc_window_unrolled.argtypes = [I64, I32, I32, I32, I32, I32, I32, P, P, P, P, P,
+                                            P, P, P, P, P, P]
+        lib.orc_window_readout.argtypes = [I64, I32, I32, I32, I32, I32, I32, P, P, P, P, P,
+                                           P, P, P, P, P, P, P]
         for name in ("orc_eager_step", "orc_deferred_step", "orc_deferred_logical",
                      "orc_deferred_commit", "orc_quantize_rows", "orc_dequantize_rows",
-                     "orc_quantize_cols", "orc_dequantize_cols",
+                     "orc_quantize_cols", "orc_dequantize_cols", "orc_fit_compensators",
                      "orc_window_step", "orc_window_commit", "orc_window_load",
                      "orc_window_unrolled", "orc_window_readout"):
             getattr(lib, name).restype = I32
@@ -202,14 +203,19 @@ class WindowInt8Oracle(_Base):
 
     col_scales=False: one FP32 scale per key row.  col_scales=True: the
     smoothed per-value-column format of LeapQuant §3.4 eq. 7 / App. B.3
-    (row factors = smoothing vector c, column factors = scales b)."""
+    (row factors = smoothing vector c, column factors = scales b).
+    compensators=r: r Compensator Tokens (LeapQuant §3.3) fitted at every
+    boundary; the residual is what is quantized."""
 
-    def __init__(self, nstates, dk, dv, dl, W, nthreads=0, col_scales=False):
+    def __init__(self, nstates, dk, dv, dl, W, nthreads=0, col_scales=False, compensators=0):
         super().__init__(nstates, dk, dv, dl, nthreads)
         if W < 1:
             raise ValueError("W >= 1")
         self.W = int(W)
         self.mode = 1 if col_scales else 0
+        self.r = int(compensators)
+        self.ck = np.zeros((self.n, max(self.r, 1), dk), dtype=np.float64)
+        self.cu = np.zeros((self.n, max(self.r, 1), dv), dtype=np.float64)
         self.Z = np.zeros((self.n, dk, dv), dtype=np.int8)
         self.s = np.zeros((self.n, dk), dtype=np.float32)
         self.fc = np.zeros((self.n, dv), dtype=np.float32)
@@ -223,8 +229,9 @@ class WindowInt8Oracle(_Base):
         idx = self._idx(idx)
         q, k, v, lam, beta = self._inputs(idx, q, k, v, lam, beta)
         y = np.zeros((idx.size, self.dv), dtype=np.float64)
-        _check(_load().orc_window_step(idx.size, self.mode, self.dk, self.dv, self.dl, self.W,
-                                       _p(self.Z), _p(self.s), _p(self.fc), _p(self.Sw),
+        _check(_load().orc_window_step(idx.size, self.mode, self.r, self.dk, self.dv, self.dl,
+                                       self.W, _p(self.Z), _p(self.s), _p(self.fc),
+                                       _p(self.ck), _p(self.cu), _p(self.Sw),
                                        _p(self.rl),
                                        _p(self.rk), _p(self.ru), _p(self.cnt), _p(idx),
                                        _p(q), _p(k), _p(v), _p(lam), _p(beta), _p(y),
@@ -244,19 +251,25 @@ class WindowInt8Oracle(_Base):
         """The per-value-column scales b (smoothed format; zeros otherwise)."""
         return self.fc[self._idx(idx)].copy()
 
+    def compensators(self, idx):
+        """The current window's compensator pairs (K~ [n, r, dk], U~ [n, r, dv])."""
+        idx = self._idx(idx)
+        return self.ck[idx, :self.r].copy(), self.cu[idx, :self.r].copy()
+
     def commit(self, idx):
         idx = self._idx(idx)
-        _check(_load().orc_window_commit(idx.size, self.mode, self.dk, self.dv, _p(self.Z),
-                                         _p(self.s), _p(self.fc), _p(self.Sw), _p(self.cnt),
-                                         _p(idx)), "window commit")
+        _check(_load().orc_window_commit(idx.size, self.mode, self.r, self.dk, self.dv,
+                                         _p(self.Z), _p(self.s), _p(self.fc), _p(self.ck),
+                                         _p(self.cu), _p(self.Sw), _p(self.cnt), _p(idx)),
+               "window commit")
 
     def load(self, idx, S):
         idx = self._idx(idx)
         S = np.ascontiguousarray(np.asarray(S, dtype=np.float64).reshape(idx.size, self.dk,
                                                                           self.dv))
-        _check(_load().orc_window_load(idx.size, self.mode, self.dk, self.dv, _p(S),
-                                       _p(self.Z), _p(self.s), _p(self.fc), _p(self.Sw),
-                                       _p(self.cnt), _p(idx)),
+        _check(_load().orc_window_load(idx.size, self.mode, self.r, self.dk, self.dv, _p(S),
+                                       _p(self.Z), _p(self.s), _p(self.fc), _p(self.ck),
+                                       _p(self.cu), _p(self.Sw), _p(self.cnt), _p(idx)),
                "window load")
 
     def reset(self, idx):
@@ -266,9 +279,9 @@ class WindowInt8Oracle(_Base):
         """S_l rebuilt from the boundary state and the buffered records (eq. 4)."""
         idx = self._idx(idx)
         out = np.zeros((idx.size, self.dk, self.dv), dtype=np.float64)
-        _check(_load().orc_window_unrolled(idx.size, self.mode, self.dk, self.dv, self.dl,
-                                           self.W, _p(self.Z), _p(self.s), _p(self.fc),
-                                           _p(self.rl), _p(self.rk),
+        _check(_load().orc_window_unrolled(idx.size, self.mode, self.r, self.dk, self.dv,
+                                           self.dl, self.W, _p(self.Z), _p(self.s), _p(self.fc),
+                                           _p(self.ck), _p(self.cu), _p(self.rl), _p(self.rk),
                                            _p(self.ru), _p(self.cnt), _p(idx), _p(out)),
                "window unrolled")
         return out
@@ -278,9 +291,9 @@ class WindowInt8Oracle(_Base):
         idx = self._idx(idx)
         x = np.ascontiguousarray(np.asarray(x, dtype=np.float64).reshape(idx.size, self.dk))
         out = np.zeros((idx.size, self.dv), dtype=np.float64)
-        _check(_load().orc_window_readout(idx.size, self.mode, self.dk, self.dv, self.dl,
-                                          self.W, _p(self.Z), _p(self.s), _p(self.fc),
-                                          _p(self.rl), _p(self.rk),
+        _check(_load().orc_window_readout(idx.size, self.mode, self.r, self.dk, self.dv,
+                                          self.dl, self.W, _p(self.Z), _p(self.s), _p(self.fc),
+                                          _p(self.ck), _p(self.cu), _p(self.rl), _p(self.rk),
                                           _p(self.ru), _p(self.cnt), _p(idx), _p(x), _p(out)),
                "window readout")
         return out
@@ -335,5 +348,22 @@ def dequantize_cols(Z, c, b):
     return S
 
 
+def fit_compensators(S, r, warm_cu=None):
+    """LeapQuant §3.3 Compensator Tokens fitted to S [..., dk, dv] by the
+    oracle's power iteration: returns (residual, K~ [..., r, dk], U~ [..., r, dv])."""
+    S = np.array(S, dtype=np.float64, copy=True, order="C")
+    lead = S.shape[:-2]
+    dk, dv = S.shape[-2:]
+    n = int(np.prod(lead)) if lead else 1
+    ck = np.zeros(lead + (r, dk), dtype=np.float64)
+    cu = np.zeros(lead + (r, dv), dtype=np.float64)
+    if warm_cu is not None:
+        cu[...] = warm_cu
+    _check(_load().orc_fit_compensators(n, int(r), dk, dv, _p(S), _p(ck), _p(cu),
+                                        1 if warm_cu is not None else 0), "fit compensators")
+    return S, ck, cu
+
+
 __all__ = ["EagerOracle", "DeferredOracle", "WindowInt8Oracle", "quantize_rows",
-           "dequantize_rows", "quantize_cols", "dequantize_cols", "max_threads", "build_oracle"]
+           "dequantize_rows", "quantize_cols", "dequantize_cols", "fit_compensators",
+           "max_threads", "build_oracle"]

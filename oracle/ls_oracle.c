@@ -508,6 +508,88 @@ static void dequant_mode(int mode, int dk, int dv, const int8_t *Z,
     else dequant_rows(dk, dv, Z, fr, S);
 }
 
+/*
+ * Compensator Tokens, [LQ] §3.3 eq. 5-6: r rank-one pairs (k~_h, u~_h)
+ * fitted to the state before quantization, fitted by power iteration (§4.1).
+ * Readings (the pages give neither): sequential deflation, h = 1..r, each
+ * fit on the residual left by the previous ones; COMP_ITERS power steps
+ *     v <- R^T (R v) / ||R^T (R v)||     (v kept if the norm is 0)
+ * from a warm start, the previous window's u~_h when it is nonzero (the
+ * state moves little in a window), else the all-ones vector / sqrt(dv);
+ * then k~_h = R v, u~_h = v (unit), R <- R - k~_h u~_h^T.
+ */
+#define COMP_ITERS 2
+
+static void fit_compensators(int r, int dk, int dv, double *R, double *ck,
+                             double *cu, int warm)
+{
+    double v[1024], z[1024], w[1024];
+    for (int h = 0; h < r; ++h) {
+        double *u = cu + (size_t)h * dv, *kk = ck + (size_t)h * dk;
+        double nv = 0.0;
+        if (warm)
+            for (int j = 0; j < dv; ++j) nv += u[j] * u[j];
+        for (int j = 0; j < dv; ++j)
+            v[j] = nv > 0.0 ? u[j] / sqrt(nv) : 1.0 / sqrt((double)dv);
+        for (int it = 0; it < COMP_ITERS; ++it) {
+            for (int i = 0; i < dk; ++i) {
+                double a = 0.0;
+                for (int j = 0; j < dv; ++j) a += R[(size_t)i * dv + j] * v[j];
+                w[i] = a;
+            }
+            double nz = 0.0;
+            for (int j = 0; j < dv; ++j) {
+                double a = 0.0;
+                for (int i = 0; i < dk; ++i) a += R[(size_t)i * dv + j] * w[i];
+                z[j] = a;
+                nz += a * a;
+            }
+            if (nz > 0.0)
+                for (int j = 0; j < dv; ++j) v[j] = z[j] / sqrt(nz);
+        }
+        for (int i = 0; i < dk; ++i) {
+            double a = 0.0;
+            for (int j = 0; j < dv; ++j) a += R[(size_t)i * dv + j] * v[j];
+            kk[i] = a;
+        }
+        for (int j = 0; j < dv; ++j) u[j] = v[j];
+        for (int i = 0; i < dk; ++i)
+            for (int j = 0; j < dv; ++j) R[(size_t)i * dv + j] -= kk[i] * u[j];
+    }
+}
+
+/* The fit alone, for n states: S [n][dk][dv] in, the residual out; ck, cu
+ * [n][r][dk], [n][r][dv] (cu is also the warm start when warm != 0). */
+int orc_fit_compensators(int64_t n, int r, int dk, int dv, double *S,
+                         double *ck, double *cu, int warm)
+{
+    if (n < 0 || r < 1 || r > 64 || dk <= 0 || dv <= 0 || dk > 1024 || dv > 1024)
+        return ORC_ERR_ARG;
+#pragma omp parallel for schedule(static)
+    for (int64_t h = 0; h < n; ++h)
+        fit_compensators(r, dk, dv, S + (size_t)h * dk * dv, ck + (size_t)h * r * dk,
+                         cu + (size_t)h * r * dv, warm);
+    return ORC_OK;
+}
+
+/*
+ * A window boundary, [LQ] eq. 4 with §3.3 eq. 6 and §3.4 eq. 7: S (the
+ * state reached, in place) -> fit r compensator pairs to it, quantize the
+ * residual R = S - K~ U~^T in the pool's format, and restart the window
+ * from dequant(R-hat) + K~ U~^T.  r = 0: plain quantization of S.
+ */
+static void boundary(int mode, int r, int dk, int dv, double *S, int8_t *Z,
+                     float *s, float *fc, double *ck, double *cu, int warm)
+{
+    if (r > 0) fit_compensators(r, dk, dv, S, ck, cu, warm);
+    quant_mode(mode, dk, dv, S, Z, s, fc);
+    dequant_mode(mode, dk, dv, Z, s, fc, S);
+    for (int h = 0; h < r; ++h)
+        for (int i = 0; i < dk; ++i)
+            for (int j = 0; j < dv; ++j)
+                S[(size_t)i * dv + j] += ck[(size_t)h * dk + i] * cu[(size_t)h * dv + j];
+}
+
 int orc_quantize_rows(int64_t n, int dk, int dv, const double *S, int8_t *Z,
                       float *s)
 {
@@ -575,10 +657,12 @@ int orc_dequantize_cols(int64_t n, int dk, int dv, const int8_t *Z,
  *     y_i = S_i^T q_i                       (read before any quantization)
  *     buffer (alpha_i, k_i, u_i)
  *     at the W-th record: S-hat <- quant_8(S_W), S_W <- dequant(S-hat),
- *     empty the buffer (quant_8 / dequant of the pool's format, `mode`).
+ *     empty the buffer (quant_8 / dequant of the pool's format, `mode`;
+ *     with nc compensator pairs, the boundary of §3.3, see boundary()).
+ *   ck   [nc*dk], cu [nc*dv] double: the window's compensator pairs.
  */
-static void window_one(int mode, int dk, int dv, int dl, int W, int8_t *Z,
-                       float *s, float *fc,
+static void window_one(int mode, int nc, int dk, int dv, int dl, int W,
+                       int8_t *Z, float *s, float *fc, double *ck, double *cu,
                        double *Sw, double *rl, double *rk, double *ru,
                        int32_t *cntp, const float *q, const float *k,
                        const float *v, const float *lam, float beta,
@@ -591,30 +675,32 @@ static void window_one(int mode, int dk, int dv, int dl, int W, int8_t *Z,
     for (int i = 0; i < dk; ++i) rk[(size_t)c * dk + i] = (double)k[i];
     for (int j = 0; j < dv; ++j) ru[(size_t)c * dv + j] = u[j];
     if (c + 1 == W) {
-        quant_mode(mode, dk, dv, Sw, Z, s, fc);
-        dequant_mode(mode, dk, dv, Z, s, fc, Sw);
+        boundary(mode, nc, dk, dv, Sw, Z, s, fc, ck, cu, 1);
         *cntp = 0;
     } else {
         *cntp = c + 1;
     }
 }
 
-static int window_args_ok(int mode, int dk, int dv, int dl, int W)
+static int window_args_ok(int mode, int r, int dk, int dv, int dl, int W)
 {
     return valid_dims(dk, dv, dl) && W >= 1 && dk <= 1024 && dv <= 1024 &&
-           (mode == 0 || mode == 1);
+           (mode == 0 || mode == 1) && r >= 0 && r <= 64;
 }
 
-/* fc: the column factors ([n_states][dv]); may be NULL in mode 0. */
-int orc_window_step(int64_t n, int mode, int dk, int dv, int dl, int W,
-                    int8_t *Z, float *s, float *fc, double *Sw, double *rl,
-                    double *rk, double *ru,
+/* fc: the column factors ([n_states][dv]); may be NULL in mode 0.  ck, cu:
+ * [n_states][nc][dk], [n_states][nc][dv] (nc compensator pairs); may be NULL
+ * when nc = 0. */
+int orc_window_step(int64_t n, int mode, int nc, int dk, int dv, int dl, int W,
+                    int8_t *Z, float *s, float *fc, double *ck, double *cu,
+                    double *Sw, double *rl, double *rk, double *ru,
                     int32_t *cnt, const int64_t *idx, const float *q,
                     const float *k, const float *v, const float *lam,
                     const float *beta, double *y, int nthreads)
 {
-    if (n < 0 || !window_args_ok(mode, dk, dv, dl, W)) return ORC_ERR_ARG;
-    if (mode == 1 && fc == NULL) return ORC_ERR_ARG;
+    if (n < 0 || !window_args_ok(mode, nc, dk, dv, dl, W)) return ORC_ERR_ARG;
+    if ((mode == 1 && fc == NULL) || (nc > 0 && (ck == NULL || cu == NULL)))
+        return ORC_ERR_ARG;
     if (n == 0) return ORC_OK;
     set_threads(nthreads);
     int err = 0;
@@ -628,8 +714,10 @@ int orc_window_step(int64_t n, int mode, int dk, int dv, int dl, int W,
 #pragma omp for schedule(dynamic, 4)
             for (int64_t row = 0; row < n; ++row) {
                 const int64_t h = idx[row];
-                window_one(mode, dk, dv, dl, W, Z + (size_t)h * dk * dv,
+                window_one(mode, nc, dk, dv, dl, W, Z + (size_t)h * dk * dv,
                            s + (size_t)h * dk, mode ? fc + (size_t)h * dv : NULL,
+                           nc ? ck + (size_t)h * nc * dk : NULL,
+                           nc ? cu + (size_t)h * nc * dv : NULL,
                            Sw + (size_t)h * dk * dv,
                            rl + (size_t)h * W * dl, rk + (size_t)h * W * dk,
                            ru + (size_t)h * W * dv, cnt + h, q + row * dk,
@@ -643,43 +731,42 @@ int orc_window_step(int64_t n, int mode, int dk, int dv, int dl, int W,
 }
 
 /* Close the current window early: quantize S_i, start a new window. */
-int orc_window_commit(int64_t n, int mode, int dk, int dv, int8_t *Z,
-                      float *s, float *fc, double *Sw, int32_t *cnt,
-                      const int64_t *idx)
+int orc_window_commit(int64_t n, int mode, int r, int dk, int dv, int8_t *Z,
+                      float *s, float *fc, double *ck, double *cu, double *Sw,
+                      int32_t *cnt, const int64_t *idx)
 {
-    if (n < 0 || dk <= 0 || dv <= 0 || dv > 1024 || (mode != 0 && mode != 1) ||
-        (mode == 1 && fc == NULL))
+    if (n < 0 || !window_args_ok(mode, r, dk, dv, 1, 1) ||
+        (mode == 1 && fc == NULL) || (r > 0 && (ck == NULL || cu == NULL)))
         return ORC_ERR_ARG;
 #pragma omp parallel for schedule(static)
     for (int64_t row = 0; row < n; ++row) {
         const int64_t h = idx[row];
         if (cnt[h] == 0) continue;
-        float *fch = mode ? fc + (size_t)h * dv : NULL;
-        quant_mode(mode, dk, dv, Sw + (size_t)h * dk * dv, Z + (size_t)h * dk * dv,
-                   s + (size_t)h * dk, fch);
-        dequant_mode(mode, dk, dv, Z + (size_t)h * dk * dv, s + (size_t)h * dk, fch,
-                     Sw + (size_t)h * dk * dv);
+        boundary(mode, r, dk, dv, Sw + (size_t)h * dk * dv, Z + (size_t)h * dk * dv,
+                 s + (size_t)h * dk, mode ? fc + (size_t)h * dv : NULL,
+                 r ? ck + (size_t)h * r * dk : NULL, r ? cu + (size_t)h * r * dv : NULL, 1);
         cnt[h] = 0;
     }
     return ORC_OK;
 }
 
 /* Start a window from a given state: S-hat_0 = quant_8(S). */
-int orc_window_load(int64_t n, int mode, int dk, int dv, const double *S,
-                    int8_t *Z, float *s, float *fc, double *Sw, int32_t *cnt,
-                    const int64_t *idx)
+/* (A load starts the compensator fit from the all-ones vector.) */
+int orc_window_load(int64_t n, int mode, int r, int dk, int dv, const double *S,
+                    int8_t *Z, float *s, float *fc, double *ck, double *cu,
+                    double *Sw, int32_t *cnt, const int64_t *idx)
 {
-    if (n < 0 || dk <= 0 || dv <= 0 || dv > 1024 || (mode != 0 && mode != 1) ||
-        (mode == 1 && fc == NULL))
+    if (n < 0 || !window_args_ok(mode, r, dk, dv, 1, 1) ||
+        (mode == 1 && fc == NULL) || (r > 0 && (ck == NULL || cu == NULL)))
         return ORC_ERR_ARG;
 #pragma omp parallel for schedule(static)
     for (int64_t row = 0; row < n; ++row) {
         const int64_t h = idx[row];
-        float *fch = mode ? fc + (size_t)h * dv : NULL;
-        quant_mode(mode, dk, dv, S + (size_t)row * dk * dv, Z + (size_t)h * dk * dv,
-                   s + (size_t)h * dk, fch);
-        dequant_mode(mode, dk, dv, Z + (size_t)h * dk * dv, s + (size_t)h * dk, fch,
-                     Sw + (size_t)h * dk * dv);
+        double *Sh = Sw + (size_t)h * dk * dv;
+        for (size_t e = 0; e < (size_t)dk * dv; ++e) Sh[e] = S[(size_t)row * dk * dv + e];
+        boundary(mode, r, dk, dv, Sh, Z + (size_t)h * dk * dv, s + (size_t)h * dk,
+                 mode ? fc + (size_t)h * dv : NULL, r ? ck + (size_t)h * r * dk : NULL,
+                 r ? cu + (size_t)h * r * dv : NULL, 0);
         cnt[h] = 0;
     }
     return ORC_OK;
@@ -692,13 +779,15 @@ int orc_window_load(int64_t n, int mode, int dk, int dv, const double *S,
  *   Gamma_{a:b} = Diag(alpha_b) ... Diag(alpha_a), identity when a > b.
  * The diagonal products are accumulated as sums of log-decays.
  */
-int orc_window_unrolled(int64_t n, int mode, int dk, int dv, int dl, int W,
-                        const int8_t *Z, const float *s, const float *fc,
-                        const double *rl, const double *rk, const double *ru,
-                        const int32_t *cnt, const int64_t *idx, double *S_out)
+int orc_window_unrolled(int64_t n, int mode, int r, int dk, int dv, int dl,
+                        int W, const int8_t *Z, const float *s, const float *fc,
+                        const double *ck, const double *cu, const double *rl,
+                        const double *rk, const double *ru, const int32_t *cnt,
+                        const int64_t *idx, double *S_out)
 {
-    if (n < 0 || !window_args_ok(mode, dk, dv, dl, W)) return ORC_ERR_ARG;
-    if (mode == 1 && fc == NULL) return ORC_ERR_ARG;
+    if (n < 0 || !window_args_ok(mode, r, dk, dv, dl, W)) return ORC_ERR_ARG;
+    if ((mode == 1 && fc == NULL) || (r > 0 && (ck == NULL || cu == NULL)))
+        return ORC_ERR_ARG;
 #pragma omp parallel for schedule(dynamic, 2)
     for (int64_t row = 0; row < n; ++row) {
         const int64_t h = idx[row];
@@ -709,6 +798,12 @@ int orc_window_unrolled(int64_t n, int mode, int dk, int dv, int dl, int W,
         double *S = S_out + (size_t)row * dk * dv;
         dequant_mode(mode, dk, dv, Z + (size_t)h * dk * dv, s + (size_t)h * dk,
                      mode ? fc + (size_t)h * dv : NULL, S);
+        /* [LQ] eq. 7: the compensator pairs join the boundary state */
+        for (int c = 0; c < r; ++c)
+            for (int i = 0; i < dk; ++i)
+                for (int j = 0; j < dv; ++j)
+                    S[(size_t)i * dv + j] += ck[((size_t)h * r + c) * dk + i] *
+                                             cu[((size_t)h * r + c) * dv + j];
         for (int i = 0; i < dk; ++i) {
             double g = 0.0; /* log of Gamma_{1:l}, row i */
             for (int t = 0; t < l; ++t) g += dlam_at(RL + (size_t)t * dl, dl, i);
@@ -735,14 +830,15 @@ int orc_window_unrolled(int64_t n, int mode, int dk, int dv, int dl, int W,
  *   S_l^T x = S-hat_0^T Gamma_{1:l} x + sum_j u_j (k_j^T Gamma_{j+1:l} x).
  * x is [n][dk]; out is [n][dv].
  */
-int orc_window_readout(int64_t n, int mode, int dk, int dv, int dl, int W,
-                       const int8_t *Z, const float *s, const float *fc,
-                       const double *rl, const double *rk, const double *ru,
-                       const int32_t *cnt, const int64_t *idx, const double *x,
-                       double *out)
+int orc_window_readout(int64_t n, int mode, int r, int dk, int dv, int dl,
+                       int W, const int8_t *Z, const float *s, const float *fc,
+                       const double *ck, const double *cu, const double *rl,
+                       const double *rk, const double *ru, const int32_t *cnt,
+                       const int64_t *idx, const double *x, double *out)
 {
-    if (n < 0 || !window_args_ok(mode, dk, dv, dl, W)) return ORC_ERR_ARG;
-    if (mode == 1 && fc == NULL) return ORC_ERR_ARG;
+    if (n < 0 || !window_args_ok(mode, r, dk, dv, dl, W)) return ORC_ERR_ARG;
+    if ((mode == 1 && fc == NULL) || (r > 0 && (ck == NULL || cu == NULL)))
+        return ORC_ERR_ARG;
 #pragma omp parallel for schedule(dynamic, 2)
     for (int64_t row = 0; row < n; ++row) {
         const int64_t h = idx[row];
@@ -756,6 +852,8 @@ int orc_window_readout(int64_t n, int mode, int dk, int dv, int dl, int W,
         const double *xr = x + (size_t)row * dk;
         double *o = out + (size_t)row * dv;
         for (int j = 0; j < dv; ++j) o[j] = 0.0;
+        double ckx[64];
+        for (int c = 0; c < r; ++c) ckx[c] = 0.0;
         for (int i = 0; i < dk; ++i) {
             double g = 0.0;
             for (int t = 0; t < l; ++t) g += dlam_at(RL + (size_t)t * dl, dl, i);
@@ -764,7 +862,11 @@ int orc_window_readout(int64_t n, int mode, int dk, int dv, int dl, int W,
             for (int j = 0; j < dv; ++j)
                 o[j] += (double)sh[i] * (double)Zh[(size_t)i * dv + j] * gx *
                         (bh ? (double)bh[j] : 1.0);
+            for (int c = 0; c < r; ++c) ckx[c] += ck[((size_t)h * r + c) * dk + i] * gx;
         }
+        /* eq. 10: + U~ (K~^T Gamma_{1:l} x) */
+        for (int c = 0; c < r; ++c)
+            for (int j = 0; j < dv; ++j) o[j] += cu[((size_t)h * r + c) * dv + j] * ckx[c];
         for (int jj = 0; jj < l; ++jj) {
             double c = 0.0;
             for (int i = 0; i < dk; ++i) {
