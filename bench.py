@@ -174,10 +174,10 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def make_pools(w, variant, window, dev, col_scales=False):
+def make_pools(w, variant, window, dev, col_scales=False, compensators=0):
     from recurrent_state_quantization_gb300 import StatePool
     return [StatePool(w.num_slots, w.heads, variant, w.gate, window, device=dev,
-                      col_scales=col_scales)
+                      col_scales=col_scales, compensators=compensators)
             for _ in range(w.pools)]
 
 
@@ -320,15 +320,16 @@ def run_native(args, rank, world, local):
 def window_sweep(w, slot_idx, masks, inputs, ring, dev, peak, peak_kind, eager_pools):
     """INT8 head-steps/s and achieved algorithmic GB/s for each window W (a
     whole number of windows, 4 pools, warmed states), and for W = 16 in the
-    smoothed per-value-column format."""
+    smoothed per-value-column format, without and with 4 Compensator Tokens
+    (the full LeapQuant boundary format)."""
     import torch
     from recurrent_state_quantization_gb300 import bytemodel as bm
     all_slots = torch.arange(w.num_slots, dtype=torch.int32, device=dev)
     res = []
     stream = torch.cuda.current_stream()
     heads = w.batch * w.heads
-    for W, cols in [(W_, False) for W_ in SWEEP_W] + [(16, True)]:
-        pools = make_pools(w, "int8", W, dev, col_scales=cols)
+    for W, cols, comp in [(W_, False, 0) for W_ in SWEEP_W] + [(16, True, 0), (16, True, 4)]:
+        pools = make_pools(w, "int8", W, dev, col_scales=cols, compensators=comp)
         for p in range(w.pools):
             pools[p].load(all_slots, eager_pools[p].read(all_slots))
         y = torch.empty(w.batch, w.heads, w.d_v, device=dev)
@@ -346,8 +347,9 @@ def window_sweep(w, slot_idx, masks, inputs, ring, dev, peak, peak_kind, eager_p
         torch.cuda.synchronize()
         ms = a.elapsed_time(b)
         hs = heads * w.pools * tokens
-        gbs = bm.int8_bytes(w.gate, W, col_scales=cols) * hs / (ms * 1e-3) / 1e9
-        res.append({"window": W, "format": "smoothed per-value-column" if cols else "per-key-row",
+        gbs = bm.int8_bytes(w.gate, W, col_scales=cols, compensators=comp) * hs / (ms * 1e-3) / 1e9
+        res.append({"window": W, "format": ("smoothed per-value-column" if cols else "per-key-row") +
+                    (f" + {comp} compensator tokens" if comp else ""),
                     "tokens": tokens, "head_steps_per_s": hs / (ms * 1e-3),
                     "achieved_gbs": gbs, "frac_of_" + peak_kind + "_hbm": gbs / peak})
         del pools

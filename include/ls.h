@@ -100,6 +100,21 @@ typedef enum {
  */
 #define LS_INT8_COLUMN_SCALES 1u
 
+/*
+ * ls_pool_desc.flags, bits 8..11: r Compensator Tokens (LS_WINDOW_INT8 only,
+ * 0 <= r <= LS_MAX_COMPENSATORS), "LeapQuant: Efficient Linear Attention with
+ * Accurate Recurrent State Quantization", §3.3 eq. 5-6: at every window
+ * boundary (window end, ls_window_commit, ls_pool_load) r rank-one pairs
+ * (k~, u~) are fitted to the state by power iteration and kept as FP32 log
+ * records with log-decay snapshot 0 at the head of the next window; only
+ * the residual S - K~ U~^T is quantized.  The fit: sequential deflation, per
+ * pair three steps v <- R^T R v / ||R^T R v|| from all-ones / sqrt(d_v),
+ * then k~ = R v, u~ = v.  A state's log then holds r + (real tokens)
+ * entries, and its window ends on its W-th real token.
+ */
+#define LS_MAX_COMPENSATORS 8
+#define LS_INT8_COMPENSATORS(r) ((uint32_t)(r) << 8)
+
 typedef struct {
     int32_t num_slots; /* P >= 1: states (requests) the pool holds            */
     int32_t num_heads; /* H >= 1                                                */
@@ -109,7 +124,8 @@ typedef struct {
     int32_t gate;      /* ls_gate                                              */
     int32_t window;    /* W (INT8) or M (deferred), 1..LS_MAX_WINDOW; ignored
                           (may be 0) for LS_EAGER_FP32                          */
-    uint32_t flags;    /* 0, or LS_INT8_COLUMN_SCALES for LS_WINDOW_INT8       */
+    uint32_t flags;    /* 0; for LS_WINDOW_INT8 also LS_INT8_COLUMN_SCALES and
+                          LS_INT8_COMPENSATORS(r)                              */
 } ls_pool_desc;
 
 /* Human-readable name of a status code.  Never NULL. */
@@ -133,7 +149,9 @@ int ls_pool_required_bytes(const ls_pool_desc *desc, size_t *bytes);
 /*
  * Bind a pool to caller-owned device memory `dev_mem` (>= required bytes,
  * 256-byte aligned) and zero it on `stream`: every state starts at S = 0 with
- * an empty log / a window boundary (the zero state is exact in INT8).
+ * an empty log / a window boundary (the zero state is exact in INT8); with
+ * compensator pairs the log holds the zero state's pairs (k~ = 0, u~ =
+ * 1 / sqrt(d_v)), as after ls_pool_reset_slots.
  * `*out` receives the host handle.  The memory stays owned by the caller and
  * must outlive the handle.
  * Errors: LS_ERR_INVALID, LS_ERR_SIZE (bytes too small, bad descriptor),
@@ -245,6 +263,16 @@ int ls_pool_read_int8(const ls_pool *pool, const int32_t *d_slots, int32_t n,
  */
 int ls_pool_read_int8_col_scales(const ls_pool *pool, const int32_t *d_slots,
                                  int32_t n, float *d_col_scales, void *stream);
+
+/*
+ * LS_WINDOW_INT8 with LS_INT8_COMPENSATORS(r), r >= 1, only: the current
+ * window's compensator pairs of `n` slots into d_k_out [n, H, r, d_k] and
+ * d_u_out [n, H, r, d_v] (FP32).  Errors as ls_pool_load, and
+ * LS_ERR_INVALID for other pools.
+ */
+int ls_pool_read_compensators(const ls_pool *pool, const int32_t *d_slots,
+                              int32_t n, float *d_k_out, float *d_u_out,
+                              void *stream);
 
 /*
  * Deferred / INT8 only: the live log length of every (slot, head) into

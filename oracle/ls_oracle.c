@@ -514,11 +514,12 @@ static void dequant_mode(int mode, int dk, int dv, const int8_t *Z,
  * Readings (the pages give neither): sequential deflation, h = 1..r, each
  * fit on the residual left by the previous ones; COMP_ITERS power steps
  *     v <- R^T (R v) / ||R^T (R v)||     (v kept if the norm is 0)
- * from a warm start, the previous window's u~_h when it is nonzero (the
- * state moves little in a window), else the all-ones vector / sqrt(dv);
- * then k~_h = R v, u~_h = v (unit), R <- R - k~_h u~_h^T.
+ * from the all-ones vector / sqrt(dv) (a warm start from the previous
+ * window's pairs can lie in the subspace the earlier pairs just removed,
+ * where the steps amplify rounding); then k~_h = R v, u~_h = v (unit),
+ * R <- R - k~_h u~_h^T.  With warm != 0 (a test hook) the start is cu[h].
  */
-#define COMP_ITERS 2
+#define COMP_ITERS 3
 
 static void fit_compensators(int r, int dk, int dv, double *R, double *ck,
                              double *cu, int warm)
@@ -581,7 +582,8 @@ int orc_fit_compensators(int64_t n, int r, int dk, int dv, double *S,
 static void boundary(int mode, int r, int dk, int dv, double *S, int8_t *Z,
                      float *s, float *fc, double *ck, double *cu, int warm)
 {
-    if (r > 0) fit_compensators(r, dk, dv, S, ck, cu, warm);
+    (void)warm;
+    if (r > 0) fit_compensators(r, dk, dv, S, ck, cu, 0);
     quant_mode(mode, dk, dv, S, Z, s, fc);
     dequant_mode(mode, dk, dv, Z, s, fc, S);
     for (int h = 0; h < r; ++h)

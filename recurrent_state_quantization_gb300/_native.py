@@ -30,6 +30,11 @@ LS_GATE_PER_KEY = 1
 
 LS_MAX_WINDOW = 256
 LS_INT8_COLUMN_SCALES = 1
+LS_MAX_COMPENSATORS = 8
+
+
+def LS_INT8_COMPENSATORS(r: int) -> int:
+    return int(r) << 8
 LS_ABI_VERSION = 2  # the include/ls.h these prototypes follow
 
 # Every symbol include/ls.h declares.
@@ -37,7 +42,8 @@ EXPORTS = (
     "ls_error_string", "ls_abi_version", "ls_pool_required_bytes", "ls_pool_create",
     "ls_pool_destroy", "ls_pool_load", "ls_pool_reset_slots", "ls_decode_step",
     "ls_step_staging_bytes", "ls_decode_step_host", "ls_window_commit", "ls_pool_read",
-    "ls_pool_read_int8", "ls_pool_read_int8_col_scales", "ls_pool_read_log_meta",
+    "ls_pool_read_int8", "ls_pool_read_int8_col_scales", "ls_pool_read_compensators",
+    "ls_pool_read_log_meta",
     "ls_pool_status",
 )
 
@@ -82,6 +88,7 @@ def load() -> C.CDLL:
         "ls_pool_read": (C.c_int, [P, P, I32, P, P]),
         "ls_pool_read_int8": (C.c_int, [P, P, I32, P, P, P]),
         "ls_pool_read_int8_col_scales": (C.c_int, [P, P, I32, P, P]),
+        "ls_pool_read_compensators": (C.c_int, [P, P, I32, P, P, P]),
         "ls_pool_read_log_meta": (C.c_int, [P, P, I32, P, P, P]),
         "ls_pool_status": (C.c_int, [P, P, C.POINTER(I32)]),
     }

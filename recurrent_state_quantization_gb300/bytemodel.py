@@ -17,7 +17,8 @@ written; the roofline fraction divides them by a measured kernel time.
   Accurate Recurrent State Quantization", §3.2): the same cycle with an INT8
   base plus one FP32 scale per key row in place of the FP32 base; the
   smoothed per-value-column format (§3.4 eq. 7, App. B.3) adds one FP32
-  scale per value column to that base.
+  scale per value column to that base; r Compensator Tokens (§3.3) add r
+  log entries read by every token and written once per window.
 """
 from __future__ import annotations
 
@@ -59,8 +60,10 @@ def deferred_bytes(gate: str, M: int, d_k: int = 128, d_v: int = 128) -> float:
     return log_cycle_bytes(state_bytes_fp32(d_k, d_v), gate, M, d_k, d_v)
 
 
-def int8_bytes(gate: str, W: int, d_k: int = 128, d_v: int = 128, col_scales: bool = False) -> float:
-    return log_cycle_bytes(state_bytes_int8(d_k, d_v, col_scales), gate, W, d_k, d_v)
+def int8_bytes(gate: str, W: int, d_k: int = 128, d_v: int = 128, col_scales: bool = False,
+               compensators: int = 0) -> float:
+    comp = compensators * entry_bytes(gate, d_k, d_v) * (1 + 1 / W)
+    return log_cycle_bytes(state_bytes_int8(d_k, d_v, col_scales), gate, W, d_k, d_v) + comp
 
 
 def variant_bytes(variant: str, gate: str, window: int = 1) -> float:

@@ -36,8 +36,11 @@ struct Layout {
 int make_layout(const ls_pool_desc* d, Layout* L) {
     if (d == nullptr || L == nullptr) return LS_ERR_INVALID;
     if (d->variant < LS_EAGER_FP32 || d->variant > LS_WINDOW_INT8) return LS_ERR_INVALID;
-    if ((d->flags & ~LS_INT8_COLUMN_SCALES) != 0) return LS_ERR_INVALID;
-    if ((d->flags & LS_INT8_COLUMN_SCALES) && d->variant != LS_WINDOW_INT8) return LS_ERR_INVALID;
+    const uint32_t known = LS_INT8_COLUMN_SCALES | LS_INT8_COMPENSATORS(15);
+    if ((d->flags & ~known) != 0) return LS_ERR_INVALID;
+    const uint32_t ncomp = (d->flags >> 8) & 15u;
+    if ((d->flags != 0) && d->variant != LS_WINDOW_INT8) return LS_ERR_INVALID;
+    if (ncomp > LS_MAX_COMPENSATORS) return LS_ERR_INVALID;
     if (d->gate != LS_GATE_SCALAR && d->gate != LS_GATE_PER_KEY) return LS_ERR_INVALID;
     if (d->num_slots < 1 || d->num_heads < 1) return LS_ERR_INVALID;
     if (d->d_k != kD || d->d_v != kD) return LS_ERR_SIZE;
@@ -45,7 +48,8 @@ int make_layout(const ls_pool_desc* d, Layout* L) {
     if (log && (d->window < 1 || d->window > LS_MAX_WINDOW)) return LS_ERR_SIZE;
     const uint64_t nh = static_cast<uint64_t>(d->num_slots) * static_cast<uint64_t>(d->num_heads);
     if (nh > 0x7fffffffull) return LS_ERR_SIZE;  // grid rows (batch * H) fit int32
-    const uint64_t W = log ? static_cast<uint64_t>(d->window) : 0;
+    // log capacity: the window's records plus the compensator pairs
+    const uint64_t W = log ? static_cast<uint64_t>(d->window) + ((d->flags >> 8) & 15u) : 0;
     const uint64_t dl = d->gate == LS_GATE_PER_KEY ? kD : 1;
     const bool int8 = d->variant == LS_WINDOW_INT8;
     size_t off = 0;
@@ -88,8 +92,10 @@ ls::PoolView make_view(const ls_pool_desc& d, const Layout& L, unsigned char* m)
     v.P = d.num_slots;
     v.H = d.num_heads;
     v.W = log ? d.window : 0;
+    v.R = log ? static_cast<int32_t>((d.flags >> 8) & 15u) : 0;
+    v.cap = v.W + v.R;
     v.dl = d.gate == LS_GATE_PER_KEY ? kD : 1;
-    v.lam_stride = d.gate == LS_GATE_PER_KEY ? v.W * kD : (v.W + 3) / 4 * 4;
+    v.lam_stride = d.gate == LS_GATE_PER_KEY ? v.cap * kD : (v.cap + 3) / 4 * 4;
     return v;
 }
 
@@ -184,7 +190,8 @@ int ls_pool_create(const ls_pool_desc* desc, void* dev_mem, size_t bytes, void* 
     p->bytes = bytes;
     p->view = make_view(*desc, L, p->mem);
     p->num_sms = sms > 0 ? sms : 1;
-    if (cudaMemsetAsync(dev_mem, 0, L.total, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    if (cudaMemsetAsync(dev_mem, 0, L.total, static_cast<cudaStream_t>(stream)) != cudaSuccess ||
+        (p->view.R > 0 && ls::launch_init_comp(p->view, static_cast<cudaStream_t>(stream)) != cudaSuccess)) {
         delete p;
         return LS_ERR_CUDA;
     }
@@ -353,6 +360,19 @@ int ls_pool_read_int8_col_scales(const ls_pool* pool, const int32_t* d_slots, in
     ls::AuxArgs a = aux_args(pool, d_slots, n);
     a.scales_out = d_col_scales;
     return cuda_status(ls::launch_read_colf(a, static_cast<cudaStream_t>(stream)));
+}
+
+int ls_pool_read_compensators(const ls_pool* pool, const int32_t* d_slots, int32_t n,
+                              float* d_k_out, float* d_u_out, void* stream) {
+    int rc = check_slot_list(pool, d_slots, n);
+    if (rc != LS_OK || n == 0) return rc;
+    if (pool->view.R < 1) return LS_ERR_INVALID;
+    if (d_k_out == nullptr || d_u_out == nullptr) return LS_ERR_INVALID;
+    if (!aligned(d_k_out, 4) || !aligned(d_u_out, 4)) return LS_ERR_ALIGN;
+    ls::AuxArgs a = aux_args(pool, d_slots, n);
+    a.state_out = d_k_out;
+    a.scales_out = d_u_out;
+    return cuda_status(ls::launch_read_comp(a, static_cast<cudaStream_t>(stream)));
 }
 
 int ls_pool_read_log_meta(const ls_pool* pool, const int32_t* d_slots, int32_t n, int32_t* d_len,

@@ -128,6 +128,42 @@ __global__ void __launch_bounds__(kThreads) load_cols_kernel(const AuxArgs a) {
     clear_log(pv, hd);
 }
 
+// INT8 with compensator pairs: state_in[n][h] -> pairs fitted from a cold
+// start, then the residual in the pool's format, and a log that holds only
+// the pairs ("LeapQuant: Efficient Linear Attention with Accurate Recurrent
+// State Quantization", §3.3 eq. 5-6); warp w holds key rows 16w..16w+15.
+__global__ void __launch_bounds__(kThreads) load_comp_kernel(const AuxArgs a) {
+    __shared__ __align__(16) float red[kWarps * kD];
+    __shared__ __align__(16) float vs[kD], ws[kD], ks[kD];
+    __shared__ float nz[4];
+    const PoolView& pv = a.pv;
+    const int H = pv.H;
+    const int n = blockIdx.x / H, h = blockIdx.x - n * H;
+    int slot;
+    if (!slot_of(a, n, &slot)) return;  // uniform over the CTA
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const size_t hd = static_cast<size_t>(slot) * H + h;
+    const float* in = a.state_in + (static_cast<size_t>(n) * H + h) * (kD * kD);
+    float2 lo[16], hi[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        const float4 v = ldg4(in + (16 * warp + r) * kD + 4 * lane);
+        lo[r] = make_float2(v.x, v.y);
+        hi[r] = make_float2(v.z, v.w);
+    }
+    fit_compensators_cta(lo, hi, pv, hd, vs, ws, ks, red, nz);
+    if (pv.colf != nullptr)
+        quantize_cols_cta(lo, hi, pv.base, hd, pv.scale + hd * kD, pv.colf + hd * kD, red, vs);
+    else
+        quantize_rows_cta(lo, hi, pv.base, hd, pv.scale + hd * kD);
+    if (pv.dl == kD) {
+        if (threadIdx.x < kD) pv.lbar[hd * kD + threadIdx.x] = 0.0f;
+    } else if (threadIdx.x == 0) {
+        pv.lbar[hd] = 0.0f;
+    }
+    if (threadIdx.x == 0) pv.len[hd] = pv.R;
+}
+
 template <bool INT8>
 __global__ void __launch_bounds__(kThreads) reset_kernel(const AuxArgs a) {
     const PoolView& pv = a.pv;
@@ -149,6 +185,19 @@ __global__ void __launch_bounds__(kThreads) reset_kernel(const AuxArgs a) {
         }
     }
     clear_log(pv, hd);
+    if (INT8 && pv.R > 0) {
+        // a zero state's pairs: k~ = 0, u~ = the cold start 1 / sqrt(128)
+        const size_t kb = hd * static_cast<size_t>(pv.cap);
+        for (int idx = threadIdx.x; idx < pv.R * kD; idx += kThreads) {
+            pv.klog[kb * kD + idx] = 0.0f;
+            pv.ulog[kb * kD + idx] = 0.08838834764831845f;
+        }
+        const int nl = pv.dl == kD ? pv.R * kD : pv.R;
+        for (int idx = threadIdx.x; idx < nl; idx += kThreads)
+            pv.lamlog[hd * static_cast<size_t>(pv.lam_stride) + idx] = 0.0f;
+        __syncthreads();  // clear_log's len = 0 store is ordered before this one
+        if (threadIdx.x == 0) pv.len[hd] = pv.R;
+    }
 }
 
 // INT8 codes in the logical layout codes[n][h][i][j] and scales[n][h][i].
@@ -210,6 +259,8 @@ cudaError_t launch_load(const AuxArgs& a, bool int8, bool has_log, cudaStream_t 
     const dim3 grid(static_cast<unsigned>(a.n) * static_cast<unsigned>(a.pv.H));
     if (!has_log)
         load_eager_kernel<<<grid, kThreads, transpose_smem_bytes(), s>>>(a);
+    else if (int8 && a.pv.R > 0)
+        load_comp_kernel<<<grid, kThreads, 0, s>>>(a);
     else if (int8 && a.pv.colf != nullptr)
         load_cols_kernel<<<grid, kThreads, 0, s>>>(a);
     else if (int8)
@@ -237,6 +288,45 @@ cudaError_t launch_read_int8(const AuxArgs& a, cudaStream_t s) {
 cudaError_t launch_read_colf(const AuxArgs& a, cudaStream_t s) {
     const dim3 grid(static_cast<unsigned>(a.n) * static_cast<unsigned>(a.pv.H));
     read_colf_kernel<<<grid, kD, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+// The current pairs: k_out [n][H][R][d_k] (state_out), u_out [n][H][R][d_v]
+// (scales_out).
+__global__ void __launch_bounds__(kThreads) read_comp_kernel(const AuxArgs a) {
+    const PoolView& pv = a.pv;
+    const int H = pv.H;
+    const int n = blockIdx.x / H, h = blockIdx.x - n * H;
+    int slot;
+    if (!slot_of(a, n, &slot)) return;
+    const size_t hd = static_cast<size_t>(slot) * H + h;
+    const size_t o = (static_cast<size_t>(n) * H + h) * static_cast<size_t>(pv.R) * kD;
+    const size_t kb = hd * static_cast<size_t>(pv.cap) * kD;
+    for (int idx = threadIdx.x; idx < pv.R * kD; idx += kThreads) {
+        a.state_out[o + idx] = pv.klog[kb + idx];
+        a.scales_out[o + idx] = pv.ulog[kb + idx];
+    }
+}
+
+// A new pool's states as a reset leaves them: for compensator pools every
+// log starts with the zero state's pairs (k~ = 0, u~ = 1 / sqrt(128),
+// snapshot 0), so len = R.  One CTA per state; the memory is zeroed before.
+__global__ void __launch_bounds__(kD) init_comp_kernel(const PoolView pv) {
+    const size_t hd = blockIdx.x;
+    const size_t kb = hd * static_cast<size_t>(pv.cap) * kD;
+    for (int idx = threadIdx.x; idx < pv.R * kD; idx += kD) pv.ulog[kb + idx] = 0.08838834764831845f;
+    if (threadIdx.x == 0) pv.len[hd] = pv.R;
+}
+
+cudaError_t launch_init_comp(const PoolView& pv, cudaStream_t s) {
+    const dim3 grid(static_cast<unsigned>(pv.P) * static_cast<unsigned>(pv.H));
+    init_comp_kernel<<<grid, kD, 0, s>>>(pv);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_read_comp(const AuxArgs& a, cudaStream_t s) {
+    const dim3 grid(static_cast<unsigned>(a.n) * static_cast<unsigned>(a.pv.H));
+    read_comp_kernel<<<grid, kThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -19,7 +19,7 @@ namespace ls {
 
 namespace {
 
-template <bool INT8, bool PER_KEY, int MODE>
+template <bool INT8, bool PER_KEY, int MODE, bool COMP>
 __global__ void __launch_bounds__(kThreads, 2) fold_kernel(const AuxArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     const PoolView& pv = a.pv;
@@ -32,11 +32,11 @@ __global__ void __launch_bounds__(kThreads, 2) fold_kernel(const AuxArgs a) {
     }
     const size_t hd = static_cast<size_t>(slot) * H + h;
     const int L = pv.len[hd];
-    if (L < 0 || L >= pv.W) {
+    if (L < 0 || L >= pv.cap) {
         if (threadIdx.x == 0) flag_status(pv.status, kDevBadState);
         return;
     }
-    if (MODE == kFoldCommit && L == 0) return;  // already at a boundary
+    if (MODE == kFoldCommit && L <= pv.R) return;  // already at a boundary (only the pairs)
     const FoldSmem fs = fold_smem(smem, INT8);
     if (threadIdx.x == 0) {
         mbar_init(fs.bar, 1);
@@ -51,7 +51,7 @@ __global__ void __launch_bounds__(kThreads, 2) fold_kernel(const AuxArgs a) {
     if constexpr (MODE == kFoldRead) out = a.state_out + (static_cast<size_t>(n) * H + h) * (kD * kD);
     const TokenIn none{nullptr, nullptr, nullptr, nullptr, 0.0f, nullptr, 0};
     FoldPipe pp;
-    const bool ok = fold_cta<INT8, PER_KEY, MODE>(pv, hd, L, pv.lbar + hd * (PER_KEY ? kD : 1), lb,
+    const bool ok = fold_cta<INT8, PER_KEY, MODE, COMP>(pv, hd, L, pv.lbar + hd * (PER_KEY ? kD : 1), lb,
                                                   out, fs, pp, none, -1, 0);
     if (MODE == kFoldCommit && ok) {
         __syncthreads();  // every reader of lbar is done
@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(kThreads, 2) fold_kernel(const AuxArgs a) {
         } else if (threadIdx.x == 0) {
             pv.lbar[hd] = 0.0f;
         }
-        if (threadIdx.x == 0) pv.len[hd] = 0;
+        if (threadIdx.x == 0) pv.len[hd] = pv.R;
     }
 }
 
@@ -93,10 +93,12 @@ template <bool INT8, bool PER_KEY>
 cudaError_t launch_mode(const AuxArgs& a, bool commit, cudaStream_t s) {
     const dim3 grid(static_cast<unsigned>(a.n) * static_cast<unsigned>(a.pv.H));
     const size_t sm = fold_smem_bytes(INT8);
-    if (commit)
-        fold_kernel<INT8, PER_KEY, kFoldCommit><<<grid, kThreads, sm, s>>>(a);
+    if (commit && INT8 && a.pv.R > 0)
+        fold_kernel<INT8, PER_KEY, kFoldCommit, INT8><<<grid, kThreads, sm, s>>>(a);
+    else if (commit)
+        fold_kernel<INT8, PER_KEY, kFoldCommit, false><<<grid, kThreads, sm, s>>>(a);
     else
-        fold_kernel<INT8, PER_KEY, kFoldRead><<<grid, kThreads, sm, s>>>(a);
+        fold_kernel<INT8, PER_KEY, kFoldRead, false><<<grid, kThreads, sm, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -108,9 +110,11 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 
 template <bool INT8, bool PER_KEY>
 cudaError_t prepare_mode() {
-    cudaError_t e = set_smem(fold_kernel<INT8, PER_KEY, kFoldCommit>, fold_smem_bytes(INT8));
+    cudaError_t e = set_smem(fold_kernel<INT8, PER_KEY, kFoldCommit, false>, fold_smem_bytes(INT8));
     if (e != cudaSuccess) return e;
-    return set_smem(fold_kernel<INT8, PER_KEY, kFoldRead>, fold_smem_bytes(INT8));
+    if ((e = set_smem(fold_kernel<INT8, PER_KEY, kFoldCommit, INT8>, fold_smem_bytes(INT8))) != cudaSuccess)
+        return e;
+    return set_smem(fold_kernel<INT8, PER_KEY, kFoldRead, false>, fold_smem_bytes(INT8));
 }
 
 }  // namespace

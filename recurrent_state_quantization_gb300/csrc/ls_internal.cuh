@@ -45,11 +45,13 @@ struct PoolView {
                            //   scales b; nullptr for per-row scales
     float* lbar;           // log variants: [P*H][dl] cumulative log-decay
     int32_t* len;          // log variants: [P*H] live log length
-    float* klog;           // [P*H][W][d_k]  key factors k
-    float* ulog;           // [P*H][W][d_v]  value factors u
+    float* klog;           // [P*H][cap][d_k]  key factors k
+    float* ulog;           // [P*H][cap][d_v]  value factors u
     float* lamlog;         // [P*H][lam_stride] cumulative log-decay snapshots:
-                           //   per-key gate [W][d_k]; scalar gate [W] padded to 4
+                           //   per-key gate [cap][d_k]; scalar gate [cap] padded to 4
     int32_t P, H, W, dl;
+    int32_t R;             // INT8: compensator pairs at the head of each window (0: none)
+    int32_t cap;           // log entries per state: W + R
     int32_t lam_stride;    // floats per state in lamlog
 };
 
@@ -124,6 +126,8 @@ cudaError_t launch_load(const AuxArgs& a, bool int8, bool has_log, cudaStream_t 
 cudaError_t launch_reset(const AuxArgs& a, bool int8, bool has_log, cudaStream_t s);
 cudaError_t launch_read_int8(const AuxArgs& a, cudaStream_t s);
 cudaError_t launch_read_colf(const AuxArgs& a, cudaStream_t s);
+cudaError_t launch_read_comp(const AuxArgs& a, cudaStream_t s);
+cudaError_t launch_init_comp(const PoolView& pv, cudaStream_t s);
 cudaError_t launch_read_log_meta(const AuxArgs& a, cudaStream_t s);
 
 }  // namespace ls

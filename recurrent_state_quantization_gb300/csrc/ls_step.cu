@@ -111,7 +111,7 @@ __device__ __forceinline__ void issue_item(WarpSmem& ws, const StepArgs& a, int 
     } else {
         const int e0 = (it - 1 - P::NT) * P::EPC;
         const int n = min(P::EPC, L - e0);
-        const size_t eo = (hd * static_cast<size_t>(pv.W) + e0) * kD;
+        const size_t eo = (hd * static_cast<size_t>(pv.cap) + e0) * kD;
         const uint32_t part = static_cast<uint32_t>(n) * kVecBytes;
         const size_t lb0 = hd * static_cast<size_t>(pv.lam_stride);
         mbar_arrive_expect_tx(bar, PER_KEY ? 3 * part : 2 * part + 16);
@@ -141,7 +141,7 @@ __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, 
     using P = Plan<INT8, PER_KEY>;
     const int lane = threadIdx.x & 31;
     const PoolView& pv = a.pv;
-    const int H = pv.H, W = pv.W;
+    const int H = pv.H, W = pv.cap;  // W: log capacity (window + compensator pairs)
     const int b = row / H, h = row - b * H;
     const size_t ro = static_cast<size_t>(row) * kD + 4 * lane;
     const float4 nan4 = make_float4(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000),
@@ -376,7 +376,7 @@ __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, 
     return static_cast<long long>(hd);  // INT8 window end: the CTA folds the W entries
 }
 
-template <bool INT8, bool PER_KEY>
+template <bool INT8, bool PER_KEY, bool COMP>
 __global__ void __launch_bounds__(kThreads, 2) log_step_kernel(const StepArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ long long fold_hd[kWarps];
@@ -423,8 +423,8 @@ __global__ void __launch_bounds__(kThreads, 2) log_step_kernel(const StepArgs a)
             const TokenIn tok{a.k, a.q, a.v, a.lam, __ldg(a.beta + r), a.y, static_cast<size_t>(r) * kD};
             const float* lbg = pv.lbar + st * (PER_KEY ? kD : 1);
             if constexpr (INT8)
-                ok = fold_cta<INT8, PER_KEY, kFoldCommit>(pv, st, pv.W, lbg, fold_lb[w], nullptr, fs, pp, tok,
-                                                          next, pv.W);
+                ok = fold_cta<INT8, PER_KEY, kFoldCommit, COMP>(pv, st, pv.cap, lbg, fold_lb[w], nullptr, fs, pp,
+                                                          tok, next, pv.cap);
             else
                 ok = fold_cta<INT8, PER_KEY, kFoldStep>(pv, st, pv.W - 1, lbg, fold_lb[w], nullptr, fs, pp,
                                                         tok, next, pv.W - 1);
@@ -436,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 2) log_step_kernel(const StepArgs a)
             } else if (threadIdx.x == 0) {
                 pv.lbar[st] = 0.0f;
             }
-            if (threadIdx.x == 0) pv.len[st] = 0;
+            if (threadIdx.x == 0) pv.len[st] = pv.R;  // the new window's compensator pairs
         } else if (!INT8 && threadIdx.x < kD) {  // after a copy timeout (flagged): no output
             a.y[static_cast<size_t>(r) * kD + threadIdx.x] = __int_as_float(0x7fc00000);
         }
@@ -454,19 +454,26 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 cudaError_t prepare_log_step_kernels() {
     cudaError_t e;
     const size_t ls = step_smem_bytes();
-    if ((e = set_smem(log_step_kernel<false, false>, ls)) != cudaSuccess) return e;
-    if ((e = set_smem(log_step_kernel<false, true>, ls)) != cudaSuccess) return e;
-    if ((e = set_smem(log_step_kernel<true, false>, ls)) != cudaSuccess) return e;
-    return set_smem(log_step_kernel<true, true>, ls);
+    if ((e = set_smem(log_step_kernel<false, false, false>, ls)) != cudaSuccess) return e;
+    if ((e = set_smem(log_step_kernel<false, true, false>, ls)) != cudaSuccess) return e;
+    if ((e = set_smem(log_step_kernel<true, false, false>, ls)) != cudaSuccess) return e;
+    if ((e = set_smem(log_step_kernel<true, true, false>, ls)) != cudaSuccess) return e;
+    if ((e = set_smem(log_step_kernel<true, false, true>, ls)) != cudaSuccess) return e;
+    return set_smem(log_step_kernel<true, true, true>, ls);
 }
 
 cudaError_t launch_log_step(const StepArgs& a, bool int8, bool per_key, cudaStream_t s) {
     const int64_t rows = static_cast<int64_t>(a.batch) * a.pv.H;
     const dim3 grid(static_cast<unsigned>((rows + kWarps - 1) / kWarps));
     const size_t sm = step_smem_bytes();
+    if (int8 && a.pv.R > 0)  // compensator pairs: the kernel that also fits them
+        return launch_dependent(per_key ? log_step_kernel<true, true, true> : log_step_kernel<true, false, true>,
+                                grid, sm, s, a);
     if (int8)
-        return launch_dependent(per_key ? log_step_kernel<true, true> : log_step_kernel<true, false>, grid, sm, s, a);
-    return launch_dependent(per_key ? log_step_kernel<false, true> : log_step_kernel<false, false>, grid, sm, s, a);
+        return launch_dependent(per_key ? log_step_kernel<true, true, false> : log_step_kernel<true, false, false>,
+                                grid, sm, s, a);
+    return launch_dependent(per_key ? log_step_kernel<false, true, false> : log_step_kernel<false, false, false>,
+                            grid, sm, s, a);
 }
 
 }  // namespace ls

@@ -207,6 +207,119 @@ __device__ __forceinline__ void quantize_cols_cta(float2 (&lo)[16], float2 (&hi)
             pack_quad_cols(lo, hi, 4 * qd, make_float2(f4.x, f4.y), make_float2(f4.z, f4.w));
 }
 
+// Per-key-row INT8 quantization of the CTA-held state (fold layout): row
+// absmax by a warp reduce-scatter, one division pair per row, codes packed
+// into column quads; writes the codes of state hd and the scales to scale[128].
+__device__ __forceinline__ void quantize_rows_cta(const float2 (&lo)[16], const float2 (&hi)[16], void* base,
+                                                  size_t hd, float* scale) {
+    const int lane = threadIdx.x & 31, i0 = 16 * (threadIdx.x >> 5);
+    float mx[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r)
+        mx[r] = fmaxf(fmaxf(fabsf(lo[r].x), fabsf(lo[r].y)), fmaxf(fabsf(hi[r].x), fabsf(hi[r].y)));
+    float s_mine, f_mine;
+    row_quant_params(warp_max16_scatter(mx, lane), s_mine, f_mine);
+    if ((lane & 1) == 0) scale[i0 + (lane >> 1)] = s_mine;
+#pragma unroll
+    for (int qd = 0; qd < 4; ++qd) {
+        float f[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) f[r] = __shfl_sync(0xffffffffu, f_mine, 2 * (4 * qd + r));
+        reinterpret_cast<uint4*>(base)[quad_index(hd, i0 / 4 + qd, lane)] = pack_quad(lo, hi, 4 * qd, f);
+    }
+}
+
+// out[i] = sum_j S_ij v_j for the CTA-held state (fold layout), v in shared
+// memory; written by the even lane of each row.
+__device__ __forceinline__ void cta_state_times(const float2 (&lo)[16], const float2 (&hi)[16], const float* v,
+                                                float* out) {
+    const int lane = threadIdx.x & 31, i0 = 16 * (threadIdx.x >> 5);
+    const float4 v4 = reinterpret_cast<const float4*>(v)[lane];
+    float part[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r)
+        part[r] = fmaf(lo[r].x, v4.x, fmaf(lo[r].y, v4.y, fmaf(hi[r].x, v4.z, hi[r].y * v4.w)));
+    const float t = warp_reduce16_scatter<true>(part, lane);
+    if ((lane & 1) == 0) out[i0 + (lane >> 1)] = t;
+}
+
+// Compensator Tokens ("LeapQuant: Efficient Linear Attention with Accurate
+// Recurrent State Quantization", §3.3 eq. 5-6) fitted by the CTA to the state
+// it holds (fold layout) before quantization.  For h = 0..R-1, on the
+// residual left by the previous pairs: v = all-ones / sqrt(128); kCompIters
+// steps v <- R^T (R v) / ||R^T (R v)|| (v kept when the norm is 0); k~ = R v,
+// u~ = v; R -= k~ u~^T; the pair becomes log entry h of state hd with
+// log-decay snapshot 0.  Shared scratch: vs, ws, ks [kD], red
+// [kWarps * kD], nz [4].  All threads of the CTA call it.
+constexpr int kCompIters = 3;
+
+__device__ __forceinline__ void fit_compensators_cta(float2 (&lo)[16], float2 (&hi)[16], const PoolView& pv,
+                                                     size_t hd, float* vs, float* ws, float* ks, float* red,
+                                                     float* nz) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int i0 = 16 * warp;
+    const size_t kb = hd * static_cast<size_t>(pv.cap);
+    for (int h = 0; h < pv.R; ++h) {
+        if (tid < kD) vs[tid] = 0.08838834764831845f;  // 1 / sqrt(128)
+        __syncthreads();
+#pragma unroll 1
+        for (int it = 0; it < kCompIters; ++it) {
+            cta_state_times(lo, hi, vs, ws);  // w = R v
+            __syncthreads();
+            float4 p = make_float4(0.f, 0.f, 0.f, 0.f);  // z = R^T w, this warp's rows
+#pragma unroll
+            for (int r4 = 0; r4 < 4; ++r4) {
+                const float4 w4 = reinterpret_cast<const float4*>(ws)[i0 / 4 + r4];
+                const float wr[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int row = 4 * r4 + r;
+                    p.x = fmaf(lo[row].x, wr[r], p.x);
+                    p.y = fmaf(lo[row].y, wr[r], p.y);
+                    p.z = fmaf(hi[row].x, wr[r], p.z);
+                    p.w = fmaf(hi[row].y, wr[r], p.w);
+                }
+            }
+            reinterpret_cast<float4*>(red)[warp * (kD / 4) + lane] = p;
+            __syncthreads();
+            float z = 0.0f;
+            if (tid < kD) {
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) z += red[w * kD + tid];
+                const float s2 = warp_sum(z * z);
+                if (lane == 0) nz[warp] = s2;
+            }
+            __syncthreads();
+            if (tid < kD) {
+                const float n2 = (nz[0] + nz[1]) + (nz[2] + nz[3]);
+                if (n2 > 0.0f) vs[tid] = z / sqrtf(n2);
+            }
+            __syncthreads();
+        }
+        cta_state_times(lo, hi, vs, ks);  // k~ = R v
+        __syncthreads();
+        const float4 v4 = reinterpret_cast<const float4*>(vs)[lane];
+#pragma unroll
+        for (int r4 = 0; r4 < 4; ++r4) {
+            const float4 k4 = reinterpret_cast<const float4*>(ks)[i0 / 4 + r4];
+            const float kr[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int row = 4 * r4 + r;
+                lo[row] = __ffma2_rn(make_float2(-kr[r], -kr[r]), make_float2(v4.x, v4.y), lo[row]);
+                hi[row] = __ffma2_rn(make_float2(-kr[r], -kr[r]), make_float2(v4.z, v4.w), hi[row]);
+            }
+        }
+        if (tid < kD) {
+            pv.klog[(kb + h) * kD + tid] = ks[tid];
+            pv.ulog[(kb + h) * kD + tid] = vs[tid];
+            if (pv.dl == kD) pv.lamlog[hd * static_cast<size_t>(pv.lam_stride) + h * kD + tid] = 0.0f;
+            else if (tid == 0) pv.lamlog[hd * static_cast<size_t>(pv.lam_stride) + h] = 0.0f;
+        }
+        __syncthreads();  // vs / ks are the next pair's scratch
+    }
+}
+
 enum FoldMode : int { kFoldCommit = 0, kFoldRead = 1, kFoldStep = 2 };
 
 // The current token of one (request, head) for kFoldStep: k, q, v, lambda at
@@ -338,7 +451,7 @@ __device__ __forceinline__ void fold_issue_tile(const PoolView& pv, size_t hd, c
 template <bool PER_KEY>
 __device__ __forceinline__ void fold_issue_log(const PoolView& pv, size_t hd, int c0, int nl,
                                                const FoldSmem& fs) {
-    const size_t eo = (hd * static_cast<size_t>(pv.W) + c0) * kD;
+    const size_t eo = (hd * static_cast<size_t>(pv.cap) + c0) * kD;
     const uint32_t part = static_cast<uint32_t>(nl) * kVecBytes;
     const size_t lb0 = hd * static_cast<size_t>(pv.lam_stride);
     const uint32_t lam_bytes = PER_KEY ? part : static_cast<uint32_t>((nl + 3) / 4 * 16);
@@ -356,7 +469,8 @@ __device__ __forceinline__ void fold_issue_log(const PoolView& pv, size_t hd, in
 // tile is in registers the tile of next_hd is staged, and (INT8) once its
 // last log chunk is staged the first next_n log entries of next_hd, so their
 // latency hides behind this fold.
-template <bool INT8, bool PER_KEY, int MODE>
+// COMP (INT8 pools with compensator pairs): fit the pairs at a commit.
+template <bool INT8, bool PER_KEY, int MODE, bool COMP = false>
 __device__ bool fold_cta(const PoolView& pv, size_t hd, int n, const float* lbg, float lb_scalar,
                          float* out, const FoldSmem& fs, FoldPipe& pp, const TokenIn& tok,
                          long long next_hd, int next_n) {
@@ -457,7 +571,7 @@ __device__ bool fold_cta(const PoolView& pv, size_t hd, int n, const float* lbg,
         pp.tile_issued = true;
     }
     // + sum_l exp(lb - Lam_l) K_l U_l^T, kFoldChunk entries at a time
-    const size_t kb = hd * static_cast<size_t>(pv.W);
+    const size_t kb = hd * static_cast<size_t>(pv.cap);
     const size_t lb0 = hd * static_cast<size_t>(pv.lam_stride);
 #pragma unroll 1
     for (int c0 = 0; c0 < n; c0 += kFoldChunk) {
@@ -609,27 +723,17 @@ __device__ bool fold_cta(const PoolView& pv, size_t hd, int n, const float* lbg,
         for (int r = 0; r < 16; ++r)
             st4(reinterpret_cast<float*>(pv.base) + hd * (kD * kD) + (i0 + r) * kD + 4 * lane,
                 make_float4(lo[r].x, lo[r].y, hi[r].x, hi[r].y));
-    } else if (pv.colf != nullptr) {
-        __syncthreads();  // the staged chunks are consumed: their area holds the column maxima
-        quantize_cols_cta(lo, hi, pv.base, hd, pv.scale + hd * kD, pv.colf + hd * kD,
-                          reinterpret_cast<float*>(fs.a2), fs.kv);
     } else {
-        // per-row absmax over the 128 columns (warp-wide), one division pair
-        // per row in the lane that holds it, factors broadcast back
-        float mx[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r)
-            mx[r] = fmaxf(fmaxf(fabsf(lo[r].x), fabsf(lo[r].y)), fmaxf(fabsf(hi[r].x), fabsf(hi[r].y)));
-        float s_mine, f_mine;
-        row_quant_params(warp_max16_scatter(mx, lane), s_mine, f_mine);
-        if ((lane & 1) == 0) pv.scale[hd * kD + i0 + (lane >> 1)] = s_mine;
-#pragma unroll
-        for (int qd = 0; qd < 4; ++qd) {
-            float f[4];
-#pragma unroll
-            for (int r = 0; r < 4; ++r) f[r] = __shfl_sync(0xffffffffu, f_mine, 2 * (4 * qd + r));
-            reinterpret_cast<uint4*>(pv.base)[quad_index(hd, i0 / 4 + qd, lane)] = pack_quad(lo, hi, 4 * qd, f);
-        }
+        // INT8 window boundary: compensator pairs first, then the residual's
+        // codes; the staged chunks are consumed, so their area is scratch
+        __syncthreads();
+        if constexpr (COMP)
+            fit_compensators_cta(lo, hi, pv, hd, fs.kv, fs.qv, fs.vv, reinterpret_cast<float*>(fs.a2), fs.misc);
+        if (pv.colf != nullptr)
+            quantize_cols_cta(lo, hi, pv.base, hd, pv.scale + hd * kD, pv.colf + hd * kD,
+                              reinterpret_cast<float*>(fs.a2), fs.kv);
+        else
+            quantize_rows_cta(lo, hi, pv.base, hd, pv.scale + hd * kD);
     }
     return true;
 }

@@ -39,11 +39,15 @@ def _need(t: torch.Tensor, name: str, dtype, device, shape=None):
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
+def _flags(col_scales: bool, compensators: int) -> int:
+    return (N.LS_INT8_COLUMN_SCALES if col_scales else 0) | N.LS_INT8_COMPENSATORS(compensators)
+
+
 def required_bytes(num_slots, num_heads, variant="eager", gate="scalar", window=0,
-                   d_k=128, d_v=128, col_scales=False) -> int:
+                   d_k=128, d_v=128, col_scales=False, compensators=0) -> int:
     lib = N.load()
     d = N.LsDesc(num_slots, num_heads, d_k, d_v, VARIANTS[variant], GATES[gate], window,
-                 N.LS_INT8_COLUMN_SCALES if col_scales else 0)
+                 _flags(col_scales, compensators))
     out = C.c_size_t(0)
     N.check(lib.ls_pool_required_bytes(C.byref(d), C.byref(out)), "ls_pool_required_bytes")
     return int(out.value)
@@ -57,11 +61,12 @@ class StatePool:
     gate: "scalar" (Gated DeltaNet) or "per_key" (KDA).
     col_scales (int8): the smoothed per-value-column format (LeapQuant §3.4
     eq. 7, App. B.3) instead of one scale per key row.
+    compensators (int8): r Compensator Tokens per window (LeapQuant §3.3).
     """
 
     def __init__(self, num_slots: int, num_heads: int, variant: str = "eager",
                  gate: str = "scalar", window: int = 0, d_k: int = 128, d_v: int = 128,
-                 device=None, stream=None, col_scales: bool = False):
+                 device=None, stream=None, col_scales: bool = False, compensators: int = 0):
         self.lib = N.load()
         self.variant, self.gate = variant, gate
         self.P, self.H, self.d_k, self.d_v = int(num_slots), int(num_heads), int(d_k), int(d_v)
@@ -74,8 +79,9 @@ class StatePool:
             dev = torch.device("cuda", torch.cuda.current_device())
         self.device = dev
         self.col_scales = bool(col_scales)
+        self.compensators = int(compensators)
         self.desc = N.LsDesc(self.P, self.H, self.d_k, self.d_v, VARIANTS[variant], GATES[gate],
-                             self.window, N.LS_INT8_COLUMN_SCALES if self.col_scales else 0)
+                             self.window, _flags(self.col_scales, self.compensators))
         nbytes = C.c_size_t(0)
         N.check(self.lib.ls_pool_required_bytes(C.byref(self.desc), C.byref(nbytes)),
                 "ls_pool_required_bytes")
@@ -205,6 +211,18 @@ class StatePool:
                                                       C.c_void_p(_stream(stream))),
                 "ls_pool_read_int8_col_scales")
         return b
+
+    def read_compensators(self, slots, stream=None):
+        """compensator pools: the current pairs (K~ [n, H, r, d_k], U~ [n, H, r, d_v])."""
+        slots = self._slots(slots)
+        n = int(slots.numel())
+        r = self.compensators
+        kk = torch.empty(n, self.H, r, self.d_k, dtype=torch.float32, device=self.device)
+        uu = torch.empty(n, self.H, r, self.d_v, dtype=torch.float32, device=self.device)
+        N.check(self.lib.ls_pool_read_compensators(self.handle, _ptr(slots), n, _ptr(kk), _ptr(uu),
+                                                   C.c_void_p(_stream(stream))),
+                "ls_pool_read_compensators")
+        return kk, uu
 
     def read_log_meta(self, slots, stream=None):
         """(live log length [n, H] int32, cumulative log-decay [n, H, dl] float32)."""

@@ -14,13 +14,14 @@ from recurrent_state_quantization_gb300 import workloads as wl
 D = 128
 
 
-def make_oracle(variant, nstates, dl, window, nthreads=0, col_scales=False):
+def make_oracle(variant, nstates, dl, window, nthreads=0, col_scales=False, compensators=0):
     if variant == "eager":
         return oracle.EagerOracle(nstates, D, D, dl, nthreads)
     if variant == "deferred":
         return oracle.DeferredOracle(nstates, D, D, dl, window, nthreads)
     if variant == "int8":
-        return oracle.WindowInt8Oracle(nstates, D, D, dl, window, nthreads, col_scales=col_scales)
+        return oracle.WindowInt8Oracle(nstates, D, D, dl, window, nthreads, col_scales=col_scales,
+                                       compensators=compensators)
     raise ValueError(variant)
 
 
@@ -68,14 +69,15 @@ class Pair:
     """A GPU pool and an oracle stepped together over a workload."""
 
     def __init__(self, w: wl.Workload, variant: str, window: int, n_sample=None, device="cuda",
-                 seed=0, nthreads=0, col_scales=False):
+                 seed=0, nthreads=0, col_scales=False, compensators=0):
         self.w, self.variant, self.window = w, variant, window
         self.col_scales = bool(col_scales)
+        self.compensators = int(compensators)
         self.dev = torch.device(device)
         self.pool = StatePool(w.num_slots, w.heads, variant, w.gate, window, device=self.dev,
-                              col_scales=col_scales)
+                              col_scales=col_scales, compensators=compensators)
         self.orc = make_oracle(variant, w.num_slots * w.heads, w.dl, window, nthreads,
-                               col_scales=col_scales)
+                               col_scales=col_scales, compensators=compensators)
         self.slot_idx = wl.slot_index(w, self.dev)
         self.sample = sample_rows(w, self.slot_idx, n_sample, seed)
         self.masks = wl.static_masks(w, self.dev)
@@ -161,19 +163,52 @@ class Pair:
         pos = {int(x): i for i, x in enumerate(uniq)}
         _, fro = self.orc.codes(s.state_idx)
         fco = self.orc.col_factors(s.state_idx)
+        mag = np.abs(self.orc.logical(s.state_idx)).reshape(len(s.rows), -1).max(axis=1)
         worst = 0.0
         for n_, r in enumerate(s.rows):
+            o_r = fro[n_].astype(np.float64)
+            o_c = fco[n_].astype(np.float64) if fc is not None else np.ones(1)
+            # compensator pools: factors of residual rows / columns at the
+            # rounding floor (see code_mismatch) are not determined
+            keep_r = np.ones(o_r.shape, bool)
+            keep_c = np.ones(o_c.shape, bool)
+            if self.compensators:
+                floor = (2.0 ** -18) * mag[n_] / 127.0
+                keep_r = o_r * np.abs(o_c).max() > floor
+                keep_c = np.abs(o_r).max() * o_c > floor
             g = fr[pos[int(slots_b[n_])], r % w.heads].astype(np.float64)
-            o = fro[n_].astype(np.float64)
-            worst = max(worst, float(np.max(np.abs(g - o) / np.maximum(np.abs(o), 1e-30))))
+            rel = np.abs(g - o_r) / np.maximum(np.abs(o_r), 1e-30)
+            worst = max(worst, float(np.max(rel[keep_r], initial=0.0)))
             if fc is not None:
                 g = fc[pos[int(slots_b[n_])], r % w.heads].astype(np.float64)
-                o = fco[n_].astype(np.float64)
-                worst = max(worst, float(np.max(np.abs(g - o) / np.maximum(np.abs(o), 1e-30))))
+                rel = np.abs(g - o_c) / np.maximum(np.abs(o_c), 1e-30)
+                worst = max(worst, float(np.max(rel[keep_c], initial=0.0)))
+        return worst
+
+    def comp_err(self):
+        """Compensator pools: max relative error of K~ U~^T (the pairs'
+        contribution) over the sampled heads, against the oracle's."""
+        w, s = self.w, self.sample
+        slots_b = self.slot_idx.cpu().numpy()[s.rows // w.heads]
+        uniq = np.unique(slots_b)
+        kk, uu = self.pool.read_compensators(torch.as_tensor(uniq, dtype=torch.int32, device=self.dev))
+        kk, uu = kk.double().cpu().numpy(), uu.double().cpu().numpy()
+        pos = {int(x): i for i, x in enumerate(uniq)}
+        ko, uo = self.orc.compensators(s.state_idx)
+        worst = 0.0
+        for n_, r in enumerate(s.rows):
+            g = np.einsum("hi,hj->ij", kk[pos[int(slots_b[n_])], r % w.heads], uu[pos[int(slots_b[n_])], r % w.heads])
+            o = np.einsum("hi,hj->ij", ko[n_], uo[n_])
+            worst = max(worst, relmax(g, o))
         return worst
 
     def code_mismatch(self):
-        """INT8: (fraction of codes that differ, max |difference|) over sampled heads."""
+        """INT8: (fraction of codes that differ, max |difference|) over sampled heads.
+
+        Compensator pools: only codes whose quantization step (by the
+        oracle's factors) is above 2^-18 of the state's magnitude are
+        compared; below it the residual is the rounding left by the fitted
+        pairs and its codes are not determined."""
         w, s = self.w, self.sample
         slots_b = self.slot_idx.cpu().numpy()[s.rows // w.heads]
         uniq = np.unique(slots_b)
@@ -181,10 +216,21 @@ class Pair:
         Z = Z.cpu().numpy()
         pos = {int(x): i for i, x in enumerate(uniq)}
         Zo, so = self.orc.codes(s.state_idx)
+        masks = None
+        if self.compensators:
+            step = so.astype(np.float64)[:, :, None] * np.ones((1, 1, D))
+            if self.col_scales:
+                step = step * self.orc.col_factors(s.state_idx).astype(np.float64)[:, None, :]
+            mag = np.abs(self.orc.logical(s.state_idx)).reshape(len(s.rows), -1).max(axis=1)
+            masks = step * 127.0 > (2.0 ** -18) * mag[:, None, None]
         diff = 0
         mx = 0
+        count = 0
         for n_, r in enumerate(s.rows):
             d = np.abs(Z[pos[int(slots_b[n_])], r % w.heads].astype(np.int32) - Zo[n_].astype(np.int32))
+            if masks is not None:
+                d = d[masks[n_]]
+            count += d.size
             diff += int((d > 0).sum())
-            mx = max(mx, int(d.max()))
-        return diff / (len(s.rows) * D * D), mx
+            mx = max(mx, int(d.max()) if d.size else 0)
+        return diff / max(count, 1), mx

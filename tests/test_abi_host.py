@@ -96,6 +96,24 @@ def test_column_scale_flag(lib):
         assert rc == N.LS_ERR_INVALID
 
 
+def test_compensator_flag(lib):
+    """LS_INT8_COMPENSATORS(r): INT8 only, r <= 8; the log holds W + r entries
+    (K, U, and the scalar-gate snapshots padded to 4)."""
+    from recurrent_state_quantization_gb300 import _native as N
+    P, Hh, W, r = 4, 2, 16, 4
+    nh = P * Hh
+    al = lambda x: (x + 255) // 256 * 256
+    rc, b = _bytes(lib, _desc(flags=N.LS_INT8_COMPENSATORS(r)))
+    C = W + r
+    expect = (256 + al(nh * 128 * 128) + al(nh * 128 * 4) + al(nh * 4)
+              + al(nh * 4) + 2 * al(nh * C * 128 * 4) + al(nh * ((C + 3) // 4 * 4) * 4))
+    assert rc == 0 and b == expect
+    rc, _ = _bytes(lib, _desc(flags=N.LS_INT8_COMPENSATORS(9)))
+    assert rc == N.LS_ERR_INVALID
+    rc, _ = _bytes(lib, _desc(variant=N.LS_DEFERRED_FP32, flags=N.LS_INT8_COMPENSATORS(1)))
+    assert rc == N.LS_ERR_INVALID
+
+
 def test_eager_ignores_window(lib):
     from recurrent_state_quantization_gb300 import _native as N
     rc, _ = _bytes(lib, _desc(variant=N.LS_EAGER_FP32, window=0))

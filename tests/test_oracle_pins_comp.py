@@ -34,7 +34,7 @@ def test_rank_one_state_is_captured_exactly(oracle_mod):
 
 @pytest.mark.parametrize("r", [1, 2, 4])
 def test_gapped_spectrum_matches_truncated_svd(oracle_mod, r):
-    """With singular values 1e6, 1e4, 1e2, 1, ... two power steps per pair
+    """With singular values 1e6, 1e4, 1e2, 1, ... three power steps per pair
     reach the top-r subspace: sum_h k~_h u~_h^T is the best rank-r
     approximation (the truncated SVD), and the residual is what is left."""
     rng = np.random.default_rng(71)
@@ -86,8 +86,8 @@ def test_compensators_cut_outlier_quantization_error(oracle_mod):
 @pytest.mark.parametrize("cols", [False, True])
 @pytest.mark.parametrize("gate,dl", GATES)
 def test_window_of_one_with_compensators(oracle_mod, gate, dl, cols):
-    """W = 1: every token ends a window: fit (warm from the last pairs),
-    quantize the residual, restart from dequant + K~ U~^T."""
+    """W = 1: every token ends a window: fit (cold start), quantize the
+    residual, restart from dequant + K~ U~^T."""
     rng = np.random.default_rng(75)
     n, T, r = 2, 6, 2
     w = oracle_mod.WindowInt8Oracle(n, DK, DV, dl, W=1, col_scales=cols, compensators=r)
@@ -95,14 +95,14 @@ def test_window_of_one_with_compensators(oracle_mod, gate, dl, cols):
     quant = oracle_mod.quantize_cols if cols else oracle_mod.quantize_rows
     deq = oracle_mod.dequantize_cols if cols else oracle_mod.dequantize_rows
 
-    def boundary(S, warm):
-        R, ck, cu = oracle_mod.fit_compensators(S, r, warm_cu=warm)
+    def boundary(S):
+        R, ck, cu = oracle_mod.fit_compensators(S, r)
         q = quant(R)
         return deq(*q) + np.einsum("nhi,nhj->nij", ck, cu), q, cu
 
     S0 = rng.standard_normal((n, DK, DV))
     w.load(range(n), S0)
-    S, q, cu = boundary(S0, None)
+    S, q, cu = boundary(S0)
     assert np.array_equal(w.Z, q[0])
     assert relerr(w.logical(range(n)), S) < 1e-13
     e.load(range(n), S)
@@ -111,7 +111,7 @@ def test_window_of_one_with_compensators(oracle_mod, gate, dl, cols):
         yw = w.step(range(n), q_[t], k_[t], v_[t], lam[t], b[t])
         ye = e.step(range(n), q_[t], k_[t], v_[t], lam[t], b[t])
         assert relerr(yw, ye) < 1e-13
-        S, q, cu = boundary(e.S, cu)
+        S, q, cu = boundary(e.S)
         assert np.array_equal(w.Z, q[0])
         assert relerr(w.logical(range(n)), S) < 1e-12
         e.load(range(n), S)
