@@ -2,10 +2,10 @@
 close the deferred FP32 trajectory stays to the eager one, per 1024-token
 block, on the GPU (every head) and in the oracle (sampled heads).
 
-Four pools (eager, deferred with the workload's merge interval, INT8 with
-window W in the per-key-row format and in the smoothed per-value-column
-format) and their oracles run the same seeded tokens, free-running (no
-restarts).  At the end of every block:
+Five pools (eager, deferred with the workload's merge interval, INT8 with
+window W in the per-key-row format, in the smoothed per-value-column format,
+and in that format with 4 Compensator Tokens) and their oracles run the same
+seeded tokens, free-running (no restarts).  At the end of every block:
 
 - state: ||S_int8 - S_fp32||_F / ||S_fp32||_F over the logical states
   (ls_pool_read), S_fp32 the eager trajectory;
@@ -80,15 +80,16 @@ def test_drift_report(wi, window, n_sample):
     pd = H.Pair(w, "deferred", w.merge_interval, n_sample=n_sample)
     pi = H.Pair(w, "int8", window, n_sample=n_sample)
     pc = H.Pair(w, "int8", window, n_sample=n_sample, col_scales=True)
+    pk = H.Pair(w, "int8", window, n_sample=n_sample, col_scales=True, compensators=4)
     all_slots = torch.arange(w.num_slots, dtype=torch.int32, device=pe.dev)
     blocks = []
     run = {k: 0.0 for k in ("g_s_num", "g_s_den", "o_s_num", "o_s_den", "g_y_num", "g_y_den",
-                            "o_y_num", "o_y_den", "gc_s_num", "oc_s_num")}
+                            "o_y_num", "o_y_den", "gc_s_num", "oc_s_num", "gk_s_num", "ok_s_num")}
     acc = None
     for t in range(w.tokens):
         if acc is None:
             acc = {k: 0.0 for k in ("gy_num", "gy_den", "gys_num", "oy_num", "oy_den",
-                                    "gcy_num", "ocy_num")}
+                                    "gcy_num", "ocy_num", "gky_num", "oky_num")}
             acc["gdy"], acc["ody"] = _HeadMax(), _HeadMax()
         ye, yoe = pe.step(t)
         yd, yod = pd.step(t)
@@ -96,6 +97,9 @@ def test_drift_report(wi, window, n_sample):
         yc, yoc = pc.step(t)
         acc["gcy_num"] += float(((yc - ye) ** 2).sum())
         acc["ocy_num"] += float(((yoc - yoe) ** 2).sum())
+        yk, yok = pk.step(t)
+        acc["gky_num"] += float(((yk - ye) ** 2).sum())
+        acc["oky_num"] += float(((yok - yoe) ** 2).sum())
         acc["gy_num"] += float(((yi - ye) ** 2).sum())
         acc["gy_den"] += float((ye ** 2).sum())
         rows = torch.as_tensor(pi.sample.rows, device=pi.dev)
@@ -111,6 +115,7 @@ def test_drift_report(wi, window, n_sample):
             Sd = pd.pool.read(all_slots)
             Si = pi.pool.read(all_slots)
             Sc = pc.pool.read(all_slots)
+            Sk = pk.pool.read(all_slots)
             g_s = float((Si - Se).norm() / Se.norm())
             g_d = _head_relmax(Sd.reshape(-1, 128, 128), Se.reshape(-1, 128, 128))
             gse, gsi = _rows_view(Se, pe), _rows_view(Si, pi)
@@ -118,7 +123,9 @@ def test_drift_report(wi, window, n_sample):
             od = pd.orc.logical(pd.sample.state_idx)
             oi = pi.orc.logical(pi.sample.state_idx)
             oc = pc.orc.logical(pc.sample.state_idx)
+            ok = pk.orc.logical(pk.sample.state_idx)
             gsc = _rows_view(Sc, pc)
+            gsk = _rows_view(Sk, pk)
             o_s = H.rel_l2(oi, oe)
             o_d = max(H.relmax(od[n], oe[n]) for n in range(len(oe)))
             blk = {"tokens": t + 1,
@@ -128,13 +135,17 @@ def test_drift_report(wi, window, n_sample):
                            "deferred_vs_eager_state_relmax": g_d,
                            "deferred_vs_eager_y_relmax": acc["gdy"].value(),
                            "state_int8_smoothed_vs_fp32": float((Sc - Se).norm() / Se.norm()),
-                           "y_int8_smoothed_vs_fp32": (acc["gcy_num"] / acc["gy_den"]) ** 0.5},
+                           "y_int8_smoothed_vs_fp32": (acc["gcy_num"] / acc["gy_den"]) ** 0.5,
+                           "state_int8_comp_vs_fp32": float((Sk - Se).norm() / Se.norm()),
+                           "y_int8_comp_vs_fp32": (acc["gky_num"] / acc["gy_den"]) ** 0.5},
                    "oracle": {"state_int8_vs_fp32": o_s,
                               "y_int8_vs_fp32": (acc["oy_num"] / acc["oy_den"]) ** 0.5,
                               "deferred_vs_eager_state_relmax": o_d,
                               "deferred_vs_eager_y_relmax": acc["ody"].value(),
                               "state_int8_smoothed_vs_fp32": H.rel_l2(oc, oe),
-                              "y_int8_smoothed_vs_fp32": (acc["ocy_num"] / acc["oy_den"]) ** 0.5}}
+                              "y_int8_smoothed_vs_fp32": (acc["ocy_num"] / acc["oy_den"]) ** 0.5,
+                              "state_int8_comp_vs_fp32": H.rel_l2(ok, oe),
+                              "y_int8_comp_vs_fp32": (acc["oky_num"] / acc["oy_den"]) ** 0.5}}
             blocks.append(blk)
             run["g_s_num"] += float(((gsi - gse) ** 2).sum())
             run["g_s_den"] += float((gse ** 2).sum())
@@ -143,13 +154,15 @@ def test_drift_report(wi, window, n_sample):
             run["g_y_num"] += acc["gys_num"]
             run["gc_s_num"] += float(((gsc - gse) ** 2).sum())
             run["oc_s_num"] += float(((oc - oe) ** 2).sum())
+            run["gk_s_num"] += float(((gsk - gse) ** 2).sum())
+            run["ok_s_num"] += float(((ok - oe) ** 2).sum())
             run["o_y_num"] += acc["oy_num"]
             run["o_y_den"] += acc["oy_den"]
             acc = None
     report = {"workload": w.name, "int8_window": window, "deferred_merge_interval": w.merge_interval,
               "sampled_heads": int(len(pi.sample.rows)), "blocks": blocks}
     print("drift-report " + json.dumps(report))
-    for p in (pe, pd, pi, pc):
+    for p in (pe, pd, pi, pc, pk):
         assert p.pool.status() == 0
     # deferred FP32 stays on the eager trajectory (both are FP32 recurrences
     # of the same state), on the GPU and in the oracle
@@ -168,3 +181,6 @@ def test_drift_report(wi, window, n_sample):
     gc_s = (run["gc_s_num"] / run["g_s_den"]) ** 0.5
     oc_s = (run["oc_s_num"] / run["o_s_den"]) ** 0.5
     assert gc_s <= 1.25 * oc_s + 1e-6, (gc_s, oc_s)
+    gk_s = (run["gk_s_num"] / run["g_s_den"]) ** 0.5
+    ok_s = (run["ok_s_num"] / run["o_s_den"]) ** 0.5
+    assert gk_s <= 1.25 * ok_s + 1e-6, (gk_s, ok_s)
