@@ -37,8 +37,8 @@ def _load():
         P = C.c_void_p
         I64, I32 = C.c_int64, C.c_int
         lib.orc_max_threads.restype = I32
-        lib.orc_eager_step.argtypes = [I64, I32, I32, I32, P, P, P, P, P, P, P, P, I32]
-        lib.orc_deferred_step.argtypes = [I64, I32, I32, I32, I32, P, P, P, P, P, P,
+        lib.orc_eager_step.argtypes = [I64, I32, I32, I32, I32, P, P, P, P, P, P, P, P, I32]
+        lib.orc_deferred_step.argtypes = [I64, I32, I32, I32, I32, I32, P, P, P, P, P, P,
                                           P, P, P, P, P, P, P, I32]
         lib.orc_deferred_logical.argtypes = [I64, I32, I32, I32, I32, P, P, P, P, P, P, P, P]
         lib.orc_deferred_commit.argtypes = [I64, I32, I32, I32, I32, P, P, P, P, P, P, P]
@@ -107,17 +107,22 @@ class _Base:
 
 
 class EagerOracle(_Base):
-    """Eager recurrence of every state (LeapQuant App. A with eq. 1)."""
+    """Eager recurrence of every state (LeapQuant App. A with eq. 1).
 
-    def __init__(self, nstates, dk, dv, dl, nthreads=0):
+    plain=True: the update pair (k, v) without the delta-rule correction
+    (DeltaLog Table 1, the linear attention / RetNet / GLA / RWKV6 rows)."""
+
+    def __init__(self, nstates, dk, dv, dl, nthreads=0, plain=False):
         super().__init__(nstates, dk, dv, dl, nthreads)
+        self.rule = 1 if plain else 0
         self.S = np.zeros((self.n, dk, dv), dtype=np.float64)
 
     def step(self, idx, q, k, v, lam, beta) -> np.ndarray:
         idx = self._idx(idx)
         q, k, v, lam, beta = self._inputs(idx, q, k, v, lam, beta)
         y = np.zeros((idx.size, self.dv), dtype=np.float64)
-        _check(_load().orc_eager_step(idx.size, self.dk, self.dv, self.dl, _p(self.S), _p(idx),
+        _check(_load().orc_eager_step(idx.size, self.rule, self.dk, self.dv, self.dl, _p(self.S),
+                                      _p(idx),
                                       _p(q), _p(k), _p(v), _p(lam), _p(beta), _p(y),
                                       self.nthreads), "eager step")
         return y
@@ -136,13 +141,15 @@ class EagerOracle(_Base):
 
 
 class DeferredOracle(_Base):
-    """Base + bounded log, DeltaLog Algorithm 1 with merge interval M."""
+    """Base + bounded log, DeltaLog Algorithm 1 with merge interval M
+    (plain=True: update pair (k, v), as EagerOracle)."""
 
-    def __init__(self, nstates, dk, dv, dl, M, nthreads=0):
+    def __init__(self, nstates, dk, dv, dl, M, nthreads=0, plain=False):
         super().__init__(nstates, dk, dv, dl, nthreads)
         if M < 1:
             raise ValueError("M >= 1")
         self.M = int(M)
+        self.rule = 1 if plain else 0
         Cap = max(self.M - 1, 0)
         self.base = np.zeros((self.n, dk, dv), dtype=np.float64)
         self.lbar = np.zeros((self.n, dl), dtype=np.float64)
@@ -163,7 +170,7 @@ class DeferredOracle(_Base):
         q, k, v, lam, beta = self._inputs(idx, q, k, v, lam, beta)
         y = np.zeros((idx.size, self.dv), dtype=np.float64)
         self._stride_guard()
-        _check(_load().orc_deferred_step(idx.size, self.dk, self.dv, self.dl, self.M,
+        _check(_load().orc_deferred_step(idx.size, self.rule, self.dk, self.dv, self.dl, self.M,
                                          *self._arrays(), _p(idx), _p(q), _p(k), _p(v),
                                          _p(lam), _p(beta), _p(y), self.nthreads),
                "deferred step")

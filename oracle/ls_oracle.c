@@ -108,10 +108,14 @@ static double dlam_at(const double *lam, int dl, int i)
  *     y   = S_t^T q
  * y is formed from the updated S_t itself, not from a fused expression.
  * u_out (dv doubles) receives u when non-NULL.
+ * rule 1 (no delta correction): u = v, the update pair (k_t, v_t) of the
+ * linear attention / RetNet / GLA / RWKV6 rows of [DL] Table 1 (read vector
+ * b_t = 0 in [LQ] App. A); beta is not used.
  */
-static void eager_one(int dk, int dv, int dl, double *S, const float *q,
-                      const float *k, const float *v, const float *lam,
-                      float beta, double *y, double *r, double *u_out)
+static void eager_one(int rule, int dk, int dv, int dl, double *S,
+                      const float *q, const float *k, const float *v,
+                      const float *lam, float beta, double *y, double *r,
+                      double *u_out)
 {
     for (int j = 0; j < dv; ++j) r[j] = 0.0;
     for (int i = 0; i < dk; ++i) {
@@ -120,7 +124,8 @@ static void eager_one(int dk, int dv, int dl, double *S, const float *q,
         for (int j = 0; j < dv; ++j) r[j] += Si[j] * w;
     }
     /* u overwrites r in place */
-    for (int j = 0; j < dv; ++j) r[j] = (double)beta * ((double)v[j] - r[j]);
+    for (int j = 0; j < dv; ++j)
+        r[j] = rule == 1 ? (double)v[j] : (double)beta * ((double)v[j] - r[j]);
     for (int i = 0; i < dk; ++i) {
         const double a = exp(lam_at(lam, dl, i));
         const double ki = (double)k[i];
@@ -137,12 +142,12 @@ static void eager_one(int dk, int dv, int dl, double *S, const float *q,
         for (int j = 0; j < dv; ++j) u_out[j] = r[j];
 }
 
-int orc_eager_step(int64_t n, int dk, int dv, int dl, double *S,
+int orc_eager_step(int64_t n, int rule, int dk, int dv, int dl, double *S,
                    const int64_t *idx, const float *q, const float *k,
                    const float *v, const float *lam, const float *beta,
                    double *y, int nthreads)
 {
-    if (n < 0 || !valid_dims(dk, dv, dl)) return ORC_ERR_ARG;
+    if (n < 0 || !valid_dims(dk, dv, dl) || (rule != 0 && rule != 1)) return ORC_ERR_ARG;
     if (n == 0) return ORC_OK;
     set_threads(nthreads);
     int err = 0;
@@ -156,7 +161,7 @@ int orc_eager_step(int64_t n, int dk, int dv, int dl, double *S,
 #pragma omp for schedule(dynamic, 4)
             for (int64_t row = 0; row < n; ++row) {
                 double *Sr = S + (size_t)idx[row] * dk * dv;
-                eager_one(dk, dv, dl, Sr, q + row * dk, k + row * dk,
+                eager_one(rule, dk, dv, dl, Sr, q + row * dk, k + row * dk,
                           v + row * dv, lam + row * dl, beta[row],
                           y + row * dv, r, NULL);
             }
@@ -220,9 +225,9 @@ static void deferred_represented(int dk, int dv, int dl, const double *base,
  *   4. L < C : append (k, u, lbar) at entry L, L <- L + 1       (eq. 5)
  *      L = C : S-bar <- D(lbar) S-bar + sum D(lbar - Lambda_i) K_i U_i^T
  *                       + a_t b_t^T, then lbar <- 0, L <- 0     (eq. 6)
- * work: 2*dk*dv doubles.
+ * work: 2*dk*dv doubles.  rule 1: b_t = v (no delta correction, as eager_one).
  */
-static void deferred_one(int dk, int dv, int dl, int M, double *base,
+static void deferred_one(int rule, int dk, int dv, int dl, int M, double *base,
                          double *lbar, double *K, double *U, double *Lam,
                          int32_t *Lp, const float *q, const float *k,
                          const float *v, const float *lam, float beta,
@@ -247,7 +252,8 @@ static void deferred_one(int dk, int dv, int dl, int M, double *base,
     for (int c = 0; c < dl; ++c) lnew[c] = lbar[c] + (double)lam[c];
     /* 3. update factors and post-update output */
     double u[1024];
-    for (int j = 0; j < dv; ++j) u[j] = (double)beta * ((double)v[j] - r[j]);
+    for (int j = 0; j < dv; ++j)
+        u[j] = rule == 1 ? (double)v[j] : (double)beta * ((double)v[j] - r[j]);
     deferred_represented(dk, dv, dl, base, lnew, K, U, Lam, L, St);
     for (int i = 0; i < dk; ++i)
         for (int j = 0; j < dv; ++j)
@@ -275,13 +281,15 @@ static int deferred_args_ok(int dk, int dv, int dl, int M)
     return valid_dims(dk, dv, dl) && M >= 1 && dk <= 1024 && dv <= 1024;
 }
 
-int orc_deferred_step(int64_t n, int dk, int dv, int dl, int M, double *base,
-                      double *lbar, double *K, double *U, double *Lam,
-                      int32_t *L, const int64_t *idx, const float *q,
-                      const float *k, const float *v, const float *lam,
-                      const float *beta, double *y, int nthreads)
+int orc_deferred_step(int64_t n, int rule, int dk, int dv, int dl, int M,
+                      double *base, double *lbar, double *K, double *U,
+                      double *Lam, int32_t *L, const int64_t *idx,
+                      const float *q, const float *k, const float *v,
+                      const float *lam, const float *beta, double *y,
+                      int nthreads)
 {
-    if (n < 0 || !deferred_args_ok(dk, dv, dl, M)) return ORC_ERR_ARG;
+    if (n < 0 || !deferred_args_ok(dk, dv, dl, M) || (rule != 0 && rule != 1))
+        return ORC_ERR_ARG;
     if (n == 0) return ORC_OK;
     const int C = M - 1;
     set_threads(nthreads);
@@ -296,7 +304,7 @@ int orc_deferred_step(int64_t n, int dk, int dv, int dl, int M, double *base,
 #pragma omp for schedule(dynamic, 2)
             for (int64_t row = 0; row < n; ++row) {
                 const int64_t s = idx[row];
-                deferred_one(dk, dv, dl, M, base + (size_t)s * dk * dv,
+                deferred_one(rule, dk, dv, dl, M, base + (size_t)s * dk * dv,
                              lbar + (size_t)s * dl, K + (size_t)s * C * dk,
                              U + (size_t)s * C * dv, Lam + (size_t)s * C * dl,
                              L + s, q + row * dk, k + row * dk, v + row * dv,
@@ -672,7 +680,7 @@ static void window_one(int mode, int nc, int dk, int dv, int dl, int W,
 {
     const int c = *cntp;
     double u[1024];
-    eager_one(dk, dv, dl, Sw, q, k, v, lam, beta, y, r, u);
+    eager_one(0, dk, dv, dl, Sw, q, k, v, lam, beta, y, r, u);
     for (int t = 0; t < dl; ++t) rl[(size_t)c * dl + t] = (double)lam[t];
     for (int i = 0; i < dk; ++i) rk[(size_t)c * dk + i] = (double)k[i];
     for (int j = 0; j < dv; ++j) ru[(size_t)c * dv + j] = u[j];
