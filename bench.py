@@ -312,6 +312,7 @@ def run_native(args, rank, world, local):
         out["int8_window_sweep"] = window_sweep(w, slot_idx, masks, inputs, ring, dev, hbm_peak,
                                                 peak_kind, pools["eager"])
         out["e2e"] = e2e(w, variants, pools, slot_idx, dev, world)
+        out["rwkv6"] = rwkv6(dev, hbm_peak, peak_kind)
         if rank == 0:
             out["cpu_baseline"] = cpu_baseline(w, variants, budget_s=6.0)
     return out
@@ -355,6 +356,44 @@ def window_sweep(w, slot_idx, masks, inputs, ring, dev, peak, peak_kind, eager_p
         del pools
         torch.cuda.empty_cache()
     return res
+
+
+def rwkv6(dev, peak, peak_kind, tokens=64):
+    """RWKV6 (per-key decay, raw (k, v) updates; DeltaLog Table 1) on one
+    256 x 48-head pool: eager and deferred (M = 16) head-steps/s and
+    algorithmic GB/s, states warmed by one merge cycle."""
+    import torch
+    from recurrent_state_quantization_gb300 import StatePool
+    from recurrent_state_quantization_gb300 import bytemodel as bm
+    from recurrent_state_quantization_gb300 import workloads as wl
+    w = wl.custom("rwkv6_b256_h48", gate="per_key", batch=256, heads=48, tokens=tokens,
+                  seed=7, lam_scale=0.05)
+    slots = torch.arange(w.batch, dtype=torch.int32, device=dev)
+    ins = [wl.step_inputs(w, t, device=dev) for t in range(16)]
+    stream = torch.cuda.current_stream()
+    out = {"workload": w.name, "gate": "per_key", "update": "plain (k, v)"}
+    for variant, M in (("eager", 0), ("deferred", 16)):
+        pool = StatePool(w.num_slots, w.heads, variant, w.gate, M, device=dev, plain=True)
+        y = torch.empty(w.batch, w.heads, w.d_v, device=dev)
+        for t in range(16):
+            pool.decode_step(slots, *ins[t % 16], y=y)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for t in range(tokens):
+            pool.decode_step(slots, *ins[t % 16], y=y)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b)
+        hs = w.batch * w.heads * tokens
+        byt = bm.variant_bytes(variant, "per_key", M or 1)
+        gbs = byt * hs / (ms * 1e-3) / 1e9
+        out[variant] = {"window": M or None, "head_steps_per_s": hs / (ms * 1e-3),
+                        "algorithmic_bytes_per_head_step": byt, "achieved_gbs": gbs,
+                        "frac_of_" + peak_kind + "_hbm": gbs / peak}
+        del pool
+    torch.cuda.empty_cache()
+    return out
 
 
 def e2e(w, variants, pools, slot_idx, dev, world=1, tokens=24):

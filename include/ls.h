@@ -113,6 +113,16 @@ typedef enum {
  * entries, and its window ends on its W-th real token.
  */
 #define LS_MAX_COMPENSATORS 8
+
+/*
+ * ls_pool_desc.flags: LS_PLAIN_UPDATE (LS_EAGER_FP32 / LS_DEFERRED_FP32):
+ * the update pair is the raw (k_t, v_t) with no delta-rule correction,
+ * S_t = D_t S_{t-1} + k_t v_t^T, y_t = S_t^T q_t: the linear attention,
+ * RetNet, GLA and RWKV6 rows of "DeltaLog: Deferred Materialization of
+ * Recurrent States for Linear Attention Decoding", Table 1 (RWKV6 = the
+ * per-key gate).  beta is passed as usual but its values are not used.
+ */
+#define LS_PLAIN_UPDATE (1u << 12)
 #define LS_INT8_COMPENSATORS(r) ((uint32_t)(r) << 8)
 
 typedef struct {
@@ -125,7 +135,8 @@ typedef struct {
     int32_t window;    /* W (INT8) or M (deferred), 1..LS_MAX_WINDOW; ignored
                           (may be 0) for LS_EAGER_FP32                          */
     uint32_t flags;    /* 0; for LS_WINDOW_INT8 also LS_INT8_COLUMN_SCALES and
-                          LS_INT8_COMPENSATORS(r)                              */
+                          LS_INT8_COMPENSATORS(r); for the FP32 variants also
+                          LS_PLAIN_UPDATE                                      */
 } ls_pool_desc;
 
 /* Human-readable name of a status code.  Never NULL. */

@@ -31,6 +31,7 @@ LS_GATE_PER_KEY = 1
 LS_MAX_WINDOW = 256
 LS_INT8_COLUMN_SCALES = 1
 LS_MAX_COMPENSATORS = 8
+LS_PLAIN_UPDATE = 1 << 12
 
 
 def LS_INT8_COMPENSATORS(r: int) -> int:

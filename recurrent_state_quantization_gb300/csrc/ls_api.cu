@@ -36,10 +36,11 @@ struct Layout {
 int make_layout(const ls_pool_desc* d, Layout* L) {
     if (d == nullptr || L == nullptr) return LS_ERR_INVALID;
     if (d->variant < LS_EAGER_FP32 || d->variant > LS_WINDOW_INT8) return LS_ERR_INVALID;
-    const uint32_t known = LS_INT8_COLUMN_SCALES | LS_INT8_COMPENSATORS(15);
-    if ((d->flags & ~known) != 0) return LS_ERR_INVALID;
+    const uint32_t int8_flags = LS_INT8_COLUMN_SCALES | LS_INT8_COMPENSATORS(15);
+    if ((d->flags & ~(int8_flags | LS_PLAIN_UPDATE)) != 0) return LS_ERR_INVALID;
     const uint32_t ncomp = (d->flags >> 8) & 15u;
-    if ((d->flags != 0) && d->variant != LS_WINDOW_INT8) return LS_ERR_INVALID;
+    if ((d->flags & int8_flags) && d->variant != LS_WINDOW_INT8) return LS_ERR_INVALID;
+    if ((d->flags & LS_PLAIN_UPDATE) && d->variant == LS_WINDOW_INT8) return LS_ERR_INVALID;
     if (ncomp > LS_MAX_COMPENSATORS) return LS_ERR_INVALID;
     if (d->gate != LS_GATE_SCALAR && d->gate != LS_GATE_PER_KEY) return LS_ERR_INVALID;
     if (d->num_slots < 1 || d->num_heads < 1) return LS_ERR_INVALID;
@@ -93,6 +94,7 @@ ls::PoolView make_view(const ls_pool_desc& d, const Layout& L, unsigned char* m)
     v.H = d.num_heads;
     v.W = log ? d.window : 0;
     v.R = log ? static_cast<int32_t>((d.flags >> 8) & 15u) : 0;
+    v.plain = (d.flags & LS_PLAIN_UPDATE) ? 1 : 0;
     v.cap = v.W + v.R;
     v.dl = d.gate == LS_GATE_PER_KEY ? kD : 1;
     v.lam_stride = d.gate == LS_GATE_PER_KEY ? v.cap * kD : (v.cap + 3) / 4 * 4;

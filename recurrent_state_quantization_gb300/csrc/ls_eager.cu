@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 3) eager_step_kernel(const StepArgs 
         }
         rr = group8_sum(rr);
         yy = group8_sum(yy);
-        const float u = beta * (v_s[j] - rr);
+        const float u = a.pv.plain ? v_s[j] : beta * (v_s[j] - rr);
         if (g == 0) y_s[j] = fmaf(kq, u, yy);
         float* dst = gtile + j * kD;
 #pragma unroll

@@ -51,6 +51,7 @@ struct PoolView {
                            //   per-key gate [cap][d_k]; scalar gate [cap] padded to 4
     int32_t P, H, W, dl;
     int32_t R;             // INT8: compensator pairs at the head of each window (0: none)
+    int32_t plain;         // 1: update pair (k, v), no delta-rule correction
     int32_t cap;           // log entries per state: W + R
     int32_t lam_stride;    // floats per state in lamlog
 };

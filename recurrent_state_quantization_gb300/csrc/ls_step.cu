@@ -352,8 +352,9 @@ __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, 
     }
 
     // ---- delta correction and output -----------------------------------------
-    const float4 u4 = make_float4(beta * (v4.x - r01.x), beta * (v4.y - r01.y),
-                                  beta * (v4.z - r23.x), beta * (v4.w - r23.y));
+    const float4 u4 = pv.plain ? v4
+                               : make_float4(beta * (v4.x - r01.x), beta * (v4.y - r01.y),
+                                             beta * (v4.z - r23.x), beta * (v4.w - r23.y));
     st4(a.y + ro, make_float4(fmaf(kq, u4.x, y01.x), fmaf(kq, u4.y, y01.y),
                               fmaf(kq, u4.z, y23.x), fmaf(kq, u4.w, y23.y)));
 

@@ -693,7 +693,7 @@ __device__ bool fold_cta(const PoolView& pv, size_t hd, int n, const float* lbg,
                 y0 += rf[(kWarps + w) * kD + tid];
             }
             const float kq = (fs.misc[0] + fs.misc[1]) + (fs.misc[2] + fs.misc[3]);
-            const float u = tok.beta * (fs.vv[tid] - r);
+            const float u = pv.plain ? fs.vv[tid] : tok.beta * (fs.vv[tid] - r);
             fs.uv[tid] = u;
             tok.y[tok.ro + tid] = fmaf(kq, u, y0);
         }

@@ -14,11 +14,12 @@ from recurrent_state_quantization_gb300 import workloads as wl
 D = 128
 
 
-def make_oracle(variant, nstates, dl, window, nthreads=0, col_scales=False, compensators=0):
+def make_oracle(variant, nstates, dl, window, nthreads=0, col_scales=False, compensators=0,
+                plain=False):
     if variant == "eager":
-        return oracle.EagerOracle(nstates, D, D, dl, nthreads)
+        return oracle.EagerOracle(nstates, D, D, dl, nthreads, plain=plain)
     if variant == "deferred":
-        return oracle.DeferredOracle(nstates, D, D, dl, window, nthreads)
+        return oracle.DeferredOracle(nstates, D, D, dl, window, nthreads, plain=plain)
     if variant == "int8":
         return oracle.WindowInt8Oracle(nstates, D, D, dl, window, nthreads, col_scales=col_scales,
                                        compensators=compensators)
@@ -69,15 +70,15 @@ class Pair:
     """A GPU pool and an oracle stepped together over a workload."""
 
     def __init__(self, w: wl.Workload, variant: str, window: int, n_sample=None, device="cuda",
-                 seed=0, nthreads=0, col_scales=False, compensators=0):
+                 seed=0, nthreads=0, col_scales=False, compensators=0, plain=False):
         self.w, self.variant, self.window = w, variant, window
         self.col_scales = bool(col_scales)
         self.compensators = int(compensators)
         self.dev = torch.device(device)
         self.pool = StatePool(w.num_slots, w.heads, variant, w.gate, window, device=self.dev,
-                              col_scales=col_scales, compensators=compensators)
+                              col_scales=col_scales, compensators=compensators, plain=plain)
         self.orc = make_oracle(variant, w.num_slots * w.heads, w.dl, window, nthreads,
-                               col_scales=col_scales, compensators=compensators)
+                               col_scales=col_scales, compensators=compensators, plain=plain)
         self.slot_idx = wl.slot_index(w, self.dev)
         self.sample = sample_rows(w, self.slot_idx, n_sample, seed)
         self.masks = wl.static_masks(w, self.dev)

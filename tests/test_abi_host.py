@@ -96,6 +96,17 @@ def test_column_scale_flag(lib):
         assert rc == N.LS_ERR_INVALID
 
 
+def test_plain_update_flag(lib):
+    """LS_PLAIN_UPDATE: the FP32 variants only; no extra memory."""
+    from recurrent_state_quantization_gb300 import _native as N
+    for variant in (N.LS_EAGER_FP32, N.LS_DEFERRED_FP32):
+        rc0, b0 = _bytes(lib, _desc(variant=variant))
+        rc1, b1 = _bytes(lib, _desc(variant=variant, flags=N.LS_PLAIN_UPDATE))
+        assert rc0 == rc1 == 0 and b0 == b1
+    rc, _ = _bytes(lib, _desc(flags=N.LS_PLAIN_UPDATE))
+    assert rc == N.LS_ERR_INVALID
+
+
 def test_compensator_flag(lib):
     """LS_INT8_COMPENSATORS(r): INT8 only, r <= 8; the log holds W + r entries
     (K, U, and the scalar-gate snapshots padded to 4)."""

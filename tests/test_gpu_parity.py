@@ -118,6 +118,23 @@ def test_gdn_b1_h4_t64(variant, window):
 CASES = [("eager", 0), ("deferred", 1), ("deferred", 3), ("deferred", 16),
          ("int8", 1), ("int8", 3), ("int8", 16), ("int8", 40)]
 
+# the plain update rule (no delta-rule correction): RWKV6 with the per-key gate
+
+
+@pytest.mark.parametrize("gate", ["scalar", "per_key"])
+@pytest.mark.parametrize("variant,window", [("eager", 0), ("deferred", 1), ("deferred", 4),
+                                            ("deferred", 16)])
+def test_small_ragged_plain(gate, variant, window):
+    from recurrent_state_quantization_gb300 import workloads as wl
+    H = _harness()
+    w = wl.custom("ragged-plain", gate=gate, batch=5, heads=3, tokens=37, num_slots=7,
+                  windows=(max(window, 1),), merge_interval=max(window, 1), permute_slots=True,
+                  seed=31 + window, lam_scale=0.3)
+    p = H.Pair(w, variant, window, plain=True)
+    run_lockstep(p, w.tokens)
+    check_fp32(p)
+    assert p.pool.status() == 0
+
 
 @pytest.mark.parametrize("gate", ["scalar", "per_key"])
 @pytest.mark.parametrize("variant,window,cols,comp", [c + (False, 0) for c in CASES] +
@@ -226,6 +243,18 @@ def test_gdn_serving_b256_h48_4pools(variant, window, cols):
     w = wl.WORKLOADS[3]
     _assert_full(_full(3, variant, window, n_sample=6, pools=w.pools, cols=cols,
                        prewarm=_prewarm_factory(w.prewarm_tokens)), variant)
+
+
+@pytest.mark.parametrize("variant,window", [("eager", 0), ("deferred", 16)])
+def test_rwkv6_b128_h32_t512(variant, window):
+    """RWKV6 (per-key decay, raw (k, v) updates) on the KDA 128x32 shapes."""
+    from recurrent_state_quantization_gb300 import workloads as wl
+    H = _harness()
+    w = wl.WORKLOADS[2]
+    p = H.Pair(w, variant, window, n_sample=16, plain=True)
+    run_lockstep(p, w.tokens)
+    check_fp32(p)
+    assert p.pool.status() == 0
 
 
 def test_gdn_serving_b256_h48_compensators():
