@@ -38,7 +38,7 @@ def _load():
         I64, I32 = C.c_int64, C.c_int
         lib.orc_max_threads.restype = I32
         lib.orc_eager_step.argtypes = [I64, I32, I32, I32, I32, P, P, P, P, P, P, P, P, I32]
-        lib.orc_deferred_step.argtypes = [I64, I32, I32, I32, I32, I32, P, P, P, P, P, P,
+        lib.orc_deferred_step.argtypes = [I64, I32, I32, I32, I32, I32, I32, P, P, P, P, P, P,
                                           P, P, P, P, P, P, P, I32]
         lib.orc_deferred_logical.argtypes = [I64, I32, I32, I32, I32, P, P, P, P, P, P, P, P]
         lib.orc_deferred_commit.argtypes = [I64, I32, I32, I32, I32, P, P, P, P, P, P, P]
@@ -47,7 +47,7 @@ def _load():
         lib.orc_quantize_cols.argtypes = [I64, I32, I32, P, P, P, P]
         lib.orc_fit_compensators.argtypes = [I64, I32, I32, I32, P, P, P, I32]
         lib.orc_dequantize_cols.argtypes = [I64, I32, I32, P, P, P, P]
-        lib.orc_window_step.argtypes = [I64, I32, I32, I32, I32, I32, I32, P, P, P, P, P,
+        lib.orc_window_step.argtypes = [I64, I32, I32, I32, I32, I32, I32, I32, P, P, P, P, P,
                                         P, P, P, P, P, P, P, P, P, P, P, P, I32]
         lib.orc_window_commit.argtypes = [I64, I32, I32, I32, I32, P, P, P, P, P, P, P, P]
         lib.orc_window_load.argtypes = [I64, I32, I32, I32, I32, P, P, P, P, P, P, P, P, P]
@@ -142,14 +142,16 @@ class EagerOracle(_Base):
 
 class DeferredOracle(_Base):
     """Base + bounded log, DeltaLog Algorithm 1 with merge interval M
-    (plain=True: update pair (k, v), as EagerOracle)."""
+    (plain=True: update pair (k, v), as EagerOracle; k16=True: key-side
+    factors stored as bfloat16, DeltaLog §3.4)."""
 
-    def __init__(self, nstates, dk, dv, dl, M, nthreads=0, plain=False):
+    def __init__(self, nstates, dk, dv, dl, M, nthreads=0, plain=False, k16=False):
         super().__init__(nstates, dk, dv, dl, nthreads)
         if M < 1:
             raise ValueError("M >= 1")
         self.M = int(M)
         self.rule = 1 if plain else 0
+        self.k16 = 1 if k16 else 0
         Cap = max(self.M - 1, 0)
         self.base = np.zeros((self.n, dk, dv), dtype=np.float64)
         self.lbar = np.zeros((self.n, dl), dtype=np.float64)
@@ -170,7 +172,8 @@ class DeferredOracle(_Base):
         q, k, v, lam, beta = self._inputs(idx, q, k, v, lam, beta)
         y = np.zeros((idx.size, self.dv), dtype=np.float64)
         self._stride_guard()
-        _check(_load().orc_deferred_step(idx.size, self.rule, self.dk, self.dv, self.dl, self.M,
+        _check(_load().orc_deferred_step(idx.size, self.rule, self.k16, self.dk, self.dv, self.dl,
+                                         self.M,
                                          *self._arrays(), _p(idx), _p(q), _p(k), _p(v),
                                          _p(lam), _p(beta), _p(y), self.nthreads),
                "deferred step")
@@ -214,13 +217,15 @@ class WindowInt8Oracle(_Base):
     compensators=r: r Compensator Tokens (LeapQuant §3.3) fitted at every
     boundary; the residual is what is quantized."""
 
-    def __init__(self, nstates, dk, dv, dl, W, nthreads=0, col_scales=False, compensators=0):
+    def __init__(self, nstates, dk, dv, dl, W, nthreads=0, col_scales=False, compensators=0,
+                 k16=False):
         super().__init__(nstates, dk, dv, dl, nthreads)
         if W < 1:
             raise ValueError("W >= 1")
         self.W = int(W)
         self.mode = 1 if col_scales else 0
         self.r = int(compensators)
+        self.k16 = 1 if k16 else 0
         self.ck = np.zeros((self.n, max(self.r, 1), dk), dtype=np.float64)
         self.cu = np.zeros((self.n, max(self.r, 1), dv), dtype=np.float64)
         self.Z = np.zeros((self.n, dk, dv), dtype=np.int8)
@@ -236,7 +241,8 @@ class WindowInt8Oracle(_Base):
         idx = self._idx(idx)
         q, k, v, lam, beta = self._inputs(idx, q, k, v, lam, beta)
         y = np.zeros((idx.size, self.dv), dtype=np.float64)
-        _check(_load().orc_window_step(idx.size, self.mode, self.r, self.dk, self.dv, self.dl,
+        _check(_load().orc_window_step(idx.size, self.mode, self.r, self.k16, self.dk, self.dv,
+                                       self.dl,
                                        self.W, _p(self.Z), _p(self.s), _p(self.fc),
                                        _p(self.ck), _p(self.cu), _p(self.Sw),
                                        _p(self.rl),

@@ -171,6 +171,27 @@ int orc_eager_step(int64_t n, int rule, int dk, int dv, int dl, double *S,
     return err ? ORC_ERR_NOMEM : ORC_OK;
 }
 
+/*
+ * 16-bit key-side log factors ([DL] §3.4: "deferred key-side factors a_t
+ * use 16-bit storage" for GDN and KDA): k stored as bfloat16, the FP32 value
+ * rounded to its top 16 bits, round half to even on the discarded bits.
+ */
+static double bf16_round(float x)
+{
+    uint32_t b;
+    memcpy(&b, &x, 4);
+    const uint32_t lsb = (b >> 16) & 1u;
+    b = (b + 0x7fffu + lsb) & 0xffff0000u;
+    float y;
+    memcpy(&y, &b, 4);
+    return (double)y;
+}
+
+static double stored_key(int k16, float k)
+{
+    return k16 ? bf16_round(k) : (double)k;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Deferred materialization (base + bounded log)                             */
 /* ------------------------------------------------------------------------ */
@@ -226,8 +247,10 @@ static void deferred_represented(int dk, int dv, int dl, const double *base,
  *      L = C : S-bar <- D(lbar) S-bar + sum D(lbar - Lambda_i) K_i U_i^T
  *                       + a_t b_t^T, then lbar <- 0, L <- 0     (eq. 6)
  * work: 2*dk*dv doubles.  rule 1: b_t = v (no delta correction, as eager_one).
+ * k16: the appended key-side factor is bf16(k) ([DL] §3.4); the token's own
+ * output and a merge that folds it use k itself.
  */
-static void deferred_one(int rule, int dk, int dv, int dl, int M, double *base,
+static void deferred_one(int rule, int k16, int dk, int dv, int dl, int M, double *base,
                          double *lbar, double *K, double *U, double *Lam,
                          int32_t *Lp, const float *q, const float *k,
                          const float *v, const float *lam, float beta,
@@ -264,7 +287,7 @@ static void deferred_one(int rule, int dk, int dv, int dl, int M, double *base,
             y[j] += St[(size_t)i * dv + j] * (double)q[i];
     /* 4. append or merge */
     if (L < C) {
-        for (int i = 0; i < dk; ++i) K[(size_t)L * dk + i] = (double)k[i];
+        for (int i = 0; i < dk; ++i) K[(size_t)L * dk + i] = stored_key(k16, k[i]);
         for (int j = 0; j < dv; ++j) U[(size_t)L * dv + j] = u[j];
         for (int c = 0; c < dl; ++c) Lam[(size_t)L * dl + c] = lnew[c];
         for (int c = 0; c < dl; ++c) lbar[c] = lnew[c];
@@ -281,7 +304,7 @@ static int deferred_args_ok(int dk, int dv, int dl, int M)
     return valid_dims(dk, dv, dl) && M >= 1 && dk <= 1024 && dv <= 1024;
 }
 
-int orc_deferred_step(int64_t n, int rule, int dk, int dv, int dl, int M,
+int orc_deferred_step(int64_t n, int rule, int k16, int dk, int dv, int dl, int M,
                       double *base, double *lbar, double *K, double *U,
                       double *Lam, int32_t *L, const int64_t *idx,
                       const float *q, const float *k, const float *v,
@@ -304,7 +327,7 @@ int orc_deferred_step(int64_t n, int rule, int dk, int dv, int dl, int M,
 #pragma omp for schedule(dynamic, 2)
             for (int64_t row = 0; row < n; ++row) {
                 const int64_t s = idx[row];
-                deferred_one(rule, dk, dv, dl, M, base + (size_t)s * dk * dv,
+                deferred_one(rule, k16, dk, dv, dl, M, base + (size_t)s * dk * dv,
                              lbar + (size_t)s * dl, K + (size_t)s * C * dk,
                              U + (size_t)s * C * dv, Lam + (size_t)s * C * dl,
                              L + s, q + row * dk, k + row * dk, v + row * dv,
@@ -671,7 +694,7 @@ int orc_dequantize_cols(int64_t n, int dk, int dv, const int8_t *Z,
  *     with nc compensator pairs, the boundary of §3.3, see boundary()).
  *   ck   [nc*dk], cu [nc*dv] double: the window's compensator pairs.
  */
-static void window_one(int mode, int nc, int dk, int dv, int dl, int W,
+static void window_one(int mode, int nc, int k16, int dk, int dv, int dl, int W,
                        int8_t *Z, float *s, float *fc, double *ck, double *cu,
                        double *Sw, double *rl, double *rk, double *ru,
                        int32_t *cntp, const float *q, const float *k,
@@ -682,7 +705,14 @@ static void window_one(int mode, int nc, int dk, int dv, int dl, int W,
     double u[1024];
     eager_one(0, dk, dv, dl, Sw, q, k, v, lam, beta, y, r, u);
     for (int t = 0; t < dl; ++t) rl[(size_t)c * dl + t] = (double)lam[t];
-    for (int i = 0; i < dk; ++i) rk[(size_t)c * dk + i] = (double)k[i];
+    for (int i = 0; i < dk; ++i) rk[(size_t)c * dk + i] = stored_key(k16, k[i]);
+    /* k16: from here on the state holds the stored key-side factor, as a
+     * read of the record does (y above used k itself) */
+    if (k16)
+        for (int i = 0; i < dk; ++i) {
+            const double dlt = rk[(size_t)c * dk + i] - (double)k[i];
+            for (int j = 0; j < dv; ++j) Sw[(size_t)i * dv + j] += dlt * u[j];
+        }
     for (int j = 0; j < dv; ++j) ru[(size_t)c * dv + j] = u[j];
     if (c + 1 == W) {
         boundary(mode, nc, dk, dv, Sw, Z, s, fc, ck, cu, 1);
@@ -701,7 +731,7 @@ static int window_args_ok(int mode, int r, int dk, int dv, int dl, int W)
 /* fc: the column factors ([n_states][dv]); may be NULL in mode 0.  ck, cu:
  * [n_states][nc][dk], [n_states][nc][dv] (nc compensator pairs); may be NULL
  * when nc = 0. */
-int orc_window_step(int64_t n, int mode, int nc, int dk, int dv, int dl, int W,
+int orc_window_step(int64_t n, int mode, int nc, int k16, int dk, int dv, int dl, int W,
                     int8_t *Z, float *s, float *fc, double *ck, double *cu,
                     double *Sw, double *rl, double *rk, double *ru,
                     int32_t *cnt, const int64_t *idx, const float *q,
@@ -724,7 +754,7 @@ int orc_window_step(int64_t n, int mode, int nc, int dk, int dv, int dl, int W,
 #pragma omp for schedule(dynamic, 4)
             for (int64_t row = 0; row < n; ++row) {
                 const int64_t h = idx[row];
-                window_one(mode, nc, dk, dv, dl, W, Z + (size_t)h * dk * dv,
+                window_one(mode, nc, k16, dk, dv, dl, W, Z + (size_t)h * dk * dv,
                            s + (size_t)h * dk, mode ? fc + (size_t)h * dv : NULL,
                            nc ? ck + (size_t)h * nc * dk : NULL,
                            nc ? cu + (size_t)h * nc * dv : NULL,
