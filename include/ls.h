@@ -123,6 +123,17 @@ typedef enum {
  * per-key gate).  beta is passed as usual but its values are not used.
  */
 #define LS_PLAIN_UPDATE (1u << 12)
+
+/*
+ * ls_pool_desc.flags: LS_LOG_BF16_K (LS_DEFERRED_FP32 / LS_WINDOW_INT8,
+ * without compensator pairs): the key-side factors of the log are stored
+ * as bfloat16 (round to nearest even), the value-side factors and decay
+ * snapshots stay FP32 ("DeltaLog: Deferred Materialization of Recurrent
+ * States for Linear Attention Decoding", §3.4).  Reads of later tokens use
+ * the stored factor; the token's own output, and a merge that folds it,
+ * use k.  A log entry shrinks by 2 d_k bytes.
+ */
+#define LS_LOG_BF16_K (1u << 13)
 #define LS_INT8_COMPENSATORS(r) ((uint32_t)(r) << 8)
 
 typedef struct {
@@ -136,7 +147,7 @@ typedef struct {
                           (may be 0) for LS_EAGER_FP32                          */
     uint32_t flags;    /* 0; for LS_WINDOW_INT8 also LS_INT8_COLUMN_SCALES and
                           LS_INT8_COMPENSATORS(r); for the FP32 variants also
-                          LS_PLAIN_UPDATE                                      */
+                          LS_PLAIN_UPDATE; LS_LOG_BF16_K for the log variants */
 } ls_pool_desc;
 
 /* Human-readable name of a status code.  Never NULL. */

@@ -32,6 +32,7 @@ LS_MAX_WINDOW = 256
 LS_INT8_COLUMN_SCALES = 1
 LS_MAX_COMPENSATORS = 8
 LS_PLAIN_UPDATE = 1 << 12
+LS_LOG_BF16_K = 1 << 13
 
 
 def LS_INT8_COMPENSATORS(r: int) -> int:

@@ -19,6 +19,7 @@ written; the roofline fraction divides them by a measured kernel time.
   smoothed per-value-column format (§3.4 eq. 7, App. B.3) adds one FP32
   scale per value column to that base; r Compensator Tokens (§3.3) add r
   log entries read by every token and written once per window.
+* bfloat16 key-side log factors (DeltaLog §3.4): p_K = 2 in C_entry.
 """
 from __future__ import annotations
 
@@ -56,14 +57,15 @@ def log_cycle_bytes(base: float, gate: str, M: int, d_k: int = 128, d_v: int = 1
     return base * (1 + 1 / M) + c_log + 2 * 4 * _dl(gate, d_k) + io_bytes(gate, d_k, d_v)
 
 
-def deferred_bytes(gate: str, M: int, d_k: int = 128, d_v: int = 128) -> float:
-    return log_cycle_bytes(state_bytes_fp32(d_k, d_v), gate, M, d_k, d_v)
+def deferred_bytes(gate: str, M: int, d_k: int = 128, d_v: int = 128, p_k: int = 4) -> float:
+    return log_cycle_bytes(state_bytes_fp32(d_k, d_v), gate, M, d_k, d_v, p_k)
 
 
 def int8_bytes(gate: str, W: int, d_k: int = 128, d_v: int = 128, col_scales: bool = False,
-               compensators: int = 0) -> float:
+               compensators: int = 0, p_k: int = 4) -> float:
     comp = compensators * entry_bytes(gate, d_k, d_v) * (1 + 1 / W)
-    return log_cycle_bytes(state_bytes_int8(d_k, d_v, col_scales), gate, W, d_k, d_v) + comp
+    return log_cycle_bytes(state_bytes_int8(d_k, d_v, col_scales), gate, W, d_k, d_v,
+                           p_k) + comp
 
 
 def variant_bytes(variant: str, gate: str, window: int = 1) -> float:

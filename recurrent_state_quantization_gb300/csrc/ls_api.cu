@@ -37,7 +37,9 @@ int make_layout(const ls_pool_desc* d, Layout* L) {
     if (d == nullptr || L == nullptr) return LS_ERR_INVALID;
     if (d->variant < LS_EAGER_FP32 || d->variant > LS_WINDOW_INT8) return LS_ERR_INVALID;
     const uint32_t int8_flags = LS_INT8_COLUMN_SCALES | LS_INT8_COMPENSATORS(15);
-    if ((d->flags & ~(int8_flags | LS_PLAIN_UPDATE)) != 0) return LS_ERR_INVALID;
+    if ((d->flags & ~(int8_flags | LS_PLAIN_UPDATE | LS_LOG_BF16_K)) != 0) return LS_ERR_INVALID;
+    if ((d->flags & LS_LOG_BF16_K) && (!is_log_variant(d->variant) || ((d->flags >> 8) & 15u) != 0))
+        return LS_ERR_INVALID;
     const uint32_t ncomp = (d->flags >> 8) & 15u;
     if ((d->flags & int8_flags) && d->variant != LS_WINDOW_INT8) return LS_ERR_INVALID;
     if ((d->flags & LS_PLAIN_UPDATE) && d->variant == LS_WINDOW_INT8) return LS_ERR_INVALID;
@@ -67,7 +69,7 @@ int make_layout(const ls_pool_desc* d, Layout* L) {
     L->len = off;
     off = align_up(off + (log ? nh * 4 : 0));
     L->klog = off;
-    off = align_up(off + nh * W * kD * 4);
+    off = align_up(off + nh * W * kD * ((d->flags & LS_LOG_BF16_K) ? 2 : 4));
     L->ulog = off;
     off = align_up(off + nh * W * kD * 4);
     L->lamlog = off;
@@ -95,6 +97,7 @@ ls::PoolView make_view(const ls_pool_desc& d, const Layout& L, unsigned char* m)
     v.W = log ? d.window : 0;
     v.R = log ? static_cast<int32_t>((d.flags >> 8) & 15u) : 0;
     v.plain = (d.flags & LS_PLAIN_UPDATE) ? 1 : 0;
+    v.k16 = (d.flags & LS_LOG_BF16_K) ? 1 : 0;
     v.cap = v.W + v.R;
     v.dl = d.gate == LS_GATE_PER_KEY ? kD : 1;
     v.lam_stride = d.gate == LS_GATE_PER_KEY ? v.cap * kD : (v.cap + 3) / 4 * 4;

@@ -5,6 +5,7 @@
 
 #include <cstdint>
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "ls_internal.cuh"
@@ -167,6 +168,18 @@ __device__ __forceinline__ void row_quant_params(float amax, float& s, float& f)
 __device__ __forceinline__ void pdl_enter() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Four bfloat16 (two words, low half first) widened to FP32, exactly.
+__device__ __forceinline__ float4 bf16x4_to_float4(uint2 w) {
+    return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                       __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+}
+
+// FP32 -> bfloat16, round to nearest even, four at a time.
+__device__ __forceinline__ uint2 float4_to_bf16x4(float4 v) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    return make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
 }
 
 __device__ __forceinline__ void flag_status(int32_t* status, int32_t bit) {

@@ -113,9 +113,10 @@ __device__ __forceinline__ void issue_item(WarpSmem& ws, const StepArgs& a, int 
         const int n = min(P::EPC, L - e0);
         const size_t eo = (hd * static_cast<size_t>(pv.cap) + e0) * kD;
         const uint32_t part = static_cast<uint32_t>(n) * kVecBytes;
+        const uint32_t kpart = pv.k16 ? part / 2 : part;  // bfloat16 keys: half the bytes
         const size_t lb0 = hd * static_cast<size_t>(pv.lam_stride);
-        mbar_arrive_expect_tx(bar, PER_KEY ? 3 * part : 2 * part + 16);
-        bulk_g2s(dst, pv.klog + eo, part, bar);
+        mbar_arrive_expect_tx(bar, kpart + (PER_KEY ? 2 * part : part + 16));
+        bulk_g2s(dst, reinterpret_cast<const unsigned char*>(pv.klog) + eo * (pv.k16 ? 2 : 4), kpart, bar);
         bulk_g2s(dst + P::EPC * kVecBytes, pv.ulog + eo, part, bar);
         if constexpr (PER_KEY)
             bulk_g2s(dst + 2 * P::EPC * kVecBytes, pv.lamlog + lb0 + static_cast<size_t>(e0) * kD,
@@ -327,7 +328,8 @@ __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, 
             const int e0 = (it - 1 - P::NT) * P::EPC;
             const int n = min(P::EPC, L - e0);
             for (int e = 0; e < n; ++e) {
-                const float4 K4 = st4p[e * 32 + lane];
+                const float4 K4 = pv.k16 ? bf16x4_to_float4(reinterpret_cast<const uint2*>(st)[e * 32 + lane])
+                                         : st4p[e * 32 + lane];
                 const float4 U4 = st4p[(P::EPC + e) * 32 + lane];
                 float ck, cq;
                 if constexpr (PER_KEY) {
@@ -361,7 +363,10 @@ __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, 
     // ---- append entry L -------------------------------------------------------
     {
         const size_t eo = (hd * static_cast<size_t>(W) + L) * kD;
-        st4(pv.klog + eo + 4 * lane, k4);
+        if (pv.k16)
+            reinterpret_cast<uint2*>(pv.klog)[(eo >> 2) + lane] = float4_to_bf16x4(k4);
+        else
+            st4(pv.klog + eo + 4 * lane, k4);
         st4(pv.ulog + eo + 4 * lane, u4);
         const size_t lb0 = hd * static_cast<size_t>(pv.lam_stride);
         if constexpr (PER_KEY) st4(pv.lamlog + lb0 + static_cast<size_t>(L) * kD + 4 * lane, lp4);

@@ -455,9 +455,10 @@ __device__ __forceinline__ void fold_issue_log(const PoolView& pv, size_t hd, in
     const uint32_t part = static_cast<uint32_t>(nl) * kVecBytes;
     const size_t lb0 = hd * static_cast<size_t>(pv.lam_stride);
     const uint32_t lam_bytes = PER_KEY ? part : static_cast<uint32_t>((nl + 3) / 4 * 16);
+    const uint32_t kpart = pv.k16 ? part / 2 : part;  // bfloat16 keys: half the bytes
     fence_proxy_async();
-    mbar_arrive_expect_tx(fs.lbar, 2 * part + lam_bytes);
-    bulk_g2s(fs.rk, pv.klog + eo, part, fs.lbar);
+    mbar_arrive_expect_tx(fs.lbar, kpart + part + lam_bytes);
+    bulk_g2s(fs.rk, reinterpret_cast<const unsigned char*>(pv.klog) + eo * (pv.k16 ? 2 : 4), kpart, fs.lbar);
     bulk_g2s(fs.ru, pv.ulog + eo, part, fs.lbar);
     if constexpr (PER_KEY)
         bulk_g2s(fs.rl, pv.lamlog + lb0 + static_cast<size_t>(c0) * kD, part, fs.lbar);
@@ -596,7 +597,13 @@ __device__ bool fold_cta(const PoolView& pv, size_t hd, int n, const float* lbg,
             // (a, a) pairs, consecutive lanes consecutive addresses
             for (int idx = tid; idx < nl * (kD / 2); idx += kThreads) {
                 const int l = idx >> 6, p = idx & 63;
-                const float2 K2 = reinterpret_cast<const float2*>(fs.rk)[idx];
+                float2 K2;
+                if (pv.k16) {
+                    const uint32_t w = reinterpret_cast<const uint32_t*>(fs.rk)[idx];
+                    K2 = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+                } else {
+                    K2 = reinterpret_cast<const float2*>(fs.rk)[idx];
+                }
                 float2 g;
                 if constexpr (PER_KEY) {
                     const float2 lm = reinterpret_cast<const float2*>(fs.rl)[idx];
@@ -624,7 +631,8 @@ __device__ bool fold_cta(const PoolView& pv, size_t hd, int n, const float* lbg,
             for (int idx = tid; idx < nl * (kD / 4); idx += kThreads) {
                 const int l = idx >> 5, q = idx & 31;  // entry, 4-row / 4-column group
                 const size_t eo = (kb + c0 + l) * kD + 4 * q;
-                const float4 K4 = ldcg4(pv.klog + eo);
+                const float4 K4 = pv.k16 ? bf16x4_to_float4(__ldcg(reinterpret_cast<const uint2*>(pv.klog) + (eo >> 2)))
+                                         : ldcg4(pv.klog + eo);
                 fs.u4[l * (kD / 4) + q] = ldcg4(pv.ulog + eo);
                 float4 g;
                 if constexpr (PER_KEY) {

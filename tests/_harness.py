@@ -15,14 +15,14 @@ D = 128
 
 
 def make_oracle(variant, nstates, dl, window, nthreads=0, col_scales=False, compensators=0,
-                plain=False):
+                plain=False, k16=False):
     if variant == "eager":
         return oracle.EagerOracle(nstates, D, D, dl, nthreads, plain=plain)
     if variant == "deferred":
-        return oracle.DeferredOracle(nstates, D, D, dl, window, nthreads, plain=plain)
+        return oracle.DeferredOracle(nstates, D, D, dl, window, nthreads, plain=plain, k16=k16)
     if variant == "int8":
         return oracle.WindowInt8Oracle(nstates, D, D, dl, window, nthreads, col_scales=col_scales,
-                                       compensators=compensators)
+                                       compensators=compensators, k16=k16)
     raise ValueError(variant)
 
 
@@ -70,15 +70,17 @@ class Pair:
     """A GPU pool and an oracle stepped together over a workload."""
 
     def __init__(self, w: wl.Workload, variant: str, window: int, n_sample=None, device="cuda",
-                 seed=0, nthreads=0, col_scales=False, compensators=0, plain=False):
+                 seed=0, nthreads=0, col_scales=False, compensators=0, plain=False, k16=False):
         self.w, self.variant, self.window = w, variant, window
         self.col_scales = bool(col_scales)
         self.compensators = int(compensators)
         self.dev = torch.device(device)
         self.pool = StatePool(w.num_slots, w.heads, variant, w.gate, window, device=self.dev,
-                              col_scales=col_scales, compensators=compensators, plain=plain)
+                              col_scales=col_scales, compensators=compensators, plain=plain,
+                              k16=k16)
         self.orc = make_oracle(variant, w.num_slots * w.heads, w.dl, window, nthreads,
-                               col_scales=col_scales, compensators=compensators, plain=plain)
+                               col_scales=col_scales, compensators=compensators, plain=plain,
+                               k16=k16)
         self.slot_idx = wl.slot_index(w, self.dev)
         self.sample = sample_rows(w, self.slot_idx, n_sample, seed)
         self.masks = wl.static_masks(w, self.dev)

@@ -107,6 +107,22 @@ def test_plain_update_flag(lib):
     assert rc == N.LS_ERR_INVALID
 
 
+def test_bf16_key_flag(lib):
+    """LS_LOG_BF16_K: log variants without compensator pairs; the key-side
+    factors take 2 bytes instead of 4."""
+    from recurrent_state_quantization_gb300 import _native as N
+    P, Hh, W = 4, 2, 16
+    nh = P * Hh
+    al = lambda x: (x + 255) // 256 * 256
+    for variant in (N.LS_DEFERRED_FP32, N.LS_WINDOW_INT8):
+        rc0, b0 = _bytes(lib, _desc(variant=variant))
+        rc1, b1 = _bytes(lib, _desc(variant=variant, flags=N.LS_LOG_BF16_K))
+        assert rc0 == rc1 == 0
+        assert b0 - b1 == al(nh * W * 128 * 4) - al(nh * W * 128 * 2)
+    assert _bytes(lib, _desc(variant=N.LS_EAGER_FP32, flags=N.LS_LOG_BF16_K))[0] == N.LS_ERR_INVALID
+    assert _bytes(lib, _desc(flags=N.LS_LOG_BF16_K | N.LS_INT8_COMPENSATORS(2)))[0] == N.LS_ERR_INVALID
+
+
 def test_compensator_flag(lib):
     """LS_INT8_COMPENSATORS(r): INT8 only, r <= 8; the log holds W + r entries
     (K, U, and the scalar-gate snapshots padded to 4)."""

@@ -245,6 +245,41 @@ def test_gdn_serving_b256_h48_4pools(variant, window, cols):
                        prewarm=_prewarm_factory(w.prewarm_tokens)), variant)
 
 
+@pytest.mark.parametrize("gate", ["scalar", "per_key"])
+@pytest.mark.parametrize("variant,window,cols", [("deferred", 1, False), ("deferred", 5, False),
+                                                 ("deferred", 16, False), ("int8", 1, False),
+                                                 ("int8", 5, False), ("int8", 16, True)])
+def test_small_ragged_bf16_keys(gate, variant, window, cols):
+    """bfloat16 key-side log factors (DeltaLog §3.4) against the oracle's."""
+    from recurrent_state_quantization_gb300 import workloads as wl
+    H = _harness()
+    w = wl.custom("ragged-k16", gate=gate, batch=5, heads=3, tokens=37, num_slots=7,
+                  windows=(window,), merge_interval=window, permute_slots=True,
+                  seed=51 + window, lam_scale=0.3)
+    p = H.Pair(w, variant, window, col_scales=cols, k16=True)
+    run_lockstep(p, w.tokens)
+    if variant == "int8":
+        check_int8(p)
+    else:
+        check_fp32(p)
+    assert p.pool.status() == 0
+
+
+@pytest.mark.parametrize("variant,window", [("deferred", 16), ("int8", 16)])
+def test_gdn_serving_b256_h48_bf16_keys(variant, window):
+    from recurrent_state_quantization_gb300 import workloads as wl
+    H = _harness()
+    w = wl.WORKLOADS[3]
+    p = H.Pair(w, variant, window, n_sample=6, k16=True)
+    _prewarm_factory(w.prewarm_tokens)(p, 0)
+    run_lockstep(p, 64)
+    if variant == "int8":
+        check_int8(p)
+    else:
+        check_fp32(p)
+    assert p.pool.status() == 0
+
+
 @pytest.mark.parametrize("variant,window", [("eager", 0), ("deferred", 16)])
 def test_rwkv6_b128_h32_t512(variant, window):
     """RWKV6 (per-key decay, raw (k, v) updates) on the KDA 128x32 shapes."""
