@@ -313,6 +313,7 @@ def run_native(args, rank, world, local):
                                                 peak_kind, pools["eager"])
         out["e2e"] = e2e(w, variants, pools, slot_idx, dev, world)
         out["rwkv6"] = rwkv6(dev, hbm_peak, peak_kind)
+        out["split_replay_ablation"] = split_ablation(dev)
         if rank == 0:
             out["cpu_baseline"] = cpu_baseline(w, variants, budget_s=6.0)
     return out
@@ -365,6 +366,53 @@ def window_sweep(w, slot_idx, masks, inputs, ring, dev, peak, peak_kind, eager_p
                     "tokens": tokens, "head_steps_per_s": hs / (ms * 1e-3),
                     "achieved_gbs": gbs, "frac_of_" + peak_kind + "_hbm": gbs / peak})
         del pools
+        torch.cuda.empty_cache()
+    return res
+
+
+def split_ablation(dev, batch=256, heads=48, cycles=8, reps=3):
+    """Split-vs-fused replay (DeltaLog §5.3, Fig. 9): amortized time per token
+    over whole merge cycles of GDN, KDA and RWKV6 at M = 4 and 8 (deferred
+    FP32) and of GDN at W = 16 (INT8), one batch x heads pool per path, the
+    two entry points timed alternately (median of `reps`)."""
+    import statistics as st
+    import torch
+    from recurrent_state_quantization_gb300 import StatePool
+    from recurrent_state_quantization_gb300 import workloads as wl
+    ops = (("gdn", "scalar", False), ("kda", "per_key", False), ("rwkv6", "per_key", True))
+    cases = [(n, g, p, "deferred", M) for n, g, p in ops for M in (4, 8)]
+    cases.append(("gdn", "scalar", False, "int8", 16))
+    stream = torch.cuda.current_stream()
+    slots = torch.arange(batch, dtype=torch.int32, device=dev)
+    res = []
+    for name, gate, plain, variant, M in cases:
+        w = wl.custom(f"{name}_b{batch}_h{heads}", gate=gate, batch=batch, heads=heads,
+                      tokens=cycles * M, seed=11, lam_scale=0.05)
+        ins = [wl.step_inputs(w, t, device=dev) for t in range(16)]
+        y = torch.empty(batch, heads, w.d_v, device=dev)
+        pools = {path: StatePool(batch, heads, variant, gate, M, device=dev, plain=plain)
+                 for path in ("fused", "split")}
+        call = {"fused": lambda t: pools["fused"].decode_step(slots, *ins[t % 16], y=y),
+                "split": lambda t: pools["split"].decode_step_split(slots, *ins[t % 16], y=y)}
+        for path in call:  # one cycle of warm-up (allocates the split scratch)
+            for t in range(M):
+                call[path](t)
+        times = {"fused": [], "split": []}
+        for _ in range(reps):
+            for path in ("fused", "split"):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize()
+                a.record(stream)
+                for t in range(cycles * M):
+                    call[path](t)
+                b.record(stream)
+                torch.cuda.synchronize()
+                times[path].append(a.elapsed_time(b) * 1e3 / (cycles * M))
+        f, s = st.median(times["fused"]), st.median(times["split"])
+        res.append({"operator": name, "variant": variant, "M": M, "batch": batch, "heads": heads,
+                    "fused_us_per_token": f, "split_us_per_token": s,
+                    "speedup_split_over_fused": f / s})
+        del pools, call
         torch.cuda.empty_cache()
     return res
 

@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define LS_ABI_VERSION 2
+#define LS_ABI_VERSION 3
 
 /* status codes */
 #define LS_OK 0
@@ -226,6 +226,36 @@ int ls_decode_step(ls_pool *pool, const int32_t *d_slot_idx, int32_t batch,
                    const float *q, const float *k, const float *v,
                    const float *log_decay, const float *beta, float *y,
                    void *stream);
+
+/*
+ * Split replay (DeltaLog §5.3, the split-replay ablation): the decode token
+ * of ls_decode_step for the deferred and INT8 variants as two kernels.  The
+ * first writes, per (request, head), the replay coefficients of every live
+ * log entry l,
+ *   c_k[l] = K_l . (exp(lp - Lam_l) . k),  c_q[l] = K_l . (exp(lp - Lam_l) . q)
+ * (lp the cumulative log-decay after this token), into the caller's device
+ * scratch d_scratch; the second streams the base and the U side of the log
+ * and applies those coefficients.  Same arguments, results and pool state as
+ * ls_decode_step, bit for bit.  d_scratch: >= ls_split_scratch_bytes bytes,
+ * 16-byte aligned, owned by the caller, contents on entry ignored; the call
+ * reads and writes it in stream order, so calls that share one scratch
+ * buffer must be ordered on one stream.  Errors: as ls_decode_step,
+ * LS_ERR_INVALID (eager pool, null scratch), LS_ERR_ALIGN, LS_ERR_SIZE
+ * (scratch smaller than required).
+ */
+int ls_decode_step_split(ls_pool *pool, const int32_t *d_slot_idx,
+                         int32_t batch, const float *q, const float *k,
+                         const float *v, const float *log_decay,
+                         const float *beta, float *y, void *d_scratch,
+                         size_t scratch_bytes, void *stream);
+
+/*
+ * Scratch bytes ls_decode_step_split needs for `batch` requests:
+ * batch * H * ceil(capacity / 6) * 6 * 8, the capacity being the window /
+ * merge interval plus the compensator pairs.  LS_ERR_INVALID for an eager
+ * pool.
+ */
+int ls_split_scratch_bytes(const ls_pool *pool, int32_t batch, size_t *bytes);
 
 /*
  * Device bytes of the staging buffer ls_decode_step_host needs for `batch`.

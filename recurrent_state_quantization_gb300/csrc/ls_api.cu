@@ -136,6 +136,39 @@ ls::AuxArgs aux_args(const ls_pool* p, const int32_t* d_slots, int32_t n) {
     return a;
 }
 
+// Validate one decode token's arguments and fill the kernel arguments
+// (batch = 0 passes with nothing filled).
+int step_args(ls_pool* pool, const int32_t* d_slot_idx, int32_t batch, const float* q,
+              const float* k, const float* v, const float* log_decay, const float* beta,
+              float* y, ls::StepArgs* a) {
+    if (pool == nullptr || batch < 0) return LS_ERR_INVALID;
+    if (batch == 0) return LS_OK;
+    if (!d_slot_idx || !q || !k || !v || !log_decay || !beta || !y) return LS_ERR_INVALID;
+    if (batch > pool->desc.num_slots) return LS_ERR_SLOT;
+    if (static_cast<int64_t>(batch) * pool->desc.num_heads > 0x7fffffffLL) return LS_ERR_SIZE;
+    const bool per_key = pool->desc.gate == LS_GATE_PER_KEY;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(y, 16) ||
+        !aligned(log_decay, per_key ? 16 : 4) || !aligned(beta, 4) || !aligned(d_slot_idx, 4))
+        return LS_ERR_ALIGN;
+    a->pv = pool->view;
+    a->slot_idx = d_slot_idx;
+    a->batch = batch;
+    a->q = q;
+    a->k = k;
+    a->v = v;
+    a->lam = log_decay;
+    a->beta = beta;
+    a->y = y;
+    return LS_OK;
+}
+
+// Split replay: coefficient entries per (request, head) row, the log
+// capacity rounded up to whole streamed chunks.
+int32_t split_stride(const ls_pool* p) {
+    const int32_t cap = p->view.cap;
+    return (cap + ls::kSplitEntries - 1) / ls::kSplitEntries * ls::kSplitEntries;
+}
+
 int launch_step(ls_pool* p, const ls::StepArgs& a, cudaStream_t s) {
     const ls_pool_desc& d = p->desc;
     const bool per_key = d.gate == LS_GATE_PER_KEY;
@@ -234,26 +267,35 @@ int ls_pool_reset_slots(ls_pool* pool, const int32_t* d_slots, int32_t n, void* 
 int ls_decode_step(ls_pool* pool, const int32_t* d_slot_idx, int32_t batch, const float* q,
                    const float* k, const float* v, const float* log_decay, const float* beta,
                    float* y, void* stream) {
-    if (pool == nullptr || batch < 0) return LS_ERR_INVALID;
-    if (batch == 0) return LS_OK;
-    if (!d_slot_idx || !q || !k || !v || !log_decay || !beta || !y) return LS_ERR_INVALID;
-    if (batch > pool->desc.num_slots) return LS_ERR_SLOT;
-    if (static_cast<int64_t>(batch) * pool->desc.num_heads > 0x7fffffffLL) return LS_ERR_SIZE;
-    const bool per_key = pool->desc.gate == LS_GATE_PER_KEY;
-    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(y, 16) ||
-        !aligned(log_decay, per_key ? 16 : 4) || !aligned(beta, 4) || !aligned(d_slot_idx, 4))
-        return LS_ERR_ALIGN;
     ls::StepArgs a{};
-    a.pv = pool->view;
-    a.slot_idx = d_slot_idx;
-    a.batch = batch;
-    a.q = q;
-    a.k = k;
-    a.v = v;
-    a.lam = log_decay;
-    a.beta = beta;
-    a.y = y;
+    const int rc = step_args(pool, d_slot_idx, batch, q, k, v, log_decay, beta, y, &a);
+    if (rc != LS_OK || batch == 0) return rc;
     return launch_step(pool, a, static_cast<cudaStream_t>(stream));
+}
+
+int ls_split_scratch_bytes(const ls_pool* pool, int32_t batch, size_t* bytes) {
+    if (pool == nullptr || bytes == nullptr || batch < 0) return LS_ERR_INVALID;
+    if (!is_log_variant(pool->desc.variant)) return LS_ERR_INVALID;
+    *bytes = static_cast<size_t>(batch) * pool->desc.num_heads * split_stride(pool) * sizeof(float2);
+    return LS_OK;
+}
+
+int ls_decode_step_split(ls_pool* pool, const int32_t* d_slot_idx, int32_t batch, const float* q,
+                         const float* k, const float* v, const float* log_decay, const float* beta,
+                         float* y, void* d_scratch, size_t scratch_bytes, void* stream) {
+    ls::StepArgs a{};
+    const int rc = step_args(pool, d_slot_idx, batch, q, k, v, log_decay, beta, y, &a);
+    if (rc != LS_OK || batch == 0) return rc;
+    if (!is_log_variant(pool->desc.variant) || d_scratch == nullptr) return LS_ERR_INVALID;
+    if (!aligned(d_scratch, 16)) return LS_ERR_ALIGN;
+    size_t need = 0;
+    ls_split_scratch_bytes(pool, batch, &need);
+    if (scratch_bytes < need) return LS_ERR_SIZE;
+    a.coef = static_cast<float2*>(d_scratch);
+    a.cstride = split_stride(pool);
+    return cuda_status(ls::launch_log_step_split(a, pool->desc.variant == LS_WINDOW_INT8,
+                                                 pool->desc.gate == LS_GATE_PER_KEY,
+                                                 static_cast<cudaStream_t>(stream)));
 }
 
 int ls_step_staging_bytes(const ls_pool* pool, int32_t batch, size_t* bytes) {

@@ -14,6 +14,7 @@ namespace ls {
 constexpr int kD = 128;         // d_k = d_v
 constexpr int kThreads = 256;   // threads of every CTA (8 warps)
 constexpr int kWarps = kThreads / 32;
+constexpr int kSplitEntries = 6;  // split replay: log entries per streamed chunk
 
 // Device status word bits (mirror LS_DEV_* of ls.h).
 constexpr int32_t kDevSlotRange = 1;
@@ -67,6 +68,8 @@ struct StepArgs {
     const float* lam;
     const float* beta;
     float* y;
+    float2* coef;     // split replay: [batch * H][cstride] (c_k, c_q) per log entry
+    int32_t cstride;  // entries per row, a multiple of kSplitEntries
 };
 
 struct AuxArgs {
@@ -120,6 +123,7 @@ cudaError_t prepare_aux_kernels();
 
 cudaError_t launch_eager_step(const StepArgs& a, bool per_key, cudaStream_t s);
 cudaError_t launch_log_step(const StepArgs& a, bool int8, bool per_key, cudaStream_t s);
+cudaError_t launch_log_step_split(const StepArgs& a, bool int8, bool per_key, cudaStream_t s);
 // deferred / INT8: fold the live log into the base (commit) or into a caller
 // buffer (read) for n slots.
 cudaError_t launch_fold(const AuxArgs& a, bool int8, bool per_key, bool commit, cudaStream_t s);

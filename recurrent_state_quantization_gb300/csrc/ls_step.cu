@@ -45,6 +45,17 @@ namespace {
 //   1 .. NT    base chunks of 4 KiB (32 INT8 rows / 8 FP32 rows)
 //   then       log chunks: K and U of EPC entries (+ their snapshots)
 // The warp is the single writer of its head's log metadata.
+//
+// Split replay (DeltaLog §5.3): a prepare kernel first writes, per (request,
+// head), the two replay coefficients of every live entry,
+//   c_k[l] = K_l . (exp(lp - Lam_l) . k),   c_q[l] = K_l . (exp(lp - Lam_l) . q),
+// into caller scratch [batch * H][cstride] (float2); the step's log chunks
+// then carry U and those coefficients only.  The prepare kernel uses the
+// fused replay's lane layout and reductions, so both orders produce the same
+// bits.  Here one warp owns all d_v columns of a head, so the fused replay
+// computes each dot product once (the pages' split removes dot products
+// duplicated across value tiles); what the split changes is where the key
+// side of the log is read and reduced.
 // ---------------------------------------------------------------------------
 constexpr int kRing = 3;
 constexpr int kChunk = 4096;
@@ -68,18 +79,21 @@ static_assert(kWarps * sizeof(WarpSmem) >= fold_smem_bytes(false) &&
 
 constexpr size_t step_smem_bytes() { return kWarps * sizeof(WarpSmem); }
 
-template <bool INT8, bool PER_KEY>
+template <bool INT8, bool PER_KEY, bool SPLIT = false>
 struct Plan {
-    static constexpr int NT = INT8 ? 4 : 16;           // base chunks
-    static constexpr int EPC = PER_KEY ? 2 : 4;        // log entries per chunk
-    static constexpr int ROWS = INT8 ? 32 : 8;         // key rows per base chunk
+    static constexpr int NT = INT8 ? 4 : 16;  // base chunks
+    // log entries per chunk: K, U (+ Lam for the per-key gate) each, or with
+    // split replay U and the two coefficients
+    static constexpr int EPC = SPLIT ? kSplitEntries : (PER_KEY ? 2 : 4);
+    static constexpr int ROWS = INT8 ? 32 : 8;  // key rows per base chunk
 };
+static_assert(kSplitEntries * (kVecBytes + 8) <= kStage, "a split log chunk fits a stage");
 
 // Issue item `it` of head hd into stage it % kRing (lane 0 only).
-template <bool INT8, bool PER_KEY>
+template <bool INT8, bool PER_KEY, bool SPLIT>
 __device__ __forceinline__ void issue_item(WarpSmem& ws, const StepArgs& a, int row, size_t hd,
                                            int L, int it) {
-    using P = Plan<INT8, PER_KEY>;
+    using P = Plan<INT8, PER_KEY, SPLIT>;
     const PoolView& pv = a.pv;
     unsigned char* dst = ws.ring[it % kRing];
     uint64_t* bar = &ws.bar[it % kRing];
@@ -108,6 +122,17 @@ __device__ __forceinline__ void issue_item(WarpSmem& ws, const StepArgs& a, int 
         bulk_g2s(dst, reinterpret_cast<const unsigned char*>(pv.base) + hd * tile_bytes(INT8) +
                           static_cast<size_t>(it - 1) * kChunk,
                  kChunk, bar);
+    } else if constexpr (SPLIT) {
+        // U of n entries, then the coefficients of all EPC entries (48 B; the
+        // row stride is a multiple of EPC, so e0 + EPC stays inside the row)
+        const int e0 = (it - 1 - P::NT) * P::EPC;
+        const int n = min(P::EPC, L - e0);
+        const size_t eo = (hd * static_cast<size_t>(pv.cap) + e0) * kD;
+        const uint32_t part = static_cast<uint32_t>(n) * kVecBytes;
+        mbar_arrive_expect_tx(bar, part + P::EPC * 8);
+        bulk_g2s(dst, pv.ulog + eo, part, bar);
+        bulk_g2s(dst + P::EPC * kVecBytes, a.coef + static_cast<size_t>(row) * a.cstride + e0,
+                 P::EPC * 8, bar);
     } else {
         const int e0 = (it - 1 - P::NT) * P::EPC;
         const int n = min(P::EPC, L - e0);
@@ -136,10 +161,10 @@ __device__ __forceinline__ void issue_item(WarpSmem& ws, const StepArgs& a, int 
 //     after the token.  The base and log the CTA re-reads were just streamed
 //     by the warp and are mostly still in L2, while the per-warp GEMV keeps
 //     the integer arithmetic of every other token.
-template <bool INT8, bool PER_KEY>
+template <bool INT8, bool PER_KEY, bool SPLIT>
 __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, int row,
                                                float* lp_out) {
-    using P = Plan<INT8, PER_KEY>;
+    using P = Plan<INT8, PER_KEY, SPLIT>;
     const int lane = threadIdx.x & 31;
     const PoolView& pv = a.pv;
     const int H = pv.H, W = pv.cap;  // W: log capacity (window + compensator pairs)
@@ -170,7 +195,7 @@ __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, 
         for (int s = 0; s < kRing; ++s) mbar_init(&ws.bar[s], 1);
         ws.bar_live = 1u;
         mbar_fence_init();
-        for (int it = 0; it < min(kRing, NI); ++it) issue_item<INT8, PER_KEY>(ws, a, row, hd, L, it);
+        for (int it = 0; it < min(kRing, NI); ++it) issue_item<INT8, PER_KEY, SPLIT>(ws, a, row, hd, L, it);
     }
     const float beta = __ldg(a.beta + row);
     float lp_scalar = 0.0f;
@@ -323,6 +348,19 @@ __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, 
                     }
                 }
             }
+        } else if constexpr (SPLIT) {
+            // replay with precomputed coefficients (c_k, c_q) per entry
+            const int e0 = (it - 1 - P::NT) * P::EPC;
+            const int n = min(P::EPC, L - e0);
+            const float2* cf = reinterpret_cast<const float2*>(st + P::EPC * kVecBytes);
+            for (int e = 0; e < n; ++e) {
+                const float4 U4 = st4p[e * 32 + lane];
+                const float2 c = cf[e];
+                r01 = make_float2(fmaf(c.x, U4.x, r01.x), fmaf(c.x, U4.y, r01.y));
+                r23 = make_float2(fmaf(c.x, U4.z, r23.x), fmaf(c.x, U4.w, r23.y));
+                y01 = make_float2(fmaf(c.y, U4.x, y01.x), fmaf(c.y, U4.y, y01.y));
+                y23 = make_float2(fmaf(c.y, U4.z, y23.x), fmaf(c.y, U4.w, y23.y));
+            }
         } else {
             // replay of this chunk's log entries (LeapQuant eq. 9)
             const int e0 = (it - 1 - P::NT) * P::EPC;
@@ -350,7 +388,7 @@ __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, 
             }
         }
         __syncwarp();  // every lane is done with the stage
-        if (lane == 0 && it + kRing < NI) issue_item<INT8, PER_KEY>(ws, a, row, hd, L, it + kRing);
+        if (lane == 0 && it + kRing < NI) issue_item<INT8, PER_KEY, SPLIT>(ws, a, row, hd, L, it + kRing);
     }
 
     // ---- delta correction and output -----------------------------------------
@@ -382,7 +420,7 @@ __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, 
     return static_cast<long long>(hd);  // INT8 window end: the CTA folds the W entries
 }
 
-template <bool INT8, bool PER_KEY, bool COMP>
+template <bool INT8, bool PER_KEY, bool COMP, bool SPLIT = false>
 __global__ void __launch_bounds__(kThreads, 2) log_step_kernel(const StepArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ long long fold_hd[kWarps];
@@ -396,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 2) log_step_kernel(const StepArgs a)
     WarpSmem& ws = reinterpret_cast<WarpSmem*>(smem)[warp];
     if (lane == 0) ws.bar_live = 0u;
     __syncwarp();
-    if (row < a.batch * pv.H) hd = warp_step<INT8, PER_KEY>(a, ws, row, &lp);
+    if (row < a.batch * pv.H) hd = warp_step<INT8, PER_KEY, SPLIT>(a, ws, row, &lp);
     if (lane == 0) {
         fold_hd[warp] = hd;
         fold_lb[warp] = lp;
@@ -449,6 +487,64 @@ __global__ void __launch_bounds__(kThreads, 2) log_step_kernel(const StepArgs a)
     }
 }
 
+// Split replay, first kernel: the replay coefficients of every live log entry
+// of each (request, head) into a.coef[row * a.cstride + l] (DeltaLog §5.3).
+// One warp per head with the fused step's lane layout (lane l holds keys
+// 4l..4l+3) and reductions.  Heads with nothing to replay, heads the step
+// will flag, and FP32 heads whose merge interval closes on this token (the
+// CTA decodes those in one pass over the state) write nothing.
+template <bool INT8, bool PER_KEY>
+__global__ void __launch_bounds__(kThreads) replay_prepare_kernel(const StepArgs a) {
+    pdl_enter();
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const PoolView& pv = a.pv;
+    if (row >= a.batch * pv.H) return;
+    const int H = pv.H;
+    const int b = row / H, h = row - b * H;
+    const int slot = __ldg(a.slot_idx + b);
+    if (slot < 0 || slot >= pv.P) return;
+    const size_t hd = static_cast<size_t>(slot) * H + h;
+    const int L = pv.len[hd];
+    if (L <= 0 || L >= pv.cap) return;
+    if (!INT8 && L + 1 == pv.W) return;
+    const size_t ro = static_cast<size_t>(row) * kD + 4 * lane;
+    const float4 k4 = __ldg(reinterpret_cast<const float4*>(a.k + ro));
+    const float4 q4 = __ldg(reinterpret_cast<const float4*>(a.q + ro));
+    float4 lp4;
+    if constexpr (PER_KEY) {
+        const float4 lam4 = __ldg(reinterpret_cast<const float4*>(a.lam + ro));
+        const float4 lb4 = *reinterpret_cast<const float4*>(pv.lbar + hd * kD + 4 * lane);
+        lp4 = make_float4(lb4.x + lam4.x, lb4.y + lam4.y, lb4.z + lam4.z, lb4.w + lam4.w);
+    } else {
+        const float lps = pv.lbar[hd] + __ldg(a.lam + row);
+        lp4 = make_float4(lps, lps, lps, lps);
+    }
+    const size_t lb0 = hd * static_cast<size_t>(pv.lam_stride);
+    const size_t e0 = hd * static_cast<size_t>(pv.cap) * kD;
+    float2* out = a.coef + static_cast<size_t>(row) * a.cstride;
+#pragma unroll 2
+    for (int e = 0; e < L; ++e) {
+        const size_t eo = e0 + static_cast<size_t>(e) * kD;
+        const float4 K4 = pv.k16 ? bf16x4_to_float4(reinterpret_cast<const uint2*>(pv.klog)[(eo >> 2) + lane])
+                                 : *reinterpret_cast<const float4*>(pv.klog + eo + 4 * lane);
+        float ck, cq;
+        if constexpr (PER_KEY) {
+            const float4 Lm = *reinterpret_cast<const float4*>(pv.lamlog + lb0 + static_cast<size_t>(e) * kD +
+                                                                4 * lane);
+            const float ax = K4.x * expf(lp4.x - Lm.x), ay = K4.y * expf(lp4.y - Lm.y);
+            const float az = K4.z * expf(lp4.z - Lm.z), aw = K4.w * expf(lp4.w - Lm.w);
+            ck = warp_sum(fmaf(ax, k4.x, fmaf(ay, k4.y, fmaf(az, k4.z, aw * k4.w))));
+            cq = warp_sum(fmaf(ax, q4.x, fmaf(ay, q4.y, fmaf(az, q4.z, aw * q4.w))));
+        } else {
+            const float g = expf(lp4.x - pv.lamlog[lb0 + e]);
+            ck = warp_sum(fmaf(K4.x, k4.x, fmaf(K4.y, k4.y, fmaf(K4.z, k4.z, K4.w * k4.w)))) * g;
+            cq = warp_sum(fmaf(K4.x, q4.x, fmaf(K4.y, q4.y, fmaf(K4.z, q4.z, K4.w * q4.w)))) * g;
+        }
+        if (lane == 0) out[e] = make_float2(ck, cq);
+    }
+}
+
 template <typename K>
 cudaError_t set_smem(K kernel, size_t bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -465,7 +561,13 @@ cudaError_t prepare_log_step_kernels() {
     if ((e = set_smem(log_step_kernel<true, false, false>, ls)) != cudaSuccess) return e;
     if ((e = set_smem(log_step_kernel<true, true, false>, ls)) != cudaSuccess) return e;
     if ((e = set_smem(log_step_kernel<true, false, true>, ls)) != cudaSuccess) return e;
-    return set_smem(log_step_kernel<true, true, true>, ls);
+    if ((e = set_smem(log_step_kernel<true, true, true>, ls)) != cudaSuccess) return e;
+    if ((e = set_smem(log_step_kernel<false, false, false, true>, ls)) != cudaSuccess) return e;
+    if ((e = set_smem(log_step_kernel<false, true, false, true>, ls)) != cudaSuccess) return e;
+    if ((e = set_smem(log_step_kernel<true, false, false, true>, ls)) != cudaSuccess) return e;
+    if ((e = set_smem(log_step_kernel<true, true, false, true>, ls)) != cudaSuccess) return e;
+    if ((e = set_smem(log_step_kernel<true, false, true, true>, ls)) != cudaSuccess) return e;
+    return set_smem(log_step_kernel<true, true, true, true>, ls);
 }
 
 cudaError_t launch_log_step(const StepArgs& a, bool int8, bool per_key, cudaStream_t s) {
@@ -479,6 +581,31 @@ cudaError_t launch_log_step(const StepArgs& a, bool int8, bool per_key, cudaStre
         return launch_dependent(per_key ? log_step_kernel<true, true, false> : log_step_kernel<true, false, false>,
                                 grid, sm, s, a);
     return launch_dependent(per_key ? log_step_kernel<false, true, false> : log_step_kernel<false, false, false>,
+                            grid, sm, s, a);
+}
+
+cudaError_t launch_log_step_split(const StepArgs& a, bool int8, bool per_key, cudaStream_t s) {
+    const int64_t rows = static_cast<int64_t>(a.batch) * a.pv.H;
+    const dim3 grid(static_cast<unsigned>((rows + kWarps - 1) / kWarps));
+    const size_t sm = step_smem_bytes();
+    cudaError_t e;
+    if (int8)
+        e = launch_dependent(per_key ? replay_prepare_kernel<true, true> : replay_prepare_kernel<true, false>,
+                             grid, 0, s, a);
+    else
+        e = launch_dependent(per_key ? replay_prepare_kernel<false, true> : replay_prepare_kernel<false, false>,
+                             grid, 0, s, a);
+    if (e != cudaSuccess) return e;
+    if (int8 && a.pv.R > 0)
+        return launch_dependent(per_key ? log_step_kernel<true, true, true, true>
+                                        : log_step_kernel<true, false, true, true>,
+                                grid, sm, s, a);
+    if (int8)
+        return launch_dependent(per_key ? log_step_kernel<true, true, false, true>
+                                        : log_step_kernel<true, false, false, true>,
+                                grid, sm, s, a);
+    return launch_dependent(per_key ? log_step_kernel<false, true, false, true>
+                                    : log_step_kernel<false, false, false, true>,
                             grid, sm, s, a);
 }
 

@@ -106,6 +106,7 @@ class StatePool:
                                             C.byref(handle)), "ls_pool_create")
         self.handle = handle
         self._staging = None
+        self._split_scratch = None
 
     def __del__(self):
         h = getattr(self, "handle", None)
@@ -144,6 +145,44 @@ class StatePool:
                                      _ptr(log_decay), _ptr(beta), _ptr(y),
                                      C.c_void_p(_stream(stream)))
         N.check(rc, "ls_decode_step")
+        return y
+
+    def split_scratch_bytes(self, batch: int) -> int:
+        out = C.c_size_t(0)
+        N.check(self.lib.ls_split_scratch_bytes(self.handle, int(batch), C.byref(out)),
+                "ls_split_scratch_bytes")
+        return int(out.value)
+
+    def decode_step_split(self, slot_idx, q, k, v, log_decay, beta, y=None, scratch=None,
+                          stream=None):
+        """ls_decode_step_split (deferred / INT8): the replay coefficients are
+        computed into ``scratch`` (a uint8 device tensor of at least
+        split_scratch_bytes(batch) bytes; one is kept on the pool when None)
+        by a first kernel, then the step applies them.  Returns y."""
+        slot_idx = self._slots(slot_idx)
+        B = int(slot_idx.numel())
+        dev, f32 = self.device, torch.float32
+        _need(q, "q", f32, dev, (B, self.H, self.d_k))
+        _need(k, "k", f32, dev, (B, self.H, self.d_k))
+        _need(v, "v", f32, dev, (B, self.H, self.d_v))
+        _need(log_decay, "log_decay", f32, dev,
+              (B, self.H) if self.dl == 1 else (B, self.H, self.d_k))
+        _need(beta, "beta", f32, dev, (B, self.H))
+        if y is None:
+            y = torch.empty(B, self.H, self.d_v, dtype=f32, device=dev)
+        _need(y, "y", f32, dev, (B, self.H, self.d_v))
+        need = self.split_scratch_bytes(B)
+        if scratch is None:
+            if self._split_scratch is None or self._split_scratch.numel() < need:
+                self._split_scratch = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+            scratch = self._split_scratch
+        if scratch.device != dev or not scratch.is_contiguous():
+            raise ValueError("scratch must be a contiguous tensor on the pool's device")
+        rc = self.lib.ls_decode_step_split(self.handle, _ptr(slot_idx), B, _ptr(q), _ptr(k),
+                                           _ptr(v), _ptr(log_decay), _ptr(beta), _ptr(y),
+                                           _ptr(scratch), scratch.numel() * scratch.element_size(),
+                                           C.c_void_p(_stream(stream)))
+        N.check(rc, "ls_decode_step_split")
         return y
 
     def staging_bytes(self, batch: int) -> int:

@@ -70,8 +70,10 @@ class Pair:
     """A GPU pool and an oracle stepped together over a workload."""
 
     def __init__(self, w: wl.Workload, variant: str, window: int, n_sample=None, device="cuda",
-                 seed=0, nthreads=0, col_scales=False, compensators=0, plain=False, k16=False):
+                 seed=0, nthreads=0, col_scales=False, compensators=0, plain=False, k16=False,
+                 split=False):
         self.w, self.variant, self.window = w, variant, window
+        self.split = bool(split)  # drive the pool through the split-replay entry point
         self.col_scales = bool(col_scales)
         self.compensators = int(compensators)
         self.dev = torch.device(device)
@@ -92,7 +94,10 @@ class Pair:
     def step(self, t: int, pool_id: int = 0, slot_idx=None, rows=None):
         w = self.w
         inputs = wl.step_inputs(w, t, pool=pool_id, device=self.dev, masks=self.masks)
-        y = self.pool.decode_step(self.slot_idx, *inputs)
+        if self.split:
+            y = self.pool.decode_step_split(self.slot_idx, *inputs)
+        else:
+            y = self.pool.decode_step(self.slot_idx, *inputs)
         s = self.sample
         hq = host_inputs(inputs, w, s.rows)
         yo = self.orc.step(s.state_idx, *hq)

@@ -280,6 +280,102 @@ def test_gdn_serving_b256_h48_bf16_keys(variant, window):
     assert p.pool.status() == 0
 
 
+# ---------------------------------------------------------------------------
+# split replay (DeltaLog §5.3): the coefficients from a prepare kernel
+# ---------------------------------------------------------------------------
+
+SPLIT_CASES = [("deferred", 1, {}), ("deferred", 5, {}), ("deferred", 16, {}),
+               ("deferred", 7, {"plain": True}), ("deferred", 6, {"k16": True}),
+               ("int8", 1, {}), ("int8", 5, {}), ("int8", 16, {"col_scales": True}),
+               ("int8", 6, {"col_scales": True, "compensators": 2}), ("int8", 13, {"k16": True})]
+
+
+@pytest.mark.parametrize("gate", ["scalar", "per_key"])
+@pytest.mark.parametrize("variant,window,fmt", SPLIT_CASES)
+def test_small_ragged_split(gate, variant, window, fmt):
+    from recurrent_state_quantization_gb300 import workloads as wl
+    H = _harness()
+    w = wl.custom("ragged-split", gate=gate, batch=5, heads=3, tokens=37, num_slots=7,
+                  windows=(window,), merge_interval=window, permute_slots=True,
+                  seed=71 + window, lam_scale=0.3)
+    p = H.Pair(w, variant, window, split=True, **fmt)
+    run_lockstep(p, w.tokens)
+    if variant == "int8":
+        check_int8(p)
+    else:
+        check_fp32(p)
+    assert p.pool.status() == 0
+
+
+@pytest.mark.parametrize("gate", ["scalar", "per_key"])
+@pytest.mark.parametrize("variant,window,fmt", SPLIT_CASES)
+def test_split_equals_fused_bitwise(gate, variant, window, fmt):
+    """The prepare kernel reduces each coefficient exactly as the fused replay
+    does, so the two entry points leave the same bits in y and in the pool."""
+    from recurrent_state_quantization_gb300 import StatePool
+    from recurrent_state_quantization_gb300 import workloads as wl
+    dev = torch.device("cuda")
+    w = wl.custom("split-bits", gate=gate, batch=6, heads=5, tokens=3 * window + 4, num_slots=9,
+                  windows=(window,), merge_interval=window, permute_slots=True, seed=91)
+    fused = StatePool(w.num_slots, w.heads, variant, gate, window, device=dev, **fmt)
+    split = StatePool(w.num_slots, w.heads, variant, gate, window, device=dev, **fmt)
+    slots = wl.slot_index(w, dev)
+    all_slots = torch.arange(w.num_slots, dtype=torch.int32, device=dev)
+    g = torch.Generator(device="cpu").manual_seed(5)
+    S0 = torch.randn(w.num_slots, w.heads, 128, 128, generator=g).to(dev) * 0.3
+    fused.load(all_slots, S0)
+    split.load(all_slots, S0)
+    masks = wl.static_masks(w, dev)
+    for t in range(w.tokens):
+        ins = wl.step_inputs(w, t, device=dev, masks=masks)
+        yf = fused.decode_step(slots, *ins)
+        ys = split.decode_step_split(slots, *ins)
+        assert torch.equal(yf, ys), f"token {t}: y differs"
+    assert torch.equal(fused.read(all_slots), split.read(all_slots))
+    if variant == "int8":
+        cf, sf = fused.read_int8(all_slots)
+        cs, ss = split.read_int8(all_slots)
+        assert torch.equal(cf, cs) and torch.equal(sf, ss)
+    assert fused.status() == 0 and split.status() == 0
+
+
+@pytest.mark.parametrize("variant,window", [("deferred", 8), ("int8", 16)])
+def test_gdn_serving_b256_h48_split(variant, window):
+    from recurrent_state_quantization_gb300 import workloads as wl
+    H = _harness()
+    w = wl.WORKLOADS[3]
+    p = H.Pair(w, variant, window, n_sample=6, split=True)
+    _prewarm_factory(w.prewarm_tokens)(p, 0)
+    run_lockstep(p, 48)
+    if variant == "int8":
+        check_int8(p)
+    else:
+        check_fp32(p)
+    assert p.pool.status() == 0
+
+
+def test_split_scratch_bytes_and_errors():
+    from recurrent_state_quantization_gb300 import StatePool
+    from recurrent_state_quantization_gb300 import _native as N
+    dev = torch.device("cuda")
+    for variant, W, comp, expect_cap in (("deferred", 16, 0, 18), ("int8", 5, 0, 6),
+                                         ("int8", 16, 4, 24), ("int8", 1, 0, 6)):
+        pool = StatePool(4, 3, variant, "scalar", W, device=dev, compensators=comp,
+                         col_scales=comp > 0)
+        assert pool.split_scratch_bytes(4) == 4 * 3 * expect_cap * 8
+        assert pool.split_scratch_bytes(0) == 0
+        slots = torch.arange(4, dtype=torch.int32, device=dev)
+        q = torch.zeros(4, 3, 128, device=dev)
+        lam = torch.zeros(4, 3, device=dev)
+        short = torch.empty(pool.split_scratch_bytes(4) - 16, dtype=torch.uint8, device=dev)
+        with pytest.raises(RuntimeError, match="buffer too small"):
+            pool.decode_step_split(slots, q, q, q, lam, lam, scratch=short)
+    eager = StatePool(4, 3, "eager", "scalar", 0, device=dev)
+    with pytest.raises(RuntimeError, match="invalid"):
+        eager.split_scratch_bytes(4)
+    assert N.LS_ABI_VERSION == 3
+
+
 @pytest.mark.parametrize("variant,window", [("eager", 0), ("deferred", 16)])
 def test_rwkv6_b128_h32_t512(variant, window):
     """RWKV6 (per-key decay, raw (k, v) updates) on the KDA 128x32 shapes."""
