@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define LS_ABI_VERSION 3
+#define LS_ABI_VERSION 4
 
 /* status codes */
 #define LS_OK 0
@@ -256,6 +256,27 @@ int ls_decode_step_split(ls_pool *pool, const int32_t *d_slot_idx,
  * pool.
  */
 int ls_split_scratch_bytes(const ls_pool *pool, int32_t batch, size_t *bytes);
+
+/*
+ * ls_decode_step_split without caller scratch.  No counterpart in the
+ * papers: an allocation-free form of the split-replay step for callers that
+ * cannot provide device scratch.  The coefficients go to one fixed device
+ * array of LS_SPLIT_STATIC_SCRATCH_BYTES per device (library-owned, placed
+ * by the CUDA runtime when the library's module loads); its address is
+ * looked up once per device, the current device being the pool's.  The call
+ * allocates nothing.  No part of the array has to start at zero.
+ * Overlapping calls race: every call on a device uses the same array, so
+ * two calls whose kernels may run at the same time (different streams,
+ * different host threads) corrupt each other's coefficients; order them on
+ * one stream.  Arguments, results and errors as ls_decode_step_split, and
+ * LS_ERR_SIZE when ls_split_scratch_bytes(pool, batch) exceeds
+ * LS_SPLIT_STATIC_SCRATCH_BYTES (nothing is launched then).
+ */
+#define LS_SPLIT_STATIC_SCRATCH_BYTES (16u << 20)
+int ls_decode_step_split_static(ls_pool *pool, const int32_t *d_slot_idx,
+                                int32_t batch, const float *q, const float *k,
+                                const float *v, const float *log_decay,
+                                const float *beta, float *y, void *stream);
 
 /*
  * Device bytes of the staging buffer ls_decode_step_host needs for `batch`.

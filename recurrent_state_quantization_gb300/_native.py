@@ -33,17 +33,18 @@ LS_INT8_COLUMN_SCALES = 1
 LS_MAX_COMPENSATORS = 8
 LS_PLAIN_UPDATE = 1 << 12
 LS_LOG_BF16_K = 1 << 13
+LS_SPLIT_STATIC_SCRATCH_BYTES = 16 << 20
 
 
 def LS_INT8_COMPENSATORS(r: int) -> int:
     return int(r) << 8
-LS_ABI_VERSION = 3  # the include/ls.h these prototypes follow
+LS_ABI_VERSION = 4  # the include/ls.h these prototypes follow
 
 # Every symbol include/ls.h declares.
 EXPORTS = (
     "ls_error_string", "ls_abi_version", "ls_pool_required_bytes", "ls_pool_create",
     "ls_pool_destroy", "ls_pool_load", "ls_pool_reset_slots", "ls_decode_step",
-    "ls_decode_step_split", "ls_split_scratch_bytes",
+    "ls_decode_step_split", "ls_split_scratch_bytes", "ls_decode_step_split_static",
     "ls_step_staging_bytes", "ls_decode_step_host", "ls_window_commit", "ls_pool_read",
     "ls_pool_read_int8", "ls_pool_read_int8_col_scales", "ls_pool_read_compensators",
     "ls_pool_read_log_meta",
@@ -88,6 +89,7 @@ def load() -> C.CDLL:
         "ls_step_staging_bytes": (C.c_int, [P, I32, C.POINTER(SZ)]),
         "ls_decode_step_split": (C.c_int, [P, P, I32, P, P, P, P, P, P, P, SZ, P]),
         "ls_split_scratch_bytes": (C.c_int, [P, I32, C.POINTER(SZ)]),
+        "ls_decode_step_split_static": (C.c_int, [P, P, I32, P, P, P, P, P, P, P]),
         "ls_decode_step_host": (C.c_int, [P, P, I32, P, P, P, P, P, P, P, SZ, P]),
         "ls_window_commit": (C.c_int, [P, P, I32, P]),
         "ls_pool_read": (C.c_int, [P, P, I32, P, P]),

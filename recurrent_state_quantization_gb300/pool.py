@@ -185,6 +185,32 @@ class StatePool:
         N.check(rc, "ls_decode_step_split")
         return y
 
+    def decode_step_split_static(self, slot_idx, q, k, v, log_decay, beta, y=None, stream=None):
+        """ls_decode_step_split_static: the split-replay step with the
+        library's fixed device scratch (allocates nothing).  Calls that may
+        run concurrently on one device race on that scratch."""
+        slot_idx = self._slots(slot_idx)
+        B = int(slot_idx.numel())
+        dev, f32 = self.device, torch.float32
+        _need(q, "q", f32, dev, (B, self.H, self.d_k))
+        _need(k, "k", f32, dev, (B, self.H, self.d_k))
+        _need(v, "v", f32, dev, (B, self.H, self.d_v))
+        _need(log_decay, "log_decay", f32, dev,
+              (B, self.H) if self.dl == 1 else (B, self.H, self.d_k))
+        _need(beta, "beta", f32, dev, (B, self.H))
+        if y is None:
+            y = torch.empty(B, self.H, self.d_v, dtype=f32, device=dev)
+        _need(y, "y", f32, dev, (B, self.H, self.d_v))
+        need = self.split_scratch_bytes(B)
+        if need > N.LS_SPLIT_STATIC_SCRATCH_BYTES:
+            raise ValueError(f"batch {B} needs {need} bytes of split-replay scratch; the static "
+                             f"array holds {N.LS_SPLIT_STATIC_SCRATCH_BYTES}")
+        rc = self.lib.ls_decode_step_split_static(self.handle, _ptr(slot_idx), B, _ptr(q), _ptr(k),
+                                                  _ptr(v), _ptr(log_decay), _ptr(beta), _ptr(y),
+                                                  C.c_void_p(_stream(stream)))
+        N.check(rc, "ls_decode_step_split_static")
+        return y
+
     def staging_bytes(self, batch: int) -> int:
         out = C.c_size_t(0)
         N.check(self.lib.ls_step_staging_bytes(self.handle, int(batch), C.byref(out)),

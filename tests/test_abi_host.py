@@ -168,7 +168,7 @@ def test_error_strings(lib):
         s = lib.ls_error_string(code)
         assert isinstance(s, bytes) and len(s) > 0
     from recurrent_state_quantization_gb300 import _native as N
-    assert lib.ls_abi_version() == N.LS_ABI_VERSION == 3
+    assert lib.ls_abi_version() == N.LS_ABI_VERSION == 4
 
 
 def test_split_entry_points_reject_null_before_any_launch(lib):
@@ -178,6 +178,8 @@ def test_split_entry_points_reject_null_before_any_launch(lib):
     assert sz.value == 7
     assert lib.ls_decode_step_split(None, None, 1, None, None, None, None, None, None, None, 0,
                                     None) == N.LS_ERR_INVALID
+    assert lib.ls_decode_step_split_static(None, None, 1, None, None, None, None, None, None,
+                                           None) == N.LS_ERR_INVALID
 
 
 def test_product_path_does_not_import_the_oracle():

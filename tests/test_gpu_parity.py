@@ -373,7 +373,7 @@ def test_split_scratch_bytes_and_errors():
     eager = StatePool(4, 3, "eager", "scalar", 0, device=dev)
     with pytest.raises(RuntimeError, match="invalid"):
         eager.split_scratch_bytes(4)
-    assert N.LS_ABI_VERSION == 3
+    assert N.LS_ABI_VERSION == 4
 
 
 @pytest.mark.parametrize("variant,window", [("eager", 0), ("deferred", 16)])
