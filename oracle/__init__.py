@@ -49,8 +49,8 @@ def _load():
         lib.orc_dequantize_cols.argtypes = [I64, I32, I32, P, P, P, P]
         lib.orc_window_step.argtypes = [I64, I32, I32, I32, I32, I32, I32, I32, P, P, P, P, P,
                                         P, P, P, P, P, P, P, P, P, P, P, P, I32]
-        lib.orc_window_commit.argtypes = [I64, I32, I32, I32, I32, P, P, P, P, P, P, P, P]
-        lib.orc_window_load.argtypes = [I64, I32, I32, I32, I32, P, P, P, P, P, P, P, P, P]
+        lib.orc_window_commit.argtypes = [I64, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, P]
+        lib.orc_window_load.argtypes = [I64, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, P, P]
         lib.orc_window_unrolled.argtypes = [I64, I32, I32, I32, I32, I32, I32, P, P, P, P, P,
                                             P, P, P, P, P, P]
         lib.orc_window_readout.argtypes = [I64, I32, I32, I32, I32, I32, I32, P, P, P, P, P,
@@ -215,17 +215,21 @@ class WindowInt8Oracle(_Base):
     smoothed per-value-column format of LeapQuant §3.4 eq. 7 / App. B.3
     (row factors = smoothing vector c, column factors = scales b).
     compensators=r: r Compensator Tokens (LeapQuant §3.3) fitted at every
-    boundary; the residual is what is quantized."""
+    boundary; the residual is what is quantized.
+    k16: bfloat16 keys in the records (DeltaLog §3.4).  r16: FP16 records,
+    keys and values, and FP16 compensator pairs (LeapQuant §4.3)."""
 
     def __init__(self, nstates, dk, dv, dl, W, nthreads=0, col_scales=False, compensators=0,
-                 k16=False):
+                 k16=False, r16=False):
         super().__init__(nstates, dk, dv, dl, nthreads)
         if W < 1:
             raise ValueError("W >= 1")
         self.W = int(W)
         self.mode = 1 if col_scales else 0
         self.r = int(compensators)
-        self.k16 = 1 if k16 else 0
+        if k16 and r16:
+            raise ValueError("k16 and r16 are exclusive")
+        self.rec = 2 if r16 else (1 if k16 else 0)
         self.ck = np.zeros((self.n, max(self.r, 1), dk), dtype=np.float64)
         self.cu = np.zeros((self.n, max(self.r, 1), dv), dtype=np.float64)
         self.Z = np.zeros((self.n, dk, dv), dtype=np.int8)
@@ -241,7 +245,7 @@ class WindowInt8Oracle(_Base):
         idx = self._idx(idx)
         q, k, v, lam, beta = self._inputs(idx, q, k, v, lam, beta)
         y = np.zeros((idx.size, self.dv), dtype=np.float64)
-        _check(_load().orc_window_step(idx.size, self.mode, self.r, self.k16, self.dk, self.dv,
+        _check(_load().orc_window_step(idx.size, self.mode, self.r, self.rec, self.dk, self.dv,
                                        self.dl,
                                        self.W, _p(self.Z), _p(self.s), _p(self.fc),
                                        _p(self.ck), _p(self.cu), _p(self.Sw),
@@ -271,7 +275,7 @@ class WindowInt8Oracle(_Base):
 
     def commit(self, idx):
         idx = self._idx(idx)
-        _check(_load().orc_window_commit(idx.size, self.mode, self.r, self.dk, self.dv,
+        _check(_load().orc_window_commit(idx.size, self.mode, self.r, self.rec, self.dk, self.dv,
                                          _p(self.Z), _p(self.s), _p(self.fc), _p(self.ck),
                                          _p(self.cu), _p(self.Sw), _p(self.cnt), _p(idx)),
                "window commit")
@@ -280,7 +284,8 @@ class WindowInt8Oracle(_Base):
         idx = self._idx(idx)
         S = np.ascontiguousarray(np.asarray(S, dtype=np.float64).reshape(idx.size, self.dk,
                                                                           self.dv))
-        _check(_load().orc_window_load(idx.size, self.mode, self.r, self.dk, self.dv, _p(S),
+        _check(_load().orc_window_load(idx.size, self.mode, self.r, self.rec, self.dk, self.dv,
+                                       _p(S),
                                        _p(self.Z), _p(self.s), _p(self.fc), _p(self.ck),
                                        _p(self.cu), _p(self.Sw), _p(self.cnt), _p(idx)),
                "window load")

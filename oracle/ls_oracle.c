@@ -187,9 +187,38 @@ static double bf16_round(float x)
     return (double)y;
 }
 
-static double stored_key(int k16, float k)
+/*
+ * FP16 records ([LQ] §4.3: the window's buffered records and the r
+ * compensator pairs are kept in FP16): x rounded to the nearest IEEE
+ * binary16 number, ties to even.  In [2^(e-1), 2^e) binary16 has 11
+ * significant bits, so its spacing is 2^(e-11); below 2^-14 (subnormals)
+ * the spacing stays 2^-24.  A magnitude that rounds above 65504 is infinite.
+ */
+static double fp16_round(double x)
 {
-    return k16 ? bf16_round(k) : (double)k;
+    if (x == 0.0 || isnan(x) || isinf(x)) return x;
+    const double a = fabs(x);
+    int e;
+    (void)frexp(a, &e); /* 2^(e-1) <= a < 2^e */
+    int q = e - 11;
+    if (q < -24) q = -24;
+    const double step = ldexp(1.0, q);
+    double r = rint(a / step) * step; /* a / step is exact */
+    if (r > 65504.0) r = INFINITY;
+    return copysign(r, x);
+}
+
+/* Record formats: 0 FP32; 1 bfloat16 keys ([DL] §3.4); 2 FP16 keys and
+ * values, and FP16 compensator pairs ([LQ] §4.3). */
+#define REC_FP32 0
+#define REC_BF16_K 1
+#define REC_FP16 2
+
+static double stored_key(int rec, float k)
+{
+    if (rec == REC_BF16_K) return bf16_round(k);
+    if (rec == REC_FP16) return fp16_round((double)k);
+    return (double)k;
 }
 
 /* ------------------------------------------------------------------------ */
@@ -553,7 +582,7 @@ static void dequant_mode(int mode, int dk, int dv, const int8_t *Z,
 #define COMP_ITERS 3
 
 static void fit_compensators(int r, int dk, int dv, double *R, double *ck,
-                             double *cu, int warm)
+                             double *cu, int warm, int rec)
 {
     double v[1024], z[1024], w[1024];
     for (int h = 0; h < r; ++h) {
@@ -585,6 +614,12 @@ static void fit_compensators(int r, int dk, int dv, double *R, double *ck,
             kk[i] = a;
         }
         for (int j = 0; j < dv; ++j) u[j] = v[j];
+        /* FP16 pairs: the stored (rounded) pair is the one the residual
+         * loses, so the next pair is fitted to what is left of it */
+        if (rec == REC_FP16) {
+            for (int i = 0; i < dk; ++i) kk[i] = fp16_round(kk[i]);
+            for (int j = 0; j < dv; ++j) u[j] = fp16_round(u[j]);
+        }
         for (int i = 0; i < dk; ++i)
             for (int j = 0; j < dv; ++j) R[(size_t)i * dv + j] -= kk[i] * u[j];
     }
@@ -600,7 +635,7 @@ int orc_fit_compensators(int64_t n, int r, int dk, int dv, double *S,
 #pragma omp parallel for schedule(static)
     for (int64_t h = 0; h < n; ++h)
         fit_compensators(r, dk, dv, S + (size_t)h * dk * dv, ck + (size_t)h * r * dk,
-                         cu + (size_t)h * r * dv, warm);
+                         cu + (size_t)h * r * dv, warm, REC_FP32);
     return ORC_OK;
 }
 
@@ -610,11 +645,11 @@ int orc_fit_compensators(int64_t n, int r, int dk, int dv, double *S,
  * residual R = S - K~ U~^T in the pool's format, and restart the window
  * from dequant(R-hat) + K~ U~^T.  r = 0: plain quantization of S.
  */
-static void boundary(int mode, int r, int dk, int dv, double *S, int8_t *Z,
+static void boundary(int mode, int r, int rec, int dk, int dv, double *S, int8_t *Z,
                      float *s, float *fc, double *ck, double *cu, int warm)
 {
     (void)warm;
-    if (r > 0) fit_compensators(r, dk, dv, S, ck, cu, 0);
+    if (r > 0) fit_compensators(r, dk, dv, S, ck, cu, 0, rec);
     quant_mode(mode, dk, dv, S, Z, s, fc);
     dequant_mode(mode, dk, dv, Z, s, fc, S);
     for (int h = 0; h < r; ++h)
@@ -694,7 +729,7 @@ int orc_dequantize_cols(int64_t n, int dk, int dv, const int8_t *Z,
  *     with nc compensator pairs, the boundary of §3.3, see boundary()).
  *   ck   [nc*dk], cu [nc*dv] double: the window's compensator pairs.
  */
-static void window_one(int mode, int nc, int k16, int dk, int dv, int dl, int W,
+static void window_one(int mode, int nc, int rec, int dk, int dv, int dl, int W,
                        int8_t *Z, float *s, float *fc, double *ck, double *cu,
                        double *Sw, double *rl, double *rk, double *ru,
                        int32_t *cntp, const float *q, const float *k,
@@ -705,17 +740,24 @@ static void window_one(int mode, int nc, int k16, int dk, int dv, int dl, int W,
     double u[1024];
     eager_one(0, dk, dv, dl, Sw, q, k, v, lam, beta, y, r, u);
     for (int t = 0; t < dl; ++t) rl[(size_t)c * dl + t] = (double)lam[t];
-    for (int i = 0; i < dk; ++i) rk[(size_t)c * dk + i] = stored_key(k16, k[i]);
-    /* k16: from here on the state holds the stored key-side factor, as a
-     * read of the record does (y above used k itself) */
-    if (k16)
+    for (int i = 0; i < dk; ++i) rk[(size_t)c * dk + i] = stored_key(rec, k[i]);
+    for (int j = 0; j < dv; ++j)
+        ru[(size_t)c * dv + j] = rec == REC_FP16 ? fp16_round(u[j]) : u[j];
+    /* 16-bit records: from here on the state holds the stored record, as a
+     * read of the record does (y above used k and u themselves) */
+    if (rec == REC_BF16_K)
         for (int i = 0; i < dk; ++i) {
             const double dlt = rk[(size_t)c * dk + i] - (double)k[i];
             for (int j = 0; j < dv; ++j) Sw[(size_t)i * dv + j] += dlt * u[j];
         }
-    for (int j = 0; j < dv; ++j) ru[(size_t)c * dv + j] = u[j];
+    else if (rec == REC_FP16)
+        for (int i = 0; i < dk; ++i) {
+            const double kh = rk[(size_t)c * dk + i], kx = (double)k[i];
+            for (int j = 0; j < dv; ++j)
+                Sw[(size_t)i * dv + j] += kh * ru[(size_t)c * dv + j] - kx * u[j];
+        }
     if (c + 1 == W) {
-        boundary(mode, nc, dk, dv, Sw, Z, s, fc, ck, cu, 1);
+        boundary(mode, nc, rec, dk, dv, Sw, Z, s, fc, ck, cu, 1);
         *cntp = 0;
     } else {
         *cntp = c + 1;
@@ -731,14 +773,15 @@ static int window_args_ok(int mode, int r, int dk, int dv, int dl, int W)
 /* fc: the column factors ([n_states][dv]); may be NULL in mode 0.  ck, cu:
  * [n_states][nc][dk], [n_states][nc][dv] (nc compensator pairs); may be NULL
  * when nc = 0. */
-int orc_window_step(int64_t n, int mode, int nc, int k16, int dk, int dv, int dl, int W,
+int orc_window_step(int64_t n, int mode, int nc, int rec, int dk, int dv, int dl, int W,
                     int8_t *Z, float *s, float *fc, double *ck, double *cu,
                     double *Sw, double *rl, double *rk, double *ru,
                     int32_t *cnt, const int64_t *idx, const float *q,
                     const float *k, const float *v, const float *lam,
                     const float *beta, double *y, int nthreads)
 {
-    if (n < 0 || !window_args_ok(mode, nc, dk, dv, dl, W)) return ORC_ERR_ARG;
+    if (n < 0 || !window_args_ok(mode, nc, dk, dv, dl, W) || rec < 0 || rec > REC_FP16)
+        return ORC_ERR_ARG;
     if ((mode == 1 && fc == NULL) || (nc > 0 && (ck == NULL || cu == NULL)))
         return ORC_ERR_ARG;
     if (n == 0) return ORC_OK;
@@ -754,7 +797,7 @@ int orc_window_step(int64_t n, int mode, int nc, int k16, int dk, int dv, int dl
 #pragma omp for schedule(dynamic, 4)
             for (int64_t row = 0; row < n; ++row) {
                 const int64_t h = idx[row];
-                window_one(mode, nc, k16, dk, dv, dl, W, Z + (size_t)h * dk * dv,
+                window_one(mode, nc, rec, dk, dv, dl, W, Z + (size_t)h * dk * dv,
                            s + (size_t)h * dk, mode ? fc + (size_t)h * dv : NULL,
                            nc ? ck + (size_t)h * nc * dk : NULL,
                            nc ? cu + (size_t)h * nc * dv : NULL,
@@ -771,18 +814,18 @@ int orc_window_step(int64_t n, int mode, int nc, int k16, int dk, int dv, int dl
 }
 
 /* Close the current window early: quantize S_i, start a new window. */
-int orc_window_commit(int64_t n, int mode, int r, int dk, int dv, int8_t *Z,
+int orc_window_commit(int64_t n, int mode, int r, int rec, int dk, int dv, int8_t *Z,
                       float *s, float *fc, double *ck, double *cu, double *Sw,
                       int32_t *cnt, const int64_t *idx)
 {
-    if (n < 0 || !window_args_ok(mode, r, dk, dv, 1, 1) ||
+    if (n < 0 || !window_args_ok(mode, r, dk, dv, 1, 1) || rec < 0 || rec > REC_FP16 ||
         (mode == 1 && fc == NULL) || (r > 0 && (ck == NULL || cu == NULL)))
         return ORC_ERR_ARG;
 #pragma omp parallel for schedule(static)
     for (int64_t row = 0; row < n; ++row) {
         const int64_t h = idx[row];
         if (cnt[h] == 0) continue;
-        boundary(mode, r, dk, dv, Sw + (size_t)h * dk * dv, Z + (size_t)h * dk * dv,
+        boundary(mode, r, rec, dk, dv, Sw + (size_t)h * dk * dv, Z + (size_t)h * dk * dv,
                  s + (size_t)h * dk, mode ? fc + (size_t)h * dv : NULL,
                  r ? ck + (size_t)h * r * dk : NULL, r ? cu + (size_t)h * r * dv : NULL, 1);
         cnt[h] = 0;
@@ -792,11 +835,11 @@ int orc_window_commit(int64_t n, int mode, int r, int dk, int dv, int8_t *Z,
 
 /* Start a window from a given state: S-hat_0 = quant_8(S). */
 /* (A load starts the compensator fit from the all-ones vector.) */
-int orc_window_load(int64_t n, int mode, int r, int dk, int dv, const double *S,
+int orc_window_load(int64_t n, int mode, int r, int rec, int dk, int dv, const double *S,
                     int8_t *Z, float *s, float *fc, double *ck, double *cu,
                     double *Sw, int32_t *cnt, const int64_t *idx)
 {
-    if (n < 0 || !window_args_ok(mode, r, dk, dv, 1, 1) ||
+    if (n < 0 || !window_args_ok(mode, r, dk, dv, 1, 1) || rec < 0 || rec > REC_FP16 ||
         (mode == 1 && fc == NULL) || (r > 0 && (ck == NULL || cu == NULL)))
         return ORC_ERR_ARG;
 #pragma omp parallel for schedule(static)
@@ -804,7 +847,7 @@ int orc_window_load(int64_t n, int mode, int r, int dk, int dv, const double *S,
         const int64_t h = idx[row];
         double *Sh = Sw + (size_t)h * dk * dv;
         for (size_t e = 0; e < (size_t)dk * dv; ++e) Sh[e] = S[(size_t)row * dk * dv + e];
-        boundary(mode, r, dk, dv, Sh, Z + (size_t)h * dk * dv, s + (size_t)h * dk,
+        boundary(mode, r, rec, dk, dv, Sh, Z + (size_t)h * dk * dv, s + (size_t)h * dk,
                  mode ? fc + (size_t)h * dv : NULL, r ? ck + (size_t)h * r * dk : NULL,
                  r ? cu + (size_t)h * r * dv : NULL, 0);
         cnt[h] = 0;
