@@ -29,8 +29,15 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 bool is_log_variant(int32_t v) { return v == LS_DEFERRED_FP32 || v == LS_WINDOW_INT8; }
 
 struct Layout {
-    size_t status, base, scale, colf, lbar, len, klog, ulog, lamlog, total;
+    size_t status, base, scale, colf, lbar, len, klog, ulog, lamlog, foldq, total;
 };
+
+// INT8 pools with per-row scales and no compensator pairs close their windows
+// on the tensor cores, in a kernel of its own after the step.
+bool int8_mma_fold(const ls_pool_desc* d) {
+    return d->variant == LS_WINDOW_INT8 && (d->flags & LS_INT8_COLUMN_SCALES) == 0 &&
+           ((d->flags >> 8) & 15u) == 0;
+}
 
 // Checks a descriptor; fills the layout when it is valid.
 int make_layout(const ls_pool_desc* d, Layout* L) {
@@ -76,6 +83,9 @@ int make_layout(const ls_pool_desc* d, Layout* L) {
     // scalar gate: one snapshot per entry, per-state stride padded to a
     // multiple of 4 floats so every state's snapshots start 16-byte aligned
     off = align_up(off + nh * (dl == 1 ? (W + 3) / 4 * 4 : W * dl) * 4);
+    // window-end queue of the tensor-core fold (INT8, per-row scales, no pairs)
+    L->foldq = off;
+    off = align_up(off + (int8_mma_fold(d) ? 16 + nh * 4 : 0));
     L->total = off;
     return LS_OK;
 }
@@ -101,6 +111,8 @@ ls::PoolView make_view(const ls_pool_desc& d, const Layout& L, unsigned char* m)
     v.cap = v.W + v.R;
     v.dl = d.gate == LS_GATE_PER_KEY ? kD : 1;
     v.lam_stride = d.gate == LS_GATE_PER_KEY ? v.cap * kD : (v.cap + 3) / 4 * 4;
+    v.foldq = int8_mma_fold(&d) ? reinterpret_cast<int32_t*>(m + L.foldq) : nullptr;
+    v.fold_grid = 1;
     return v;
 }
 
@@ -112,6 +124,7 @@ int prepare_all() {
     if (ls::prepare_log_step_kernels() != cudaSuccess) return LS_ERR_CUDA;
     if (ls::prepare_fold_kernels() != cudaSuccess) return LS_ERR_CUDA;
     if (ls::prepare_aux_kernels() != cudaSuccess) return LS_ERR_CUDA;
+    if (ls::prepare_window_fold_kernels() != cudaSuccess) return LS_ERR_CUDA;
     return LS_OK;
 }
 
@@ -174,7 +187,8 @@ int launch_step(ls_pool* p, const ls::StepArgs& a, cudaStream_t s) {
     const bool per_key = d.gate == LS_GATE_PER_KEY;
     if (d.variant == LS_EAGER_FP32) return cuda_status(ls::launch_eager_step(a, per_key, s));
     // deferred / INT8: one launch; a head whose window closes on this token
-    // folds its log into the base inside the same kernel
+    // folds its log into the base inside the same kernel, or (INT8 with a
+    // window-end queue) in the tensor-core fold launched right after it
     return cuda_status(ls::launch_log_step(a, d.variant == LS_WINDOW_INT8, per_key, s));
 }
 
@@ -228,6 +242,7 @@ int ls_pool_create(const ls_pool_desc* desc, void* dev_mem, size_t bytes, void* 
     p->bytes = bytes;
     p->view = make_view(*desc, L, p->mem);
     p->num_sms = sms > 0 ? sms : 1;
+    p->view.fold_grid = p->num_sms;
     if (cudaMemsetAsync(dev_mem, 0, L.total, static_cast<cudaStream_t>(stream)) != cudaSuccess ||
         (p->view.R > 0 && ls::launch_init_comp(p->view, static_cast<cudaStream_t>(stream)) != cudaSuccess)) {
         delete p;

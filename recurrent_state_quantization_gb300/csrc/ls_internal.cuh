@@ -56,6 +56,11 @@ struct PoolView {
     int32_t k16;           // 1: klog holds bfloat16
     int32_t cap;           // log entries per state: W + R
     int32_t lam_stride;    // floats per state in lamlog
+    int32_t* foldq;        // INT8 with per-row scales and no compensator pairs:
+                           //   window-end queue [0] count, [1] next, [2] done,
+                           //   [3] unused, [4 ..] state indices (the tensor-core
+                           //   fold kernel's work list); nullptr otherwise
+    int32_t fold_grid;     // CTAs of the window-end fold kernel (the SM count)
 };
 
 struct StepArgs {
@@ -120,10 +125,14 @@ cudaError_t prepare_eager_step_kernels();
 cudaError_t prepare_log_step_kernels();
 cudaError_t prepare_fold_kernels();
 cudaError_t prepare_aux_kernels();
+cudaError_t prepare_window_fold_kernels();
 
 cudaError_t launch_eager_step(const StepArgs& a, bool per_key, cudaStream_t s);
 cudaError_t launch_log_step(const StepArgs& a, bool int8, bool per_key, cudaStream_t s);
 cudaError_t launch_log_step_split(const StepArgs& a, bool int8, bool per_key, cudaStream_t s);
+// INT8 pools with a window-end queue: fold every state the step just queued
+// (a no-op launch when the queue is empty).
+cudaError_t launch_window_fold(const PoolView& pv, bool per_key, cudaStream_t s);
 // deferred / INT8: fold the live log into the base (commit) or into a caller
 // buffer (read) for n slots.
 cudaError_t launch_fold(const AuxArgs& a, bool int8, bool per_key, bool commit, cudaStream_t s);

@@ -416,6 +416,15 @@ __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, 
         if (lane == 0) pv.len[hd] = L + 1;
         return -1;
     }
+    if (INT8 && pv.foldq != nullptr) {
+        // window end, folded by the tensor-core kernel launched after this
+        // one: the log is full (len = W) until that kernel resets it
+        if (lane == 0) {
+            pv.len[hd] = W;
+            pv.foldq[4 + atomicAdd(pv.foldq, 1)] = static_cast<int32_t>(hd);
+        }
+        return -1;
+    }
     *lp_out = lp4.x;
     return static_cast<long long>(hd);  // INT8 window end: the CTA folds the W entries
 }
@@ -577,9 +586,12 @@ cudaError_t launch_log_step(const StepArgs& a, bool int8, bool per_key, cudaStre
     if (int8 && a.pv.R > 0)  // compensator pairs: the kernel that also fits them
         return launch_dependent(per_key ? log_step_kernel<true, true, true> : log_step_kernel<true, false, true>,
                                 grid, sm, s, a);
-    if (int8)
-        return launch_dependent(per_key ? log_step_kernel<true, true, false> : log_step_kernel<true, false, false>,
-                                grid, sm, s, a);
+    if (int8) {
+        const cudaError_t e = launch_dependent(
+            per_key ? log_step_kernel<true, true, false> : log_step_kernel<true, false, false>, grid, sm, s, a);
+        if (e != cudaSuccess || a.pv.foldq == nullptr) return e;
+        return launch_window_fold(a.pv, per_key, s);
+    }
     return launch_dependent(per_key ? log_step_kernel<false, true, false> : log_step_kernel<false, false, false>,
                             grid, sm, s, a);
 }
@@ -600,10 +612,13 @@ cudaError_t launch_log_step_split(const StepArgs& a, bool int8, bool per_key, cu
         return launch_dependent(per_key ? log_step_kernel<true, true, true, true>
                                         : log_step_kernel<true, false, true, true>,
                                 grid, sm, s, a);
-    if (int8)
-        return launch_dependent(per_key ? log_step_kernel<true, true, false, true>
-                                        : log_step_kernel<true, false, false, true>,
-                                grid, sm, s, a);
+    if (int8) {
+        e = launch_dependent(per_key ? log_step_kernel<true, true, false, true>
+                                     : log_step_kernel<true, false, false, true>,
+                             grid, sm, s, a);
+        if (e != cudaSuccess || a.pv.foldq == nullptr) return e;
+        return launch_window_fold(a.pv, per_key, s);
+    }
     return launch_dependent(per_key ? log_step_kernel<false, true, false, true>
                                     : log_step_kernel<false, false, false, true>,
                             grid, sm, s, a);

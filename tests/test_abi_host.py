@@ -60,10 +60,13 @@ def test_required_bytes_layout(lib):
     # eager: header + dense FP32 states
     rc, b = _bytes(lib, _desc(variant=N.LS_EAGER_FP32, window=0))
     assert rc == 0 and b == 256 + al(nh * 128 * 128 * 4)
-    # INT8, scalar gate: INT8 base, scales, lbar, len, W entries (K, U, log-decay)
+    # INT8, scalar gate: INT8 base, scales, lbar, len, W entries (K, U, log-decay),
+    # and the window-end queue of the tensor-core fold (16-byte header + one
+    # state index per state)
     rc, b = _bytes(lib, _desc())
     expect = (256 + al(nh * 128 * 128) + al(nh * 128 * 4) + al(nh * 4)
-              + al(nh * 4) + 2 * al(nh * W * 128 * 4) + al(nh * ((W + 3) // 4 * 4) * 4))
+              + al(nh * 4) + 2 * al(nh * W * 128 * 4) + al(nh * ((W + 3) // 4 * 4) * 4)
+              + al(16 + nh * 4))
     assert rc == 0 and b == expect
     # deferred, per-key gate
     rc, b = _bytes(lib, _desc(variant=N.LS_DEFERRED_FP32, gate=N.LS_GATE_PER_KEY))
@@ -90,7 +93,8 @@ def test_column_scale_flag(lib):
     al = lambda x: (x + 255) // 256 * 256
     rc0, b0 = _bytes(lib, _desc())
     rc1, b1 = _bytes(lib, _desc(flags=N.LS_INT8_COLUMN_SCALES))
-    assert rc0 == 0 and rc1 == 0 and b1 == b0 + al(nh * 128 * 4)
+    # no window-end queue: the column-scale format folds inside the step kernel
+    assert rc0 == 0 and rc1 == 0 and b1 == b0 + al(nh * 128 * 4) - al(16 + nh * 4)
     for variant in (N.LS_EAGER_FP32, N.LS_DEFERRED_FP32):
         rc, _ = _bytes(lib, _desc(variant=variant, flags=N.LS_INT8_COLUMN_SCALES))
         assert rc == N.LS_ERR_INVALID
