@@ -174,10 +174,10 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def make_pools(w, variant, window, dev, col_scales=False, compensators=0, k16=False):
+def make_pools(w, variant, window, dev, col_scales=False, compensators=0, k16=False, r16=False):
     from recurrent_state_quantization_gb300 import StatePool
     return [StatePool(w.num_slots, w.heads, variant, w.gate, window, device=dev,
-                      col_scales=col_scales, compensators=compensators, k16=k16)
+                      col_scales=col_scales, compensators=compensators, k16=k16, r16=r16)
             for _ in range(w.pools)]
 
 
@@ -323,19 +323,23 @@ def window_sweep(w, slot_idx, masks, inputs, ring, dev, peak, peak_kind, eager_p
     """INT8 head-steps/s and achieved algorithmic GB/s for each window W (a
     whole number of windows, 4 pools, warmed states); for W = 16 in the
     smoothed per-value-column format, without and with 4 Compensator Tokens
-    (the full LeapQuant boundary format); and, with bfloat16 key-side log
-    factors (DeltaLog §3.4), INT8 W = 16 and deferred FP32 M = 16."""
+    (the full LeapQuant boundary format); with bfloat16 key-side log factors
+    (DeltaLog §3.4), INT8 W = 16 and deferred FP32 M = 16; and with FP16
+    records (LeapQuant §4.1, §4.3), INT8 W = 16 per-key-row and in the full
+    LeapQuant format (smoothed + 4 FP16 Compensator Tokens)."""
     import torch
     from recurrent_state_quantization_gb300 import bytemodel as bm
     all_slots = torch.arange(w.num_slots, dtype=torch.int32, device=dev)
     res = []
     stream = torch.cuda.current_stream()
     heads = w.batch * w.heads
-    cases = ([("int8", W_, False, 0, False) for W_ in SWEEP_W]
-             + [("int8", 16, True, 0, False), ("int8", 16, True, 4, False),
-                ("int8", 16, False, 0, True), ("deferred", 16, False, 0, True)])
-    for variant, W, cols, comp, k16 in cases:
-        pools = make_pools(w, variant, W, dev, col_scales=cols, compensators=comp, k16=k16)
+    cases = ([("int8", W_, False, 0, False, False) for W_ in SWEEP_W]
+             + [("int8", 16, True, 0, False, False), ("int8", 16, True, 4, False, False),
+                ("int8", 16, False, 0, True, False), ("deferred", 16, False, 0, True, False),
+                ("int8", 16, False, 0, False, True), ("int8", 16, True, 4, False, True)])
+    for variant, W, cols, comp, k16, r16 in cases:
+        pools = make_pools(w, variant, W, dev, col_scales=cols, compensators=comp, k16=k16,
+                           r16=r16)
         for p in range(w.pools):
             pools[p].load(all_slots, eager_pools[p].read(all_slots))
         y = torch.empty(w.batch, w.heads, w.d_v, device=dev)
@@ -353,15 +357,16 @@ def window_sweep(w, slot_idx, masks, inputs, ring, dev, peak, peak_kind, eager_p
         torch.cuda.synchronize()
         ms = a.elapsed_time(b)
         hs = heads * w.pools * tokens
-        p_k = 2 if k16 else 4
+        p_k = 2 if (k16 or r16) else 4
         per = (bm.deferred_bytes(w.gate, W, p_k=p_k) if variant == "deferred" else
-               bm.int8_bytes(w.gate, W, col_scales=cols, compensators=comp, p_k=p_k))
+               bm.int8_bytes(w.gate, W, col_scales=cols, compensators=comp, p_k=p_k,
+                             p_u=2 if r16 else 4))
         gbs = per * hs / (ms * 1e-3) / 1e9
         fmt = ("fp32 base" if variant == "deferred" else
                "smoothed per-value-column" if cols else "per-key-row")
         res.append({"variant": variant, "window": W,
                     "format": fmt + (f" + {comp} compensator tokens" if comp else "") +
-                    (" + bf16 key log" if k16 else ""),
+                    (" + bf16 key log" if k16 else "") + (" + fp16 records" if r16 else ""),
                     "algorithmic_bytes_per_head_step": per,
                     "tokens": tokens, "head_steps_per_s": hs / (ms * 1e-3),
                     "achieved_gbs": gbs, "frac_of_" + peak_kind + "_hbm": gbs / peak})

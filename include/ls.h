@@ -134,6 +134,19 @@ typedef enum {
  * use k.  A log entry shrinks by 2 d_k bytes.
  */
 #define LS_LOG_BF16_K (1u << 13)
+
+/*
+ * ls_pool_desc.flags: LS_INT8_FP16_RECORDS (LS_WINDOW_INT8 only, not with
+ * LS_LOG_BF16_K): the window's buffered records -- the keys k and the
+ * corrected values u -- and the compensator pairs are stored in IEEE
+ * binary16, rounded to nearest even; the decay snapshots stay FP32 ("LeapQuant:
+ * Efficient Linear Attention with Accurate Recurrent State Quantization", §4.1:
+ * FP16 Compensator Tokens; §4.3: the FP16 update buffer of a window).  The
+ * token's own output uses k and u; later reads, the window end and the state
+ * use the stored records.  A scalar-gate record takes 516 bytes instead of
+ * 1028.  Values beyond the binary16 range become infinite (not checked).
+ */
+#define LS_INT8_FP16_RECORDS (1u << 14)
 #define LS_INT8_COMPENSATORS(r) ((uint32_t)(r) << 8)
 
 typedef struct {
@@ -145,9 +158,10 @@ typedef struct {
     int32_t gate;      /* ls_gate                                              */
     int32_t window;    /* W (INT8) or M (deferred), 1..LS_MAX_WINDOW; ignored
                           (may be 0) for LS_EAGER_FP32                          */
-    uint32_t flags;    /* 0; for LS_WINDOW_INT8 also LS_INT8_COLUMN_SCALES and
-                          LS_INT8_COMPENSATORS(r); for the FP32 variants also
-                          LS_PLAIN_UPDATE; LS_LOG_BF16_K for the log variants */
+    uint32_t flags;    /* 0; for LS_WINDOW_INT8 also LS_INT8_COLUMN_SCALES,
+                          LS_INT8_COMPENSATORS(r) and LS_INT8_FP16_RECORDS; for
+                          the FP32 variants also LS_PLAIN_UPDATE; LS_LOG_BF16_K
+                          for the log variants */
 } ls_pool_desc;
 
 /* Human-readable name of a status code.  Never NULL. */

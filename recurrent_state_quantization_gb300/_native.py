@@ -33,6 +33,7 @@ LS_INT8_COLUMN_SCALES = 1
 LS_MAX_COMPENSATORS = 8
 LS_PLAIN_UPDATE = 1 << 12
 LS_LOG_BF16_K = 1 << 13
+LS_INT8_FP16_RECORDS = 1 << 14
 LS_SPLIT_STATIC_SCRATCH_BYTES = 16 << 20
 
 

@@ -20,6 +20,8 @@ written; the roofline fraction divides them by a measured kernel time.
   scale per value column to that base; r Compensator Tokens (§3.3) add r
   log entries read by every token and written once per window.
 * bfloat16 key-side log factors (DeltaLog §3.4): p_K = 2 in C_entry.
+* FP16 records (LeapQuant §4.1, §4.3): p_K = p_U = 2 in C_entry, for the
+  window's records and the compensator pairs alike.
 """
 from __future__ import annotations
 
@@ -62,10 +64,10 @@ def deferred_bytes(gate: str, M: int, d_k: int = 128, d_v: int = 128, p_k: int =
 
 
 def int8_bytes(gate: str, W: int, d_k: int = 128, d_v: int = 128, col_scales: bool = False,
-               compensators: int = 0, p_k: int = 4) -> float:
-    comp = compensators * entry_bytes(gate, d_k, d_v) * (1 + 1 / W)
+               compensators: int = 0, p_k: int = 4, p_u: int = 4) -> float:
+    comp = compensators * entry_bytes(gate, d_k, d_v, p_k, p_u) * (1 + 1 / W)
     return log_cycle_bytes(state_bytes_int8(d_k, d_v, col_scales), gate, W, d_k, d_v,
-                           p_k) + comp
+                           p_k, p_u) + comp
 
 
 def variant_bytes(variant: str, gate: str, window: int = 1) -> float:

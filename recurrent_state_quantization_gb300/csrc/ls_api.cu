@@ -44,7 +44,11 @@ int make_layout(const ls_pool_desc* d, Layout* L) {
     if (d == nullptr || L == nullptr) return LS_ERR_INVALID;
     if (d->variant < LS_EAGER_FP32 || d->variant > LS_WINDOW_INT8) return LS_ERR_INVALID;
     const uint32_t int8_flags = LS_INT8_COLUMN_SCALES | LS_INT8_COMPENSATORS(15);
-    if ((d->flags & ~(int8_flags | LS_PLAIN_UPDATE | LS_LOG_BF16_K)) != 0) return LS_ERR_INVALID;
+    if ((d->flags & ~(int8_flags | LS_PLAIN_UPDATE | LS_LOG_BF16_K | LS_INT8_FP16_RECORDS)) != 0)
+        return LS_ERR_INVALID;
+    if ((d->flags & LS_INT8_FP16_RECORDS) &&
+        (d->variant != LS_WINDOW_INT8 || (d->flags & LS_LOG_BF16_K)))
+        return LS_ERR_INVALID;
     if ((d->flags & LS_LOG_BF16_K) && (!is_log_variant(d->variant) || ((d->flags >> 8) & 15u) != 0))
         return LS_ERR_INVALID;
     const uint32_t ncomp = (d->flags >> 8) & 15u;
@@ -75,10 +79,11 @@ int make_layout(const ls_pool_desc* d, Layout* L) {
     off = align_up(off + (log ? nh * dl * 4 : 0));
     L->len = off;
     off = align_up(off + (log ? nh * 4 : 0));
+    const bool rec16 = (d->flags & LS_INT8_FP16_RECORDS) != 0;
     L->klog = off;
-    off = align_up(off + nh * W * kD * ((d->flags & LS_LOG_BF16_K) ? 2 : 4));
+    off = align_up(off + nh * W * kD * (((d->flags & LS_LOG_BF16_K) || rec16) ? 2 : 4));
     L->ulog = off;
-    off = align_up(off + nh * W * kD * 4);
+    off = align_up(off + nh * W * kD * (rec16 ? 2 : 4));
     L->lamlog = off;
     // scalar gate: one snapshot per entry, per-state stride padded to a
     // multiple of 4 floats so every state's snapshots start 16-byte aligned
@@ -108,6 +113,7 @@ ls::PoolView make_view(const ls_pool_desc& d, const Layout& L, unsigned char* m)
     v.R = log ? static_cast<int32_t>((d.flags >> 8) & 15u) : 0;
     v.plain = (d.flags & LS_PLAIN_UPDATE) ? 1 : 0;
     v.k16 = (d.flags & LS_LOG_BF16_K) ? 1 : 0;
+    v.rec16 = (d.flags & LS_INT8_FP16_RECORDS) ? 1 : 0;
     v.cap = v.W + v.R;
     v.dl = d.gate == LS_GATE_PER_KEY ? kD : 1;
     v.lam_stride = d.gate == LS_GATE_PER_KEY ? v.cap * kD : (v.cap + 3) / 4 * 4;

@@ -189,8 +189,13 @@ __global__ void __launch_bounds__(kThreads) reset_kernel(const AuxArgs a) {
         // a zero state's pairs: k~ = 0, u~ = the cold start 1 / sqrt(128)
         const size_t kb = hd * static_cast<size_t>(pv.cap);
         for (int idx = threadIdx.x; idx < pv.R * kD; idx += kThreads) {
-            pv.klog[kb * kD + idx] = 0.0f;
-            pv.ulog[kb * kD + idx] = 0.08838834764831845f;
+            if (pv.rec16) {
+                reinterpret_cast<__half*>(pv.klog)[kb * kD + idx] = __float2half_rn(0.0f);
+                reinterpret_cast<__half*>(pv.ulog)[kb * kD + idx] = __float2half_rn(0.08838834764831845f);
+            } else {
+                pv.klog[kb * kD + idx] = 0.0f;
+                pv.ulog[kb * kD + idx] = 0.08838834764831845f;
+            }
         }
         const int nl = pv.dl == kD ? pv.R * kD : pv.R;
         for (int idx = threadIdx.x; idx < nl; idx += kThreads)
@@ -303,8 +308,13 @@ __global__ void __launch_bounds__(kThreads) read_comp_kernel(const AuxArgs a) {
     const size_t o = (static_cast<size_t>(n) * H + h) * static_cast<size_t>(pv.R) * kD;
     const size_t kb = hd * static_cast<size_t>(pv.cap) * kD;
     for (int idx = threadIdx.x; idx < pv.R * kD; idx += kThreads) {
-        a.state_out[o + idx] = pv.klog[kb + idx];
-        a.scales_out[o + idx] = pv.ulog[kb + idx];
+        if (pv.rec16) {
+            a.state_out[o + idx] = __half2float(reinterpret_cast<const __half*>(pv.klog)[kb + idx]);
+            a.scales_out[o + idx] = __half2float(reinterpret_cast<const __half*>(pv.ulog)[kb + idx]);
+        } else {
+            a.state_out[o + idx] = pv.klog[kb + idx];
+            a.scales_out[o + idx] = pv.ulog[kb + idx];
+        }
     }
 }
 
@@ -314,7 +324,12 @@ __global__ void __launch_bounds__(kThreads) read_comp_kernel(const AuxArgs a) {
 __global__ void __launch_bounds__(kD) init_comp_kernel(const PoolView pv) {
     const size_t hd = blockIdx.x;
     const size_t kb = hd * static_cast<size_t>(pv.cap) * kD;
-    for (int idx = threadIdx.x; idx < pv.R * kD; idx += kD) pv.ulog[kb + idx] = 0.08838834764831845f;
+    for (int idx = threadIdx.x; idx < pv.R * kD; idx += kD) {
+        if (pv.rec16)
+            reinterpret_cast<__half*>(pv.ulog)[kb + idx] = __float2half_rn(0.08838834764831845f);
+        else
+            pv.ulog[kb + idx] = 0.08838834764831845f;
+    }
     if (threadIdx.x == 0) pv.len[hd] = pv.R;
 }
 

@@ -6,6 +6,7 @@
 #include <cstdint>
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "ls_internal.cuh"
@@ -181,6 +182,44 @@ __device__ __forceinline__ uint2 float4_to_bf16x4(float4 v) {
     const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
     return make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
 }
+
+// Four binary16 (two words, low half first) widened to FP32, exactly.
+__device__ __forceinline__ float4 half4_to_float4(uint2 w) {
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// FP32 -> binary16, round to nearest even, four at a time.
+__device__ __forceinline__ uint2 float4_to_half4(float4 v) {
+    const __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+    return make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+}
+
+// One stored 16-bit key factor widened to FP32: bfloat16 (bf16) or binary16.
+__device__ __forceinline__ float key16_to_float(unsigned short h, bool bf16) {
+    return bf16 ? __uint_as_float(static_cast<uint32_t>(h) << 16) : __half2float(__ushort_as_half(h));
+}
+
+// Four stored key factors (16-byte or 8-byte group at element index e, a
+// multiple of 4) as FP32: FP32, bfloat16 (k16) or binary16 (rec16).
+__device__ __forceinline__ float4 key4_at(const void* p, size_t e, const PoolView& pv) {
+    if (pv.k16) return bf16x4_to_float4(reinterpret_cast<const uint2*>(p)[e >> 2]);
+    if (pv.rec16) return half4_to_float4(reinterpret_cast<const uint2*>(p)[e >> 2]);
+    return reinterpret_cast<const float4*>(p)[e >> 2];
+}
+
+// The same for value factors: FP32 or binary16 (rec16).
+__device__ __forceinline__ float4 val4_at(const void* p, size_t e, const PoolView& pv) {
+    if (pv.rec16) return half4_to_float4(reinterpret_cast<const uint2*>(p)[e >> 2]);
+    return reinterpret_cast<const float4*>(p)[e >> 2];
+}
+
+// Bytes per stored key / value factor.
+__host__ __device__ __forceinline__ uint32_t key_bytes(const PoolView& pv) {
+    return (pv.k16 || pv.rec16) ? 2u : 4u;
+}
+__host__ __device__ __forceinline__ uint32_t val_bytes(const PoolView& pv) { return pv.rec16 ? 2u : 4u; }
 
 __device__ __forceinline__ void flag_status(int32_t* status, int32_t bit) {
     atomicOr(status, bit);

@@ -46,14 +46,16 @@ struct PoolView {
                            //   scales b; nullptr for per-row scales
     float* lbar;           // log variants: [P*H][dl] cumulative log-decay
     int32_t* len;          // log variants: [P*H] live log length
-    float* klog;           // [P*H][cap][d_k]  key factors k (bfloat16 when k16)
-    float* ulog;           // [P*H][cap][d_v]  value factors u
+    float* klog;           // [P*H][cap][d_k]  key factors k (bfloat16 when k16,
+                           //   binary16 when rec16)
+    float* ulog;           // [P*H][cap][d_v]  value factors u (binary16 when rec16)
     float* lamlog;         // [P*H][lam_stride] cumulative log-decay snapshots:
                            //   per-key gate [cap][d_k]; scalar gate [cap] padded to 4
     int32_t P, H, W, dl;
     int32_t R;             // INT8: compensator pairs at the head of each window (0: none)
     int32_t plain;         // 1: update pair (k, v), no delta-rule correction
     int32_t k16;           // 1: klog holds bfloat16
+    int32_t rec16;         // 1: klog and ulog hold IEEE binary16 (INT8 FP16 records)
     int32_t cap;           // log entries per state: W + R
     int32_t lam_stride;    // floats per state in lamlog
     int32_t* foldq;        // INT8 with per-row scales and no compensator pairs:

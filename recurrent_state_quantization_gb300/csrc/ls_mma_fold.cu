@@ -110,16 +110,16 @@ template <bool PER_KEY>
 __device__ __forceinline__ void stage_records(const PoolView& pv, size_t hd, int c0, int nl, GroupSmem& gs) {
     const size_t eo = (hd * static_cast<size_t>(pv.cap) + c0) * kD;
     const uint32_t part = static_cast<uint32_t>(nl) * kVecBytes;
-    const uint32_t kpart = pv.k16 ? part / 2 : part;
+    const uint32_t kpart = static_cast<uint32_t>(nl) * kD * key_bytes(pv);
+    const uint32_t upart = static_cast<uint32_t>(nl) * kD * val_bytes(pv);
     const size_t lb0 = hd * static_cast<size_t>(pv.lam_stride);
     const uint32_t lam_bytes = PER_KEY ? part : static_cast<uint32_t>((nl + 3) / 4 * 16);
-    uint32_t bytes = part + kpart + lam_bytes;
+    uint32_t bytes = upart + kpart + lam_bytes;
     if (c0 == 0) bytes += kVecBytes + (PER_KEY ? kVecBytes : 0);
     fence_proxy_async();  // the buffers were last used by generic loads and stores
     mbar_arrive_expect_tx(&gs.ld_bar, bytes);
-    bulk_g2s(gs.ops[1], pv.ulog + eo, part, &gs.ld_bar);
-    bulk_g2s(gs.ops[3], reinterpret_cast<const unsigned char*>(pv.klog) + eo * (pv.k16 ? 2 : 4), kpart,
-             &gs.ld_bar);
+    bulk_g2s(gs.ops[1], reinterpret_cast<const unsigned char*>(pv.ulog) + eo * val_bytes(pv), upart, &gs.ld_bar);
+    bulk_g2s(gs.ops[3], reinterpret_cast<const unsigned char*>(pv.klog) + eo * key_bytes(pv), kpart, &gs.ld_bar);
     if constexpr (PER_KEY)
         bulk_g2s(gs.ops[2], pv.lamlog + lb0 + static_cast<size_t>(c0) * kD, part, &gs.ld_bar);
     else
@@ -218,11 +218,12 @@ __device__ __forceinline__ bool fold_state(const PoolView& pv, size_t hd, float 
             u[l] = 0.0f;
             x[l] = 0.0f;
             if (l < nl) {
-                u[l] = ru[l * kD + gt];
-                x[l] = pv.k16 ? __uint_as_float(static_cast<uint32_t>(
-                                                    reinterpret_cast<const unsigned short*>(gs.ops[3])[l * kD + gt])
-                                                << 16)
-                              : reinterpret_cast<const float*>(gs.ops[3])[l * kD + gt];
+                u[l] = pv.rec16 ? __half2float(reinterpret_cast<const __half*>(gs.ops[1])[l * kD + gt])
+                                : ru[l * kD + gt];
+                x[l] = (pv.k16 || pv.rec16)
+                           ? key16_to_float(reinterpret_cast<const unsigned short*>(gs.ops[3])[l * kD + gt],
+                                            pv.k16 != 0)
+                           : reinterpret_cast<const float*>(gs.ops[3])[l * kD + gt];
                 if constexpr (PER_KEY) x[l] *= expf(lb - rl[l * kD + gt]);
             }
         }

@@ -128,9 +128,9 @@ __device__ __forceinline__ void issue_item(WarpSmem& ws, const StepArgs& a, int 
         const int e0 = (it - 1 - P::NT) * P::EPC;
         const int n = min(P::EPC, L - e0);
         const size_t eo = (hd * static_cast<size_t>(pv.cap) + e0) * kD;
-        const uint32_t part = static_cast<uint32_t>(n) * kVecBytes;
-        mbar_arrive_expect_tx(bar, part + P::EPC * 8);
-        bulk_g2s(dst, pv.ulog + eo, part, bar);
+        const uint32_t upart = static_cast<uint32_t>(n) * kD * val_bytes(pv);
+        mbar_arrive_expect_tx(bar, upart + P::EPC * 8);
+        bulk_g2s(dst, reinterpret_cast<const unsigned char*>(pv.ulog) + eo * val_bytes(pv), upart, bar);
         bulk_g2s(dst + P::EPC * kVecBytes, a.coef + static_cast<size_t>(row) * a.cstride + e0,
                  P::EPC * 8, bar);
     } else {
@@ -138,11 +138,13 @@ __device__ __forceinline__ void issue_item(WarpSmem& ws, const StepArgs& a, int 
         const int n = min(P::EPC, L - e0);
         const size_t eo = (hd * static_cast<size_t>(pv.cap) + e0) * kD;
         const uint32_t part = static_cast<uint32_t>(n) * kVecBytes;
-        const uint32_t kpart = pv.k16 ? part / 2 : part;  // bfloat16 keys: half the bytes
+        const uint32_t kpart = static_cast<uint32_t>(n) * kD * key_bytes(pv);  // 16-bit keys: half
+        const uint32_t upart = static_cast<uint32_t>(n) * kD * val_bytes(pv);
         const size_t lb0 = hd * static_cast<size_t>(pv.lam_stride);
-        mbar_arrive_expect_tx(bar, kpart + (PER_KEY ? 2 * part : part + 16));
-        bulk_g2s(dst, reinterpret_cast<const unsigned char*>(pv.klog) + eo * (pv.k16 ? 2 : 4), kpart, bar);
-        bulk_g2s(dst + P::EPC * kVecBytes, pv.ulog + eo, part, bar);
+        mbar_arrive_expect_tx(bar, kpart + upart + (PER_KEY ? part : 16));
+        bulk_g2s(dst, reinterpret_cast<const unsigned char*>(pv.klog) + eo * key_bytes(pv), kpart, bar);
+        bulk_g2s(dst + P::EPC * kVecBytes, reinterpret_cast<const unsigned char*>(pv.ulog) + eo * val_bytes(pv),
+                 upart, bar);
         if constexpr (PER_KEY)
             bulk_g2s(dst + 2 * P::EPC * kVecBytes, pv.lamlog + lb0 + static_cast<size_t>(e0) * kD,
                      part, bar);
@@ -354,7 +356,7 @@ __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, 
             const int n = min(P::EPC, L - e0);
             const float2* cf = reinterpret_cast<const float2*>(st + P::EPC * kVecBytes);
             for (int e = 0; e < n; ++e) {
-                const float4 U4 = st4p[e * 32 + lane];
+                const float4 U4 = val4_at(st, static_cast<size_t>(e) * kD + 4 * lane, pv);
                 const float2 c = cf[e];
                 r01 = make_float2(fmaf(c.x, U4.x, r01.x), fmaf(c.x, U4.y, r01.y));
                 r23 = make_float2(fmaf(c.x, U4.z, r23.x), fmaf(c.x, U4.w, r23.y));
@@ -366,9 +368,8 @@ __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, 
             const int e0 = (it - 1 - P::NT) * P::EPC;
             const int n = min(P::EPC, L - e0);
             for (int e = 0; e < n; ++e) {
-                const float4 K4 = pv.k16 ? bf16x4_to_float4(reinterpret_cast<const uint2*>(st)[e * 32 + lane])
-                                         : st4p[e * 32 + lane];
-                const float4 U4 = st4p[(P::EPC + e) * 32 + lane];
+                const float4 K4 = key4_at(st, static_cast<size_t>(e) * kD + 4 * lane, pv);
+                const float4 U4 = val4_at(st + P::EPC * kVecBytes, static_cast<size_t>(e) * kD + 4 * lane, pv);
                 float ck, cq;
                 if constexpr (PER_KEY) {
                     const float4 Lm = st4p[(2 * P::EPC + e) * 32 + lane];
@@ -403,9 +404,14 @@ __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, 
         const size_t eo = (hd * static_cast<size_t>(W) + L) * kD;
         if (pv.k16)
             reinterpret_cast<uint2*>(pv.klog)[(eo >> 2) + lane] = float4_to_bf16x4(k4);
+        else if (pv.rec16)
+            reinterpret_cast<uint2*>(pv.klog)[(eo >> 2) + lane] = float4_to_half4(k4);
         else
             st4(pv.klog + eo + 4 * lane, k4);
-        st4(pv.ulog + eo + 4 * lane, u4);
+        if (pv.rec16)
+            reinterpret_cast<uint2*>(pv.ulog)[(eo >> 2) + lane] = float4_to_half4(u4);
+        else
+            st4(pv.ulog + eo + 4 * lane, u4);
         const size_t lb0 = hd * static_cast<size_t>(pv.lam_stride);
         if constexpr (PER_KEY) st4(pv.lamlog + lb0 + static_cast<size_t>(L) * kD + 4 * lane, lp4);
         else if (lane == 0) pv.lamlog[lb0 + L] = lp4.x;
@@ -535,8 +541,7 @@ __global__ void __launch_bounds__(kThreads) replay_prepare_kernel(const StepArgs
 #pragma unroll 2
     for (int e = 0; e < L; ++e) {
         const size_t eo = e0 + static_cast<size_t>(e) * kD;
-        const float4 K4 = pv.k16 ? bf16x4_to_float4(reinterpret_cast<const uint2*>(pv.klog)[(eo >> 2) + lane])
-                                 : *reinterpret_cast<const float4*>(pv.klog + eo + 4 * lane);
+        const float4 K4 = key4_at(pv.klog, eo + 4 * lane, pv);
         float ck, cq;
         if constexpr (PER_KEY) {
             const float4 Lm = *reinterpret_cast<const float4*>(pv.lamlog + lb0 + static_cast<size_t>(e) * kD +

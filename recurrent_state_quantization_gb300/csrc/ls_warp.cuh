@@ -298,6 +298,15 @@ __device__ __forceinline__ void fit_compensators_cta(float2 (&lo)[16], float2 (&
         }
         cta_state_times(lo, hi, vs, ks);  // k~ = R v
         __syncthreads();
+        if (pv.rec16) {
+            // FP16 pairs: the stored (rounded) pair is the one the residual
+            // loses, so the next pair is fitted to what it leaves
+            if (tid < kD) {
+                ks[tid] = __half2float(__float2half_rn(ks[tid]));
+                vs[tid] = __half2float(__float2half_rn(vs[tid]));
+            }
+            __syncthreads();
+        }
         const float4 v4 = reinterpret_cast<const float4*>(vs)[lane];
 #pragma unroll
         for (int r4 = 0; r4 < 4; ++r4) {
@@ -311,8 +320,13 @@ __device__ __forceinline__ void fit_compensators_cta(float2 (&lo)[16], float2 (&
             }
         }
         if (tid < kD) {
-            pv.klog[(kb + h) * kD + tid] = ks[tid];
-            pv.ulog[(kb + h) * kD + tid] = vs[tid];
+            if (pv.rec16) {
+                reinterpret_cast<__half*>(pv.klog)[(kb + h) * kD + tid] = __float2half_rn(ks[tid]);
+                reinterpret_cast<__half*>(pv.ulog)[(kb + h) * kD + tid] = __float2half_rn(vs[tid]);
+            } else {
+                pv.klog[(kb + h) * kD + tid] = ks[tid];
+                pv.ulog[(kb + h) * kD + tid] = vs[tid];
+            }
             if (pv.dl == kD) pv.lamlog[hd * static_cast<size_t>(pv.lam_stride) + h * kD + tid] = 0.0f;
             else if (tid == 0) pv.lamlog[hd * static_cast<size_t>(pv.lam_stride) + h] = 0.0f;
         }
@@ -455,11 +469,12 @@ __device__ __forceinline__ void fold_issue_log(const PoolView& pv, size_t hd, in
     const uint32_t part = static_cast<uint32_t>(nl) * kVecBytes;
     const size_t lb0 = hd * static_cast<size_t>(pv.lam_stride);
     const uint32_t lam_bytes = PER_KEY ? part : static_cast<uint32_t>((nl + 3) / 4 * 16);
-    const uint32_t kpart = pv.k16 ? part / 2 : part;  // bfloat16 keys: half the bytes
+    const uint32_t kpart = static_cast<uint32_t>(nl) * kD * key_bytes(pv);  // 16-bit keys: half
+    const uint32_t upart = static_cast<uint32_t>(nl) * kD * val_bytes(pv);
     fence_proxy_async();
-    mbar_arrive_expect_tx(fs.lbar, kpart + part + lam_bytes);
-    bulk_g2s(fs.rk, reinterpret_cast<const unsigned char*>(pv.klog) + eo * (pv.k16 ? 2 : 4), kpart, fs.lbar);
-    bulk_g2s(fs.ru, pv.ulog + eo, part, fs.lbar);
+    mbar_arrive_expect_tx(fs.lbar, kpart + upart + lam_bytes);
+    bulk_g2s(fs.rk, reinterpret_cast<const unsigned char*>(pv.klog) + eo * key_bytes(pv), kpart, fs.lbar);
+    bulk_g2s(fs.ru, reinterpret_cast<const unsigned char*>(pv.ulog) + eo * val_bytes(pv), upart, fs.lbar);
     if constexpr (PER_KEY)
         bulk_g2s(fs.rl, pv.lamlog + lb0 + static_cast<size_t>(c0) * kD, part, fs.lbar);
     else
@@ -601,6 +616,8 @@ __device__ bool fold_cta(const PoolView& pv, size_t hd, int n, const float* lbg,
                 if (pv.k16) {
                     const uint32_t w = reinterpret_cast<const uint32_t*>(fs.rk)[idx];
                     K2 = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+                } else if (pv.rec16) {
+                    K2 = __half22float2(reinterpret_cast<const __half2*>(fs.rk)[idx]);
                 } else {
                     K2 = reinterpret_cast<const float2*>(fs.rk)[idx];
                 }
@@ -616,7 +633,8 @@ __device__ bool fold_cta(const PoolView& pv, size_t hd, int n, const float* lbg,
                 const float a0 = g.x * K2.x, a1 = g.y * K2.y;
                 reinterpret_cast<float4*>(fs.a2)[idx] = make_float4(a0, a0, a1, a1);
             }
-            for (int idx = tid; idx < nl * (kD / 4); idx += kThreads) fs.u4[idx] = fs.ru[idx];
+            for (int idx = tid; idx < nl * (kD / 4); idx += kThreads)
+                fs.u4[idx] = val4_at(fs.ru, static_cast<size_t>(idx) * 4, pv);
             __syncthreads();
             const bool more = c0 + kFoldChunk < n;
             const bool next = !more && next_hd >= 0 && next_n > 0;

@@ -15,14 +15,14 @@ D = 128
 
 
 def make_oracle(variant, nstates, dl, window, nthreads=0, col_scales=False, compensators=0,
-                plain=False, k16=False):
+                plain=False, k16=False, r16=False):
     if variant == "eager":
         return oracle.EagerOracle(nstates, D, D, dl, nthreads, plain=plain)
     if variant == "deferred":
         return oracle.DeferredOracle(nstates, D, D, dl, window, nthreads, plain=plain, k16=k16)
     if variant == "int8":
         return oracle.WindowInt8Oracle(nstates, D, D, dl, window, nthreads, col_scales=col_scales,
-                                       compensators=compensators, k16=k16)
+                                       compensators=compensators, k16=k16, r16=r16)
     raise ValueError(variant)
 
 
@@ -71,18 +71,19 @@ class Pair:
 
     def __init__(self, w: wl.Workload, variant: str, window: int, n_sample=None, device="cuda",
                  seed=0, nthreads=0, col_scales=False, compensators=0, plain=False, k16=False,
-                 split=False):
+                 split=False, r16=False):
         self.w, self.variant, self.window = w, variant, window
         self.split = bool(split)  # drive the pool through the split-replay entry point
         self.col_scales = bool(col_scales)
         self.compensators = int(compensators)
+        self.r16 = bool(r16)
         self.dev = torch.device(device)
         self.pool = StatePool(w.num_slots, w.heads, variant, w.gate, window, device=self.dev,
                               col_scales=col_scales, compensators=compensators, plain=plain,
-                              k16=k16)
+                              k16=k16, r16=r16)
         self.orc = make_oracle(variant, w.num_slots * w.heads, w.dl, window, nthreads,
                                col_scales=col_scales, compensators=compensators, plain=plain,
-                               k16=k16)
+                               k16=k16, r16=r16)
         self.slot_idx = wl.slot_index(w, self.dev)
         self.sample = sample_rows(w, self.slot_idx, n_sample, seed)
         self.masks = wl.static_masks(w, self.dev)
@@ -208,6 +209,38 @@ class Pair:
             g = np.einsum("hi,hj->ij", kk[pos[int(slots_b[n_])], r % w.heads], uu[pos[int(slots_b[n_])], r % w.heads])
             o = np.einsum("hi,hj->ij", ko[n_], uo[n_])
             worst = max(worst, relmax(g, o))
+        return worst
+
+    def boundary_step_err(self):
+        """INT8 at a window boundary: max over the sampled heads' elements of
+        |S_gpu - S_orc| / (step_gpu / 2 + step_orc / 2 + 2^-10 max|S_orc|),
+        S the logical (dequantized) states and step the code step of each
+        side's own format (s_i, or c_i b_j with column scales).  Each side's
+        boundary state lies within half its own step of its unquantized
+        state, and the two unquantized states differ by FP32 rounding and by
+        binary16 rounding flips of single record elements (2^-11 of a record,
+        at most 2^-10 of the state), so the ratio is at most 1 whatever pairs
+        each side fitted."""
+        w, s = self.w, self.sample
+        slots_b = self.slot_idx.cpu().numpy()[s.rows // w.heads]
+        uniq = np.unique(slots_b)
+        ut = torch.as_tensor(uniq, dtype=torch.int32, device=self.dev)
+        S = self.pool.read(ut).double().cpu().numpy()
+        _, fr = self.pool.read_int8(ut)
+        fr = fr.double().cpu().numpy()
+        fc = self.pool.read_int8_col_scales(ut).double().cpu().numpy() if self.col_scales else None
+        pos = {int(x): i for i, x in enumerate(uniq)}
+        So = self.orc.logical(s.state_idx)
+        _, fro = self.orc.codes(s.state_idx)
+        fco = self.orc.col_factors(s.state_idx) if self.col_scales else None
+        worst = 0.0
+        for n_, r in enumerate(s.rows):
+            i = pos[int(slots_b[n_])]
+            sg = fr[i, r % w.heads][:, None] * (fc[i, r % w.heads][None, :] if fc is not None else 1.0)
+            so = fro[n_].astype(np.float64)[:, None] * (
+                fco[n_].astype(np.float64)[None, :] if fco is not None else 1.0)
+            bound = 0.5 * sg + 0.5 * so + (2.0 ** -10) * np.abs(So[n_]).max()
+            worst = max(worst, float(np.max(np.abs(S[i, r % w.heads] - So[n_]) / bound)))
         return worst
 
     def code_mismatch(self):

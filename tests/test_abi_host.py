@@ -127,6 +127,24 @@ def test_bf16_key_flag(lib):
     assert _bytes(lib, _desc(flags=N.LS_LOG_BF16_K | N.LS_INT8_COMPENSATORS(2)))[0] == N.LS_ERR_INVALID
 
 
+def test_fp16_record_flag(lib):
+    """LS_INT8_FP16_RECORDS: INT8 only, not with bfloat16 keys, compensator
+    pairs allowed; keys and values of the log take 2 bytes each."""
+    from recurrent_state_quantization_gb300 import _native as N
+    P, Hh, W = 4, 2, 16
+    nh = P * Hh
+    al = lambda x: (x + 255) // 256 * 256
+    for r in (0, 3):
+        C = W + r
+        rc0, b0 = _bytes(lib, _desc(flags=N.LS_INT8_COMPENSATORS(r)))
+        rc1, b1 = _bytes(lib, _desc(flags=N.LS_INT8_COMPENSATORS(r) | N.LS_INT8_FP16_RECORDS))
+        assert rc0 == rc1 == 0
+        assert b0 - b1 == 2 * (al(nh * C * 128 * 4) - al(nh * C * 128 * 2))
+    for variant in (N.LS_EAGER_FP32, N.LS_DEFERRED_FP32):
+        assert _bytes(lib, _desc(variant=variant, flags=N.LS_INT8_FP16_RECORDS))[0] == N.LS_ERR_INVALID
+    assert _bytes(lib, _desc(flags=N.LS_INT8_FP16_RECORDS | N.LS_LOG_BF16_K))[0] == N.LS_ERR_INVALID
+
+
 def test_compensator_flag(lib):
     """LS_INT8_COMPENSATORS(r): INT8 only, r <= 8; the log holds W + r entries
     (K, U, and the scalar-gate snapshots padded to 4)."""

@@ -63,3 +63,17 @@ def test_cycle_models_reduce_to_eager_at_m1():
     # M = 1: one base read and one base write per token, no log traffic
     assert bm.deferred_bytes("scalar", 1) == pytest.approx(bm.eager_bytes("scalar") + 8)
     assert bm.int8_bytes("scalar", 16) < bm.deferred_bytes("scalar", 16) < bm.eager_bytes("scalar")
+
+
+def test_fp16_records_halve_the_record_bytes():
+    """LeapQuant §4.3: a window of 16 FP16 records (k, u) of a 128 x 128 head
+    takes about 8 KiB; a scalar-gate record is 2 d_k + 2 d_v bytes plus its
+    FP32 decay snapshot, against 4 d_k + 4 d_v + 4 with FP32 records."""
+    from recurrent_state_quantization_gb300 import bytemodel as bm
+    assert bm.entry_bytes("scalar", p_k=2, p_u=2) == 516
+    assert bm.entry_bytes("scalar") == 1028
+    assert 16 * (bm.entry_bytes("scalar", p_k=2, p_u=2) - 4) == 8 * 1024
+    W = 16
+    full = bm.int8_bytes("scalar", W)
+    half = bm.int8_bytes("scalar", W, p_k=2, p_u=2)
+    assert full - half == ((W - 1) / W + (W - 1) / 2) * (1028 - 516)

@@ -36,6 +36,24 @@ CODE_FRAC_TOL_COMP = 2e-3
 # residual ~10x smaller than the state) inherit that difference relatively
 COMP_TOL = 1e-3
 FACTOR_TOL_COMP = 1e-2
+# FP16 records (LeapQuant §4.1, §4.3): a record element whose FP32 (kernel)
+# and fp64 (oracle) values straddle a binary16 rounding boundary is stored
+# one binary16 step (2^-11 relative) apart on the two sides, with
+# probability ~ their difference / 2^-11 (~1e-4 per element).  That moves S
+# by one step of the record's k_i u_j in one row or column: a row's absmax
+# by at most 2^-10 relative (k and u of one record), the codes of that row
+# or column by up to 127 * 2^-10 ~ 0.12 LSB, so near-tie flips there are
+# ~10x more frequent than in the FP32-record format; stored pairs differ by
+# one binary16 step in each factor.
+FACTOR_TOL_R16 = 2.0 ** -10
+CODE_FRAC_TOL_R16 = 2e-3
+# binary16 pairs: pair elements may sit one binary16 step apart (2^-11
+# relative in k~ and in u~); every later pair is fitted, by three power
+# steps that do not converge, to a residual that differs by those steps, so
+# it can turn within a near-degenerate singular subspace.  The pairs'
+# products are checked loosely; the boundary states are checked tightly
+# (boundary_step_err).
+COMP_TOL_R16_PAIRS = 5e-2
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -72,15 +90,28 @@ def run_lockstep(p, tokens, pool_id=0, code_checks=None):
         if p.variant == "int8" and t % p.window == 0 and t > 0:
             p.force_boundary()
         p.step(t, pool_id=pool_id)
-        if p.variant == "int8" and (t + 1) % p.window == 0:
+        if p.variant == "int8" and (t + 1) % p.window == 0 and p.r16 and p.compensators:
+            # binary16 pairs: a pair element whose FP32 and fp64 fits straddle
+            # a binary16 rounding boundary is stored one step apart, and the
+            # residual (quantized against a ~10-100x smaller row maximum)
+            # absorbs that step, so codes are not comparable one to one; each
+            # side's boundary state is still within half a code step of the
+            # same unquantized state
+            be = p.boundary_step_err()
+            assert be <= 1.0, f"token {t}: boundary states differ by {be:.3g} x the bound"
+            ce = p.comp_err()
+            assert ce <= COMP_TOL_R16_PAIRS, f"token {t}: compensator pairs rel err {ce:.3g}"
+        elif p.variant == "int8" and (t + 1) % p.window == 0:
             frac, mx = p.code_mismatch()
             if code_checks is not None:
                 code_checks.append((t, frac, mx))
             assert mx <= 1, f"token {t}: codes differ by {mx} LSB"
-            tol = CODE_FRAC_TOL_COMP if p.compensators else CODE_FRAC_TOL
+            tol = (CODE_FRAC_TOL_COMP if p.compensators else
+                   CODE_FRAC_TOL_R16 if p.r16 else CODE_FRAC_TOL)
             assert frac <= tol, f"token {t}: {frac:.3g} of codes differ"
             fe = p.factor_err()
-            ftol = FACTOR_TOL_COMP if p.compensators else FACTOR_TOL
+            ftol = (FACTOR_TOL_COMP if p.compensators else
+                    FACTOR_TOL_R16 if p.r16 else FACTOR_TOL)
             assert fe <= ftol, f"token {t}: scale / smoothing factors rel err {fe:.3g}"
             if p.compensators:
                 ce = p.comp_err()
@@ -281,13 +312,49 @@ def test_gdn_serving_b256_h48_bf16_keys(variant, window):
 
 
 # ---------------------------------------------------------------------------
+# FP16 records (LeapQuant §4.1, §4.3): k, u and the compensator pairs in binary16
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("gate", ["scalar", "per_key"])
+@pytest.mark.parametrize("window,cols,comp", [(1, False, 0), (5, False, 0), (16, False, 0),
+                                              (40, False, 0), (16, True, 0), (5, False, 2),
+                                              (16, True, 4)])
+def test_small_ragged_fp16_records(gate, window, cols, comp):
+    """The INT8 window with binary16 records against the oracle's: the row-scale
+    format folds on the tensor cores, the others in the step kernel."""
+    from recurrent_state_quantization_gb300 import workloads as wl
+    H = _harness()
+    w = wl.custom("ragged-r16", gate=gate, batch=5, heads=3, tokens=37, num_slots=7,
+                  windows=(window,), merge_interval=window, permute_slots=True,
+                  seed=61 + window, lam_scale=0.3)
+    p = H.Pair(w, "int8", window, col_scales=cols, compensators=comp, r16=True)
+    run_lockstep(p, w.tokens)
+    check_int8(p)
+    assert p.pool.status() == 0
+    ln, _ = p.pool.read_log_meta(p.slot_idx)
+    assert torch.all(ln == comp + (w.tokens % window))
+
+
+def test_gdn_serving_b256_h48_fp16_records():
+    from recurrent_state_quantization_gb300 import workloads as wl
+    H = _harness()
+    w = wl.WORKLOADS[3]
+    p = H.Pair(w, "int8", 16, n_sample=6, r16=True)
+    _prewarm_factory(w.prewarm_tokens)(p, 0)
+    run_lockstep(p, 64)
+    check_int8(p)
+    assert p.pool.status() == 0
+
+
+# ---------------------------------------------------------------------------
 # split replay (DeltaLog §5.3): the coefficients from a prepare kernel
 # ---------------------------------------------------------------------------
 
 SPLIT_CASES = [("deferred", 1, {}), ("deferred", 5, {}), ("deferred", 16, {}),
                ("deferred", 7, {"plain": True}), ("deferred", 6, {"k16": True}),
                ("int8", 1, {}), ("int8", 5, {}), ("int8", 16, {"col_scales": True}),
-               ("int8", 6, {"col_scales": True, "compensators": 2}), ("int8", 13, {"k16": True})]
+               ("int8", 6, {"col_scales": True, "compensators": 2}), ("int8", 13, {"k16": True}),
+               ("int8", 9, {"r16": True}), ("int8", 6, {"r16": True, "compensators": 2})]
 
 
 @pytest.mark.parametrize("gate", ["scalar", "per_key"])
