@@ -6,7 +6,7 @@ H = 48 heads, d = 128, four independent layer pools, states pre-warmed by 256
 eager updates) through all three storage variants, i.e. every step of the hot
 path: eager FP32 (read / update / write the dense state), deferred FP32 base +
 log (merge interval M = 16), per-window INT8 (window W = 16; appends, and the
-window-end fold + requantization on every 16th token).  The same tokens feed
+window-end fold + requantization on the tensor cores on every 16th token).  The same tokens feed
 the three variants.
 
 Prints one JSON line.  ``value`` = head-steps (B * H * tokens * pools *
@@ -277,8 +277,10 @@ def run_native(args, rank, world, local):
                           "algorithmic_bytes_per_head_step": bm.variant_bytes(n, w.gate, W),
                           "achieved_gbs": gbs, "frac_of_" + peak_kind + "_hbm": gbs / hbm_peak}
     value = job_throughput(heads * w.pools * len(variants) * args.steps, world, elapsed_ms)
-    # one kernel launch per decode call (the window fold runs inside the step kernel)
-    launches_per_step = w.pools * len(variants)
+    # kernel launches per decode call: one step kernel; an INT8 pool with
+    # per-row scales also launches the tensor-core window-end fold after it
+    # (every token; it returns at once unless a window closed)
+    launches_per_step = w.pools * sum(2 if n == "int8" else 1 for n, _ in variants)
 
     out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
