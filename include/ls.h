@@ -232,7 +232,11 @@ int ls_pool_reset_slots(ls_pool *pool, const int32_t *d_slots, int32_t n,
  * on the window-th token since the slot's last boundary the log is folded
  * into the base (FP32 for deferred; re-quantized per key row for INT8, after
  * y was read from the unquantized state).  Different slots may be at
- * different positions of their windows.
+ * different positions of their windows.  An INT8 pool with per-row scales
+ * and no compensator pairs queues its closing states in its own memory and
+ * folds them in a second kernel on the tensor cores, launched on the same
+ * stream by this call (every call; it ends at once when no window closed);
+ * the other formats fold inside the step kernel.
  * batch = 0 is a no-op.  Errors: LS_ERR_INVALID, LS_ERR_ALIGN, LS_ERR_SLOT
  * (batch > num_slots), LS_ERR_SIZE (batch * H >= 2^31), LS_ERR_CUDA.
  */

@@ -175,15 +175,19 @@ def test_commit_mid_window_and_reset(gate, variant, window):
 
 
 @pytest.mark.parametrize("gate", ["scalar", "per_key"])
-@pytest.mark.parametrize("variant,window", [("eager", 0), ("deferred", 4), ("int8", 4)])
-def test_changing_batches_keep_per_slot_phase(gate, variant, window):
+@pytest.mark.parametrize("variant,window,fmt", [("eager", 0, {}), ("deferred", 4, {}), ("int8", 4, {}),
+                                                ("int8", 5, {"r16": True}),
+                                                ("int8", 4, {"col_scales": True})])
+def test_changing_batches_keep_per_slot_phase(gate, variant, window, fmt):
     """Different subsets of slots decode at different tokens (continuous
-    batching), so every slot is at its own position in its window."""
+    batching), so every slot is at its own position in its window and the
+    window-end queue holds a different subset of states at every token
+    (per-row INT8 scales); the column-scale format folds in the step kernel."""
     oracle, H, StatePool, _, wl, _ = _mods()
     P, Hh = 6, 2
     w = wl.custom(gate=gate, batch=P, heads=Hh, num_slots=P, seed=21, lam_scale=0.3)
-    pool = StatePool(P, Hh, variant, gate, window)
-    orc = H.make_oracle(variant, P * Hh, w.dl, window)
+    pool = StatePool(P, Hh, variant, gate, window, **fmt)
+    orc = H.make_oracle(variant, P * Hh, w.dl, window, **fmt)
     rng = np.random.default_rng(0)
     worst = 0.0
     for t in range(23):
