@@ -464,7 +464,10 @@ def rwkv6(dev, peak, peak_kind, tokens=64):
 
 def e2e(w, variants, pools, slot_idx, dev, world=1, tokens=24):
     """The same step through ls_decode_step_host: inputs copied from pinned host
-    memory and y copied back inside the timed region, every call."""
+    memory and y copied back inside the timed region, every call.  Pool p is
+    driven on stream p % 2 (the layer pools are independent), so one pool's
+    host copies overlap another pool's kernels; every pool has its own host
+    output buffer."""
     import torch
     from recurrent_state_quantization_gb300 import workloads as wl
     host = []
@@ -475,14 +478,18 @@ def e2e(w, variants, pools, slot_idx, dev, world=1, tokens=24):
             row.append([x.cpu().pin_memory() for x in ins])
         host.append(row)
     hslots = slot_idx.cpu().pin_memory()
-    hy = torch.empty(w.batch, w.heads, w.d_v).pin_memory()
-    stream = torch.cuda.current_stream()
+    hy = {(n, p): torch.empty(w.batch, w.heads, w.d_v).pin_memory()
+          for n, _ in variants for p in range(w.pools)}
+    streams = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
+    torch.cuda.synchronize()
 
     def step(t):
         for n, _ in variants:
             for p in range(w.pools):
-                pools[n][p].decode_step_host(hslots, *host[p][t % 4], hy)
-        stream.synchronize()  # the step's result is on the host
+                pools[n][p].decode_step_host(hslots, *host[p][t % 4], hy[(n, p)],
+                                             stream=streams[p % 2])
+        for s in streams:
+            s.synchronize()  # the step's results are on the host
 
     for t in range(2):
         step(t)
@@ -498,7 +505,8 @@ def e2e(w, variants, pools, slot_idx, dev, world=1, tokens=24):
     return {"value": job_throughput(heads * calls * tokens, world, dt * 1e3), "unit": UNIT, "tokens": tokens,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "api": "ls_decode_step_host (pinned host buffers, cudaMemcpyAsync inside the "
-                   "library, host synchronizes on y every token)"}
+                   "library; layer pools alternate between two streams; the host synchronizes "
+                   "on every y every token)"}
 
 
 def cpu_baseline(w, variants, budget_s=6.0, steps=None):

@@ -89,8 +89,28 @@ struct Plan {
 };
 static_assert(kSplitEntries * (kVecBytes + 8) <= kStage, "a split log chunk fits a stage");
 
+// Log record formats, a template parameter of the step kernels so that the
+// per-entry replay carries no format branches: FP32 key and value factors,
+// bfloat16 keys (DeltaLog §3.4), or binary16 keys and values (LeapQuant
+// §4.1, §4.3).  The pool view's k16 / rec16 select the instantiation.
+constexpr int kRecFP32 = 0, kRecBF16K = 1, kRecFP16 = 2;
+__host__ __device__ constexpr uint32_t rec_key_bytes(int rec) { return rec == kRecFP32 ? 4u : 2u; }
+__host__ __device__ constexpr uint32_t rec_val_bytes(int rec) { return rec == kRecFP16 ? 2u : 4u; }
+
+template <int REC>
+__device__ __forceinline__ float4 rec_key4(const void* p, size_t e) {
+    if constexpr (REC == kRecBF16K) return bf16x4_to_float4(reinterpret_cast<const uint2*>(p)[e >> 2]);
+    else if constexpr (REC == kRecFP16) return half4_to_float4(reinterpret_cast<const uint2*>(p)[e >> 2]);
+    else return reinterpret_cast<const float4*>(p)[e >> 2];
+}
+template <int REC>
+__device__ __forceinline__ float4 rec_val4(const void* p, size_t e) {
+    if constexpr (REC == kRecFP16) return half4_to_float4(reinterpret_cast<const uint2*>(p)[e >> 2]);
+    else return reinterpret_cast<const float4*>(p)[e >> 2];
+}
+
 // Issue item `it` of head hd into stage it % kRing (lane 0 only).
-template <bool INT8, bool PER_KEY, bool SPLIT>
+template <bool INT8, bool PER_KEY, bool SPLIT, int REC>
 __device__ __forceinline__ void issue_item(WarpSmem& ws, const StepArgs& a, int row, size_t hd,
                                            int L, int it) {
     using P = Plan<INT8, PER_KEY, SPLIT>;
@@ -128,9 +148,9 @@ __device__ __forceinline__ void issue_item(WarpSmem& ws, const StepArgs& a, int 
         const int e0 = (it - 1 - P::NT) * P::EPC;
         const int n = min(P::EPC, L - e0);
         const size_t eo = (hd * static_cast<size_t>(pv.cap) + e0) * kD;
-        const uint32_t upart = static_cast<uint32_t>(n) * kD * val_bytes(pv);
+        const uint32_t upart = static_cast<uint32_t>(n) * kD * rec_val_bytes(REC);
         mbar_arrive_expect_tx(bar, upart + P::EPC * 8);
-        bulk_g2s(dst, reinterpret_cast<const unsigned char*>(pv.ulog) + eo * val_bytes(pv), upart, bar);
+        bulk_g2s(dst, reinterpret_cast<const unsigned char*>(pv.ulog) + eo * rec_val_bytes(REC), upart, bar);
         bulk_g2s(dst + P::EPC * kVecBytes, a.coef + static_cast<size_t>(row) * a.cstride + e0,
                  P::EPC * 8, bar);
     } else {
@@ -138,13 +158,13 @@ __device__ __forceinline__ void issue_item(WarpSmem& ws, const StepArgs& a, int 
         const int n = min(P::EPC, L - e0);
         const size_t eo = (hd * static_cast<size_t>(pv.cap) + e0) * kD;
         const uint32_t part = static_cast<uint32_t>(n) * kVecBytes;
-        const uint32_t kpart = static_cast<uint32_t>(n) * kD * key_bytes(pv);  // 16-bit keys: half
-        const uint32_t upart = static_cast<uint32_t>(n) * kD * val_bytes(pv);
+        const uint32_t kpart = static_cast<uint32_t>(n) * kD * rec_key_bytes(REC);  // 16-bit keys: half
+        const uint32_t upart = static_cast<uint32_t>(n) * kD * rec_val_bytes(REC);
         const size_t lb0 = hd * static_cast<size_t>(pv.lam_stride);
         mbar_arrive_expect_tx(bar, kpart + upart + (PER_KEY ? part : 16));
-        bulk_g2s(dst, reinterpret_cast<const unsigned char*>(pv.klog) + eo * key_bytes(pv), kpart, bar);
-        bulk_g2s(dst + P::EPC * kVecBytes, reinterpret_cast<const unsigned char*>(pv.ulog) + eo * val_bytes(pv),
-                 upart, bar);
+        bulk_g2s(dst, reinterpret_cast<const unsigned char*>(pv.klog) + eo * rec_key_bytes(REC), kpart, bar);
+        bulk_g2s(dst + P::EPC * kVecBytes,
+                 reinterpret_cast<const unsigned char*>(pv.ulog) + eo * rec_val_bytes(REC), upart, bar);
         if constexpr (PER_KEY)
             bulk_g2s(dst + 2 * P::EPC * kVecBytes, pv.lamlog + lb0 + static_cast<size_t>(e0) * kD,
                      part, bar);
@@ -163,7 +183,7 @@ __device__ __forceinline__ void issue_item(WarpSmem& ws, const StepArgs& a, int 
 //     after the token.  The base and log the CTA re-reads were just streamed
 //     by the warp and are mostly still in L2, while the per-warp GEMV keeps
 //     the integer arithmetic of every other token.
-template <bool INT8, bool PER_KEY, bool SPLIT>
+template <bool INT8, bool PER_KEY, bool SPLIT, int REC>
 __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, int row,
                                                float* lp_out) {
     using P = Plan<INT8, PER_KEY, SPLIT>;
@@ -197,7 +217,7 @@ __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, 
         for (int s = 0; s < kRing; ++s) mbar_init(&ws.bar[s], 1);
         ws.bar_live = 1u;
         mbar_fence_init();
-        for (int it = 0; it < min(kRing, NI); ++it) issue_item<INT8, PER_KEY, SPLIT>(ws, a, row, hd, L, it);
+        for (int it = 0; it < min(kRing, NI); ++it) issue_item<INT8, PER_KEY, SPLIT, REC>(ws, a, row, hd, L, it);
     }
     const float beta = __ldg(a.beta + row);
     float lp_scalar = 0.0f;
@@ -356,7 +376,7 @@ __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, 
             const int n = min(P::EPC, L - e0);
             const float2* cf = reinterpret_cast<const float2*>(st + P::EPC * kVecBytes);
             for (int e = 0; e < n; ++e) {
-                const float4 U4 = val4_at(st, static_cast<size_t>(e) * kD + 4 * lane, pv);
+                const float4 U4 = rec_val4<REC>(st, static_cast<size_t>(e) * kD + 4 * lane);
                 const float2 c = cf[e];
                 r01 = make_float2(fmaf(c.x, U4.x, r01.x), fmaf(c.x, U4.y, r01.y));
                 r23 = make_float2(fmaf(c.x, U4.z, r23.x), fmaf(c.x, U4.w, r23.y));
@@ -368,8 +388,8 @@ __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, 
             const int e0 = (it - 1 - P::NT) * P::EPC;
             const int n = min(P::EPC, L - e0);
             for (int e = 0; e < n; ++e) {
-                const float4 K4 = key4_at(st, static_cast<size_t>(e) * kD + 4 * lane, pv);
-                const float4 U4 = val4_at(st + P::EPC * kVecBytes, static_cast<size_t>(e) * kD + 4 * lane, pv);
+                const float4 K4 = rec_key4<REC>(st, static_cast<size_t>(e) * kD + 4 * lane);
+                const float4 U4 = rec_val4<REC>(st + P::EPC * kVecBytes, static_cast<size_t>(e) * kD + 4 * lane);
                 float ck, cq;
                 if constexpr (PER_KEY) {
                     const float4 Lm = st4p[(2 * P::EPC + e) * 32 + lane];
@@ -389,7 +409,7 @@ __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, 
             }
         }
         __syncwarp();  // every lane is done with the stage
-        if (lane == 0 && it + kRing < NI) issue_item<INT8, PER_KEY, SPLIT>(ws, a, row, hd, L, it + kRing);
+        if (lane == 0 && it + kRing < NI) issue_item<INT8, PER_KEY, SPLIT, REC>(ws, a, row, hd, L, it + kRing);
     }
 
     // ---- delta correction and output -----------------------------------------
@@ -402,13 +422,13 @@ __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, 
     // ---- append entry L -------------------------------------------------------
     {
         const size_t eo = (hd * static_cast<size_t>(W) + L) * kD;
-        if (pv.k16)
+        if constexpr (REC == kRecBF16K)
             reinterpret_cast<uint2*>(pv.klog)[(eo >> 2) + lane] = float4_to_bf16x4(k4);
-        else if (pv.rec16)
+        else if constexpr (REC == kRecFP16)
             reinterpret_cast<uint2*>(pv.klog)[(eo >> 2) + lane] = float4_to_half4(k4);
         else
             st4(pv.klog + eo + 4 * lane, k4);
-        if (pv.rec16)
+        if constexpr (REC == kRecFP16)
             reinterpret_cast<uint2*>(pv.ulog)[(eo >> 2) + lane] = float4_to_half4(u4);
         else
             st4(pv.ulog + eo + 4 * lane, u4);
@@ -435,7 +455,7 @@ __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, 
     return static_cast<long long>(hd);  // INT8 window end: the CTA folds the W entries
 }
 
-template <bool INT8, bool PER_KEY, bool COMP, bool SPLIT = false>
+template <bool INT8, bool PER_KEY, bool COMP, bool SPLIT, int REC>
 __global__ void __launch_bounds__(kThreads, 2) log_step_kernel(const StepArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ long long fold_hd[kWarps];
@@ -449,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 2) log_step_kernel(const StepArgs a)
     WarpSmem& ws = reinterpret_cast<WarpSmem*>(smem)[warp];
     if (lane == 0) ws.bar_live = 0u;
     __syncwarp();
-    if (row < a.batch * pv.H) hd = warp_step<INT8, PER_KEY, SPLIT>(a, ws, row, &lp);
+    if (row < a.batch * pv.H) hd = warp_step<INT8, PER_KEY, SPLIT, REC>(a, ws, row, &lp);
     if (lane == 0) {
         fold_hd[warp] = hd;
         fold_lb[warp] = lp;
@@ -565,46 +585,78 @@ cudaError_t set_smem(K kernel, size_t bytes) {
                                 static_cast<int>(bytes));
 }
 
+// The record formats a (variant, compensator) pair offers: bfloat16 keys
+// without compensator pairs; binary16 records for INT8 only.
+template <bool INT8, bool COMP, int REC>
+constexpr bool rec_valid() {
+    return REC == kRecFP32 || (REC == kRecBF16K && !COMP) || (REC == kRecFP16 && INT8);
+}
+
+template <bool INT8, bool COMP, bool SPLIT, int REC>
+cudaError_t prepare_rec() {
+    if constexpr (rec_valid<INT8, COMP, REC>()) {
+        cudaError_t e = set_smem(log_step_kernel<INT8, false, COMP, SPLIT, REC>, step_smem_bytes());
+        if (e != cudaSuccess) return e;
+        return set_smem(log_step_kernel<INT8, true, COMP, SPLIT, REC>, step_smem_bytes());
+    } else {
+        return cudaSuccess;
+    }
+}
+
+template <bool INT8, bool COMP, bool SPLIT>
+cudaError_t prepare_formats() {
+    cudaError_t e;
+    if ((e = prepare_rec<INT8, COMP, SPLIT, kRecFP32>()) != cudaSuccess) return e;
+    if ((e = prepare_rec<INT8, COMP, SPLIT, kRecBF16K>()) != cudaSuccess) return e;
+    return prepare_rec<INT8, COMP, SPLIT, kRecFP16>();
+}
+
+template <bool INT8, bool COMP, bool SPLIT, int REC>
+cudaError_t launch_rec(const StepArgs& a, bool per_key, dim3 grid, cudaStream_t s) {
+    if constexpr (rec_valid<INT8, COMP, REC>()) {
+        const size_t sm = step_smem_bytes();
+        return launch_dependent(per_key ? log_step_kernel<INT8, true, COMP, SPLIT, REC>
+                                        : log_step_kernel<INT8, false, COMP, SPLIT, REC>,
+                                grid, sm, s, a);
+    } else {
+        return cudaErrorInvalidValue;  // the descriptor checks exclude this format
+    }
+}
+
+// The step kernel of a pool: its record format picks the instantiation.
+template <bool INT8, bool COMP, bool SPLIT>
+cudaError_t launch_step_kernel(const StepArgs& a, bool per_key, dim3 grid, cudaStream_t s) {
+    if (a.pv.k16) return launch_rec<INT8, COMP, SPLIT, kRecBF16K>(a, per_key, grid, s);
+    if (a.pv.rec16) return launch_rec<INT8, COMP, SPLIT, kRecFP16>(a, per_key, grid, s);
+    return launch_rec<INT8, COMP, SPLIT, kRecFP32>(a, per_key, grid, s);
+}
+
 }  // namespace
 
 cudaError_t prepare_log_step_kernels() {
     cudaError_t e;
-    const size_t ls = step_smem_bytes();
-    if ((e = set_smem(log_step_kernel<false, false, false>, ls)) != cudaSuccess) return e;
-    if ((e = set_smem(log_step_kernel<false, true, false>, ls)) != cudaSuccess) return e;
-    if ((e = set_smem(log_step_kernel<true, false, false>, ls)) != cudaSuccess) return e;
-    if ((e = set_smem(log_step_kernel<true, true, false>, ls)) != cudaSuccess) return e;
-    if ((e = set_smem(log_step_kernel<true, false, true>, ls)) != cudaSuccess) return e;
-    if ((e = set_smem(log_step_kernel<true, true, true>, ls)) != cudaSuccess) return e;
-    if ((e = set_smem(log_step_kernel<false, false, false, true>, ls)) != cudaSuccess) return e;
-    if ((e = set_smem(log_step_kernel<false, true, false, true>, ls)) != cudaSuccess) return e;
-    if ((e = set_smem(log_step_kernel<true, false, false, true>, ls)) != cudaSuccess) return e;
-    if ((e = set_smem(log_step_kernel<true, true, false, true>, ls)) != cudaSuccess) return e;
-    if ((e = set_smem(log_step_kernel<true, false, true, true>, ls)) != cudaSuccess) return e;
-    return set_smem(log_step_kernel<true, true, true, true>, ls);
+    if ((e = prepare_formats<false, false, false>()) != cudaSuccess) return e;
+    if ((e = prepare_formats<true, false, false>()) != cudaSuccess) return e;
+    if ((e = prepare_formats<true, true, false>()) != cudaSuccess) return e;
+    if ((e = prepare_formats<false, false, true>()) != cudaSuccess) return e;
+    if ((e = prepare_formats<true, false, true>()) != cudaSuccess) return e;
+    return prepare_formats<true, true, true>();
 }
 
 cudaError_t launch_log_step(const StepArgs& a, bool int8, bool per_key, cudaStream_t s) {
     const int64_t rows = static_cast<int64_t>(a.batch) * a.pv.H;
     const dim3 grid(static_cast<unsigned>((rows + kWarps - 1) / kWarps));
-    const size_t sm = step_smem_bytes();
-    if (int8 && a.pv.R > 0)  // compensator pairs: the kernel that also fits them
-        return launch_dependent(per_key ? log_step_kernel<true, true, true> : log_step_kernel<true, false, true>,
-                                grid, sm, s, a);
-    if (int8) {
-        const cudaError_t e = launch_dependent(
-            per_key ? log_step_kernel<true, true, false> : log_step_kernel<true, false, false>, grid, sm, s, a);
-        if (e != cudaSuccess || a.pv.foldq == nullptr) return e;
-        return launch_window_fold(a.pv, per_key, s);
-    }
-    return launch_dependent(per_key ? log_step_kernel<false, true, false> : log_step_kernel<false, false, false>,
-                            grid, sm, s, a);
+    if (!int8) return launch_step_kernel<false, false, false>(a, per_key, grid, s);
+    if (a.pv.R > 0)  // compensator pairs: the kernel that also fits them
+        return launch_step_kernel<true, true, false>(a, per_key, grid, s);
+    const cudaError_t e = launch_step_kernel<true, false, false>(a, per_key, grid, s);
+    if (e != cudaSuccess || a.pv.foldq == nullptr) return e;
+    return launch_window_fold(a.pv, per_key, s);
 }
 
 cudaError_t launch_log_step_split(const StepArgs& a, bool int8, bool per_key, cudaStream_t s) {
     const int64_t rows = static_cast<int64_t>(a.batch) * a.pv.H;
     const dim3 grid(static_cast<unsigned>((rows + kWarps - 1) / kWarps));
-    const size_t sm = step_smem_bytes();
     cudaError_t e;
     if (int8)
         e = launch_dependent(per_key ? replay_prepare_kernel<true, true> : replay_prepare_kernel<true, false>,
@@ -613,20 +665,11 @@ cudaError_t launch_log_step_split(const StepArgs& a, bool int8, bool per_key, cu
         e = launch_dependent(per_key ? replay_prepare_kernel<false, true> : replay_prepare_kernel<false, false>,
                              grid, 0, s, a);
     if (e != cudaSuccess) return e;
-    if (int8 && a.pv.R > 0)
-        return launch_dependent(per_key ? log_step_kernel<true, true, true, true>
-                                        : log_step_kernel<true, false, true, true>,
-                                grid, sm, s, a);
-    if (int8) {
-        e = launch_dependent(per_key ? log_step_kernel<true, true, false, true>
-                                     : log_step_kernel<true, false, false, true>,
-                             grid, sm, s, a);
-        if (e != cudaSuccess || a.pv.foldq == nullptr) return e;
-        return launch_window_fold(a.pv, per_key, s);
-    }
-    return launch_dependent(per_key ? log_step_kernel<false, true, false, true>
-                                    : log_step_kernel<false, false, false, true>,
-                            grid, sm, s, a);
+    if (!int8) return launch_step_kernel<false, false, true>(a, per_key, grid, s);
+    if (a.pv.R > 0) return launch_step_kernel<true, true, true>(a, per_key, grid, s);
+    e = launch_step_kernel<true, false, true>(a, per_key, grid, s);
+    if (e != cudaSuccess || a.pv.foldq == nullptr) return e;
+    return launch_window_fold(a.pv, per_key, s);
 }
 
 }  // namespace ls
