@@ -253,3 +253,65 @@ def test_largest_window(variant):
         assert p.y_rel_l2() <= 2e-3
     else:
         assert p.y_err() <= 1e-4 and p.state_err() <= 1e-4
+
+
+@pytest.mark.parametrize("gate", ["scalar", "per_key"])
+@pytest.mark.parametrize("variant,window,fmt", [("deferred", 4, {}), ("int8", 4, {}),
+                                                ("int8", 3, {"r16": True}),
+                                                ("int8", 4, {"col_scales": True}),
+                                                ("int8", 5, {"compensators": 2})])
+def test_lifecycle_fuzz(gate, variant, window, fmt):
+    """Seeded random interleaving of decode calls on random slot subsets with
+    resets, loads and window commits of random slots: every slot has its own
+    window phase, the window-end queue (per-row INT8 scales) sees a different
+    subset at every call, and the lifecycle calls run between folds.  Each
+    call's outputs, the final logical states and the log lengths are compared
+    with the oracle driven through the same operations."""
+    oracle, H, StatePool, _, wl, _ = _mods()
+    P, Hh = 6, 2
+    w = wl.custom(gate=gate, batch=P, heads=Hh, num_slots=P, seed=23, lam_scale=0.3)
+    pool = StatePool(P, Hh, variant, gate, window, **fmt)
+    orc = H.make_oracle(variant, P * Hh, w.dl, window, **fmt)
+    rng = np.random.default_rng(7)
+    g = torch.Generator(device="cpu").manual_seed(3)
+    sidx = lambda s: (s[:, None] * Hh + np.arange(Hh)).reshape(-1)
+    worst, t = 0.0, 0
+    for op in range(48):
+        kind = rng.choice(["step"] * 6 + ["reset", "load", "commit"])
+        if kind == "step":
+            nb = int(rng.integers(1, P + 1))
+            slots = np.sort(rng.choice(P, nb, replace=False)).astype(np.int32)
+            ins = [x[:nb].contiguous() for x in _inputs(w, t, "cuda")]
+            t += 1
+            y = pool.decode_step(torch.as_tensor(slots, device="cuda"), *ins)
+            sub = wl.custom(gate=gate, batch=nb, heads=Hh, num_slots=P, seed=23)
+            yo = orc.step(sidx(slots), *H.host_inputs(ins, sub, np.arange(nb * Hh)))
+            yg = y.reshape(-1, D).double().cpu().numpy()
+            worst = max(worst, H.rel_l2(yg, yo) if variant == "int8" else H.relmax(yg, yo))
+            continue
+        n = int(rng.integers(1, 3))
+        slots = np.sort(rng.choice(P, n, replace=False)).astype(np.int32)
+        st = torch.as_tensor(slots, device="cuda")
+        if kind == "reset":
+            pool.reset(st)
+            orc.reset(sidx(slots))
+        elif kind == "load":
+            S = (torch.randn(n, Hh, D, D, generator=g) * 0.5).float()
+            pool.load(st, S.to("cuda"))
+            orc.load(sidx(slots), S.double().numpy().reshape(-1, D, D))
+        else:
+            pool.window_commit(st)
+            orc.commit(sidx(slots))
+    assert t > 0
+    assert worst <= (2e-3 if variant == "int8" else 1e-4), worst
+    S = pool.read(range(P)).reshape(-1, D, D).double().cpu().numpy()
+    So = orc.logical(np.arange(P * Hh))
+    if variant == "int8":
+        assert H.rel_l2(S, So) <= 2e-3
+    else:
+        assert H.relmax(S, So) <= 1e-4
+    ln, _ = pool.read_log_meta(range(P))
+    # compensator pools: the log holds the r pairs ahead of the window's tokens
+    cnt = orc.cnt + fmt.get("compensators", 0) if variant == "int8" else orc.L
+    assert np.array_equal(ln.cpu().numpy().reshape(-1), cnt)
+    assert pool.status() == 0
