@@ -464,10 +464,10 @@ def rwkv6(dev, peak, peak_kind, tokens=64):
 
 def e2e(w, variants, pools, slot_idx, dev, world=1, tokens=24):
     """The same step through ls_decode_step_host: inputs copied from pinned host
-    memory and y copied back inside the timed region, every call.  Pool p is
-    driven on stream p % 2 (the layer pools are independent), so one pool's
-    host copies overlap another pool's kernels; every pool has its own host
-    output buffer."""
+    memory and y copied back inside the timed region, every call.  Layer pool
+    p is driven on its own stream (the layer pools are independent), so one
+    pool's host copies overlap another pool's kernels; every pool has its own
+    host output buffer."""
     import torch
     from recurrent_state_quantization_gb300 import workloads as wl
     host = []
@@ -480,14 +480,14 @@ def e2e(w, variants, pools, slot_idx, dev, world=1, tokens=24):
     hslots = slot_idx.cpu().pin_memory()
     hy = {(n, p): torch.empty(w.batch, w.heads, w.d_v).pin_memory()
           for n, _ in variants for p in range(w.pools)}
-    streams = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
+    streams = [torch.cuda.Stream(device=dev) for _ in range(w.pools)]
     torch.cuda.synchronize()
 
     def step(t):
         for n, _ in variants:
             for p in range(w.pools):
                 pools[n][p].decode_step_host(hslots, *host[p][t % 4], hy[(n, p)],
-                                             stream=streams[p % 2])
+                                             stream=streams[p])
         for s in streams:
             s.synchronize()  # the step's results are on the host
 
@@ -505,8 +505,8 @@ def e2e(w, variants, pools, slot_idx, dev, world=1, tokens=24):
     return {"value": job_throughput(heads * calls * tokens, world, dt * 1e3), "unit": UNIT, "tokens": tokens,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "api": "ls_decode_step_host (pinned host buffers, cudaMemcpyAsync inside the "
-                   "library; layer pools alternate between two streams; the host synchronizes "
-                   "on every y every token)"}
+                   "library; one stream per layer pool; the host synchronizes on every y "
+                   "every token)"}
 
 
 def cpu_baseline(w, variants, budget_s=6.0, steps=None):
