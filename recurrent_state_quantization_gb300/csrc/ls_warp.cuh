@@ -383,7 +383,7 @@ constexpr int kFoldChunk = 16;
 struct FoldSmem {
     unsigned char* tile;  // tile_bytes(INT8)
     float2* a2;           // [kFoldChunk][kD] (a, a); kFoldStep: then partial sums
-    float4* u4;           // [kFoldChunk][kD / 4]
+    float4* u4;           // [kFoldChunk][kD / 4] U as FP32 (FP32 folds: the staged ru)
     float* es;            // [kD] exp(lb_i) (* s_i for INT8)
     float* lp;            // [kD] lb_i (per-key gate)
     float* kv;            // [kD] k, q, v, u of the token (kFoldStep)
@@ -391,21 +391,23 @@ struct FoldSmem {
     float* vv;
     float* uv;
     float* misc;          // [4] partial k.q
-    float4* rk;           // INT8: raw log chunk K [kFoldChunk][kD], U, Lambda
+    float4* rk;           // raw log chunk K [kFoldChunk][kD], U, Lambda
     float4* ru;           //   (per key row, or kFoldChunk scalars)
     float4* rl;
     uint64_t* bar;        // tile copies
-    uint64_t* lbar;       // INT8: log chunk copies
+    uint64_t* lbar;       // log chunk copies
 };
 
-// INT8 stages its log chunks by bulk copies too (room for them next to the
-// 16 KiB tile); FP32 loads them per thread.
-__host__ __device__ constexpr size_t fold_raw_bytes(bool int8) {
-    return int8 ? size_t(3) * kFoldChunk * kD * 4 : 0;
-}
+// Log chunks are staged by bulk copies next to the tile (K, U, Lambda of
+// kFoldChunk entries), one chunk ahead: the next chunk, or the next state's
+// first, is in flight while the current one is folded.
+__host__ __device__ constexpr size_t fold_raw_bytes(bool) { return size_t(3) * kFoldChunk * kD * 4; }
 
+// INT8 converts U into u4 (its records may be binary16); an FP32 fold reads
+// the staged U in place.
 __host__ __device__ constexpr size_t fold_smem_bytes(bool int8) {
-    return tile_bytes(int8) + size_t(kFoldChunk) * kD * 12 + 6 * kD * 4 + 16 + fold_raw_bytes(int8) + 16;
+    return tile_bytes(int8) + size_t(kFoldChunk) * kD * (int8 ? 12 : 8) + 6 * kD * 4 + 16 + fold_raw_bytes(int8) +
+           16;
 }
 
 __device__ __forceinline__ FoldSmem fold_smem(unsigned char* base, bool int8) {
@@ -415,8 +417,11 @@ __device__ __forceinline__ FoldSmem fold_smem(unsigned char* base, bool int8) {
     p += tile_bytes(int8);
     f.a2 = reinterpret_cast<float2*>(p);
     p += size_t(kFoldChunk) * kD * 8;
-    f.u4 = reinterpret_cast<float4*>(p);
-    p += size_t(kFoldChunk) * kD * 4;
+    f.u4 = nullptr;
+    if (int8) {
+        f.u4 = reinterpret_cast<float4*>(p);
+        p += size_t(kFoldChunk) * kD * 4;
+    }
     float* v = reinterpret_cast<float*>(p);
     f.es = v;
     f.lp = v + kD;
@@ -429,6 +434,7 @@ __device__ __forceinline__ FoldSmem fold_smem(unsigned char* base, bool int8) {
     f.rk = reinterpret_cast<float4*>(p);
     f.ru = f.rk + kFoldChunk * (kD / 4);
     f.rl = f.ru + kFoldChunk * (kD / 4);
+    if (!int8) f.u4 = f.ru;  // FP32 records: U is used where it was staged
     p += fold_raw_bytes(int8);
     f.bar = reinterpret_cast<uint64_t*>(p);
     f.lbar = f.bar + 1;
@@ -493,12 +499,10 @@ __device__ bool fold_cta(const PoolView& pv, size_t hd, int n, const float* lbg,
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) {
         if (!pp.tile_issued) fold_issue_tile<INT8>(pv, hd, fs);
-        if constexpr (INT8) {
-            if (!pp.log_issued && n > 0) fold_issue_log<PER_KEY>(pv, hd, 0, min(kFoldChunk, n), fs);
-        }
+        if (!pp.log_issued && n > 0) fold_issue_log<PER_KEY>(pv, hd, 0, min(kFoldChunk, n), fs);
     }
     pp.tile_issued = false;
-    const bool log_in_flight = INT8 && n > 0;  // this state's first chunk
+    const bool log_in_flight = n > 0;  // this state's first chunk
     pp.log_issued = false;
     // decay (and INT8 scale) of every key row, once per CTA (a scalar-gate
     // FP32 fold needs one value only); the token's vectors for kFoldStep
@@ -587,57 +591,58 @@ __device__ bool fold_cta(const PoolView& pv, size_t hd, int n, const float* lbg,
         pp.tile_issued = true;
     }
     // + sum_l exp(lb - Lam_l) K_l U_l^T, kFoldChunk entries at a time
-    const size_t kb = hd * static_cast<size_t>(pv.cap);
-    const size_t lb0 = hd * static_cast<size_t>(pv.lam_stride);
 #pragma unroll 1
     for (int c0 = 0; c0 < n; c0 += kFoldChunk) {
         const int nl = min(kFoldChunk, n - c0);
         __syncthreads();  // the previous chunk is consumed
+        // raw chunk (bulk copies) -> (a, a) pairs (and, INT8, U as FP32); then
+        // the next chunk, or the next state's first one, is staged behind it:
+        // INT8 right away, FP32 (whose U is read in place) after the updates
+        const bool lok = mbar_wait_bounded(fs.lbar, pp.log_phase);
+        if (__syncthreads_or(!lok)) {
+            if (tid == 0) {
+                flag_status(pv.status, kDevTimeout);
+                mbar_wait_bounded(fs.lbar, pp.log_phase);
+                if (pp.tile_issued) mbar_wait_bounded(fs.bar, pp.tile_phase);
+            }
+            __syncthreads();
+            pp.tile_issued = false;
+            return false;
+        }
+        pp.log_phase ^= 1u;
+        // (entry, key-row pair) items: each lane stores one float4 of
+        // (a, a) pairs, consecutive lanes consecutive addresses
+        for (int idx = tid; idx < nl * (kD / 2); idx += kThreads) {
+            const int l = idx >> 6, p = idx & 63;
+            float2 K2;
+            if (pv.k16) {
+                const uint32_t w = reinterpret_cast<const uint32_t*>(fs.rk)[idx];
+                K2 = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+            } else if (INT8 && pv.rec16) {
+                K2 = __half22float2(reinterpret_cast<const __half2*>(fs.rk)[idx]);
+            } else {
+                K2 = reinterpret_cast<const float2*>(fs.rk)[idx];
+            }
+            float2 g;
+            if constexpr (PER_KEY) {
+                const float2 lm = reinterpret_cast<const float2*>(fs.rl)[idx];
+                const float2 lb2 = reinterpret_cast<const float2*>(fs.lp)[p];
+                g = make_float2(expf(lb2.x - lm.x), expf(lb2.y - lm.y));
+            } else {
+                const float gg = expf(lb_scalar - reinterpret_cast<const float*>(fs.rl)[l]);
+                g = make_float2(gg, gg);
+            }
+            const float a0 = g.x * K2.x, a1 = g.y * K2.y;
+            reinterpret_cast<float4*>(fs.a2)[idx] = make_float4(a0, a0, a1, a1);
+        }
         if constexpr (INT8) {
-            // raw chunk (bulk copies) -> (a, a) pairs and U; then the next
-            // chunk, or the next state's first one, is staged behind it
-            const bool lok = mbar_wait_bounded(fs.lbar, pp.log_phase);
-            if (__syncthreads_or(!lok)) {
-                if (tid == 0) {
-                    flag_status(pv.status, kDevTimeout);
-                    mbar_wait_bounded(fs.lbar, pp.log_phase);
-                    if (pp.tile_issued) mbar_wait_bounded(fs.bar, pp.tile_phase);
-                }
-                __syncthreads();
-                pp.tile_issued = false;
-                return false;
-            }
-            pp.log_phase ^= 1u;
-            // (entry, key-row pair) items: each lane stores one float4 of
-            // (a, a) pairs, consecutive lanes consecutive addresses
-            for (int idx = tid; idx < nl * (kD / 2); idx += kThreads) {
-                const int l = idx >> 6, p = idx & 63;
-                float2 K2;
-                if (pv.k16) {
-                    const uint32_t w = reinterpret_cast<const uint32_t*>(fs.rk)[idx];
-                    K2 = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-                } else if (pv.rec16) {
-                    K2 = __half22float2(reinterpret_cast<const __half2*>(fs.rk)[idx]);
-                } else {
-                    K2 = reinterpret_cast<const float2*>(fs.rk)[idx];
-                }
-                float2 g;
-                if constexpr (PER_KEY) {
-                    const float2 lm = reinterpret_cast<const float2*>(fs.rl)[idx];
-                    const float2 lb2 = reinterpret_cast<const float2*>(fs.lp)[p];
-                    g = make_float2(expf(lb2.x - lm.x), expf(lb2.y - lm.y));
-                } else {
-                    const float gg = expf(lb_scalar - reinterpret_cast<const float*>(fs.rl)[l]);
-                    g = make_float2(gg, gg);
-                }
-                const float a0 = g.x * K2.x, a1 = g.y * K2.y;
-                reinterpret_cast<float4*>(fs.a2)[idx] = make_float4(a0, a0, a1, a1);
-            }
             for (int idx = tid; idx < nl * (kD / 4); idx += kThreads)
                 fs.u4[idx] = val4_at(fs.ru, static_cast<size_t>(idx) * 4, pv);
-            __syncthreads();
-            const bool more = c0 + kFoldChunk < n;
-            const bool next = !more && next_hd >= 0 && next_n > 0;
+        }
+        __syncthreads();
+        const bool more = c0 + kFoldChunk < n;
+        const bool next = !more && next_hd >= 0 && next_n > 0;
+        if constexpr (INT8) {
             if (tid == 0) {
                 if (more)
                     fold_issue_log<PER_KEY>(pv, hd, c0 + kFoldChunk, min(kFoldChunk, n - c0 - kFoldChunk), fs);
@@ -645,29 +650,6 @@ __device__ bool fold_cta(const PoolView& pv, size_t hd, int n, const float* lbg,
                     fold_issue_log<PER_KEY>(pv, static_cast<size_t>(next_hd), 0, min(kFoldChunk, next_n), fs);
             }
             pp.log_issued = next;
-        } else {
-            for (int idx = tid; idx < nl * (kD / 4); idx += kThreads) {
-                const int l = idx >> 5, q = idx & 31;  // entry, 4-row / 4-column group
-                const size_t eo = (kb + c0 + l) * kD + 4 * q;
-                const float4 K4 = pv.k16 ? bf16x4_to_float4(__ldcg(reinterpret_cast<const uint2*>(pv.klog) + (eo >> 2)))
-                                         : ldcg4(pv.klog + eo);
-                fs.u4[l * (kD / 4) + q] = ldcg4(pv.ulog + eo);
-                float4 g;
-                if constexpr (PER_KEY) {
-                    const float4 lm = ldcg4(pv.lamlog + lb0 + static_cast<size_t>(c0 + l) * kD + 4 * q);
-                    const float4 lb4 = reinterpret_cast<const float4*>(fs.lp)[q];
-                    g = make_float4(expf(lb4.x - lm.x), expf(lb4.y - lm.y), expf(lb4.z - lm.z),
-                                    expf(lb4.w - lm.w));
-                } else {
-                    const float gg = expf(lb_scalar - __ldcg(pv.lamlog + lb0 + c0 + l));
-                    g = make_float4(gg, gg, gg, gg);
-                }
-                float4* a2 = reinterpret_cast<float4*>(fs.a2 + l * kD + 4 * q);
-                const float ax = g.x * K4.x, ay = g.y * K4.y, az = g.z * K4.z, aw = g.w * K4.w;
-                a2[0] = make_float4(ax, ax, ay, ay);
-                a2[1] = make_float4(az, az, aw, aw);
-            }
-            __syncthreads();
         }
 #pragma unroll 2
         for (int l = 0; l < nl; ++l) {
@@ -683,6 +665,16 @@ __device__ bool fold_cta(const PoolView& pv, size_t hd, int n, const float* lbg,
                 lo[2 * r2 + 1] = __ffma2_rn(a1, u01, lo[2 * r2 + 1]);
                 hi[2 * r2 + 1] = __ffma2_rn(a1, u23, hi[2 * r2 + 1]);
             }
+        }
+        if constexpr (!INT8) {
+            __syncthreads();  // the staged U is consumed
+            if (tid == 0) {
+                if (more)
+                    fold_issue_log<PER_KEY>(pv, hd, c0 + kFoldChunk, min(kFoldChunk, n - c0 - kFoldChunk), fs);
+                else if (next)
+                    fold_issue_log<PER_KEY>(pv, static_cast<size_t>(next_hd), 0, min(kFoldChunk, next_n), fs);
+            }
+            pp.log_issued = next;
         }
     }
     if constexpr (MODE == kFoldStep) {
