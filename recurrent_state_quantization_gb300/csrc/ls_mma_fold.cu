@@ -33,10 +33,11 @@
 // tensor-memory columns and commits them to the group's mbarrier, and the
 // copies of the next state start as soon as the MMAs have read the operands.
 // The epilogue runs on the CUDA cores: thread t of a group owns value column
-// j = t (the tensor-memory lanes its warp may read) for all 128 key rows.  The INT8 words of a state hold 4 key rows of one
-// value column, so each thread reads and writes 32 whole words and a warp
-// 128 contiguous bytes per access; a key row's absmax over a warp's 32
-// columns is one redux.sync, over the group's 4 warps a shared-memory max.
+// j = t (the tensor-memory lanes its warp may read) for all 128 key rows.
+// The INT8 words of a state hold 4 key rows of one value column, so each
+// thread reads and writes 32 whole words and a warp 128 contiguous bytes per
+// access; a key row's absmax over a warp's 32 columns is one redux.sync, over
+// the group's 4 warps a shared-memory max.
 // S goes back to tensor memory between the absmax pass and the quantization
 // pass, so no thread holds more than 32 of its 128 values.
 //
@@ -55,7 +56,6 @@
 namespace ls {
 
 namespace {
-
 
 constexpr int kGroups = 4;
 constexpr int kGroupThreads = 128;
@@ -85,6 +85,7 @@ struct alignas(128) GroupSmem {
 };
 
 constexpr size_t window_fold_smem_bytes() { return kGroups * sizeof(GroupSmem); }
+static_assert(window_fold_smem_bytes() <= 232448, "the four groups fit one CTA's shared memory (227 KiB)");
 
 // K-major core-matrix offset of records 4q..4q+3 of operand row `row`
 // (8-row groups 512 B apart, 4-record groups 128 B apart).
