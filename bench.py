@@ -315,6 +315,7 @@ def run_native(args, rank, world, local):
                                                 peak_kind, pools["eager"])
         out["e2e"] = e2e(w, variants, pools, slot_idx, dev, world)
         out["rwkv6"] = rwkv6(dev, hbm_peak, peak_kind)
+        out["kda"] = kda(dev, hbm_peak, peak_kind)
         out["split_replay_ablation"] = split_ablation(dev)
         if rank == 0:
             out["cpu_baseline"] = cpu_baseline(w, variants, budget_s=6.0)
@@ -455,6 +456,45 @@ def rwkv6(dev, peak, peak_kind, tokens=64):
         byt = bm.variant_bytes(variant, "per_key", M or 1)
         gbs = byt * hs / (ms * 1e-3) / 1e9
         out[variant] = {"window": M or None, "head_steps_per_s": hs / (ms * 1e-3),
+                        "algorithmic_bytes_per_head_step": byt, "achieved_gbs": gbs,
+                        "frac_of_" + peak_kind + "_hbm": gbs / peak}
+        del pool
+    torch.cuda.empty_cache()
+    return out
+
+
+def kda(dev, peak, peak_kind, tokens=64):
+    """The KDA workload (per-key gate with 10 % long-lived channels, 128
+    requests x 32 heads, one pool of 256 MB FP32 states): eager, deferred
+    (M = 16) and INT8 (W = 32) head-steps/s and algorithmic GB/s over two INT8
+    windows, states warmed by one window."""
+    import torch
+    from recurrent_state_quantization_gb300 import StatePool
+    from recurrent_state_quantization_gb300 import bytemodel as bm
+    from recurrent_state_quantization_gb300 import workloads as wl
+    w = wl.WORKLOAD_BY_NAME["kda_b128_h32_t512_longlived"]
+    slots = wl.slot_index(w, dev)
+    masks = wl.static_masks(w, dev)
+    ins = [wl.step_inputs(w, t, device=dev, masks=masks) for t in range(16)]
+    stream = torch.cuda.current_stream()
+    out = {"workload": w.name, "gate": "per_key (KDA)"}
+    for variant, W in (("eager", 0), ("deferred", 16), ("int8", 32)):
+        pool = StatePool(w.num_slots, w.heads, variant, w.gate, W, device=dev)
+        y = torch.empty(w.batch, w.heads, w.d_v, device=dev)
+        for t in range(32):
+            pool.decode_step(slots, *ins[t % 16], y=y)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for t in range(tokens):
+            pool.decode_step(slots, *ins[t % 16], y=y)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b)
+        hs = w.batch * w.heads * tokens
+        byt = bm.variant_bytes(variant, "per_key", W or 1)
+        gbs = byt * hs / (ms * 1e-3) / 1e9
+        out[variant] = {"window": W or None, "head_steps_per_s": hs / (ms * 1e-3),
                         "algorithmic_bytes_per_head_step": byt, "achieved_gbs": gbs,
                         "frac_of_" + peak_kind + "_hbm": gbs / peak}
         del pool
