@@ -2,10 +2,10 @@
 close the deferred FP32 trajectory stays to the eager one, per 1024-token
 block, on the GPU (every head) and in the oracle (sampled heads).
 
-Five pools (eager, deferred with the workload's merge interval, INT8 with
+Six pools (eager, deferred with the workload's merge interval, INT8 with
 window W in the per-key-row format, in the smoothed per-value-column format,
-and in that format with 4 Compensator Tokens) and their oracles run the same
-seeded tokens, free-running (no restarts).  At the end of every block:
+in that format with 4 Compensator Tokens, and per-key-row with FP16 records)
+and their oracles run the same seeded tokens, free-running (no restarts).  At the end of every block:
 
 - state: ||S_int8 - S_fp32||_F / ||S_fp32||_F over the logical states
   (ls_pool_read), S_fp32 the eager trajectory;
@@ -81,15 +81,17 @@ def test_drift_report(wi, window, n_sample):
     pi = H.Pair(w, "int8", window, n_sample=n_sample)
     pc = H.Pair(w, "int8", window, n_sample=n_sample, col_scales=True)
     pk = H.Pair(w, "int8", window, n_sample=n_sample, col_scales=True, compensators=4)
+    pr = H.Pair(w, "int8", window, n_sample=n_sample, r16=True)
     all_slots = torch.arange(w.num_slots, dtype=torch.int32, device=pe.dev)
     blocks = []
     run = {k: 0.0 for k in ("g_s_num", "g_s_den", "o_s_num", "o_s_den", "g_y_num", "g_y_den",
-                            "o_y_num", "o_y_den", "gc_s_num", "oc_s_num", "gk_s_num", "ok_s_num")}
+                            "o_y_num", "o_y_den", "gc_s_num", "oc_s_num", "gk_s_num", "ok_s_num",
+                            "gr_s_num", "or_s_num")}
     acc = None
     for t in range(w.tokens):
         if acc is None:
             acc = {k: 0.0 for k in ("gy_num", "gy_den", "gys_num", "oy_num", "oy_den",
-                                    "gcy_num", "ocy_num", "gky_num", "oky_num")}
+                                    "gcy_num", "ocy_num", "gky_num", "oky_num", "gry_num", "ory_num")}
             acc["gdy"], acc["ody"] = _HeadMax(), _HeadMax()
         ye, yoe = pe.step(t)
         yd, yod = pd.step(t)
@@ -100,6 +102,9 @@ def test_drift_report(wi, window, n_sample):
         yk, yok = pk.step(t)
         acc["gky_num"] += float(((yk - ye) ** 2).sum())
         acc["oky_num"] += float(((yok - yoe) ** 2).sum())
+        yr, yor = pr.step(t)
+        acc["gry_num"] += float(((yr - ye) ** 2).sum())
+        acc["ory_num"] += float(((yor - yoe) ** 2).sum())
         acc["gy_num"] += float(((yi - ye) ** 2).sum())
         acc["gy_den"] += float((ye ** 2).sum())
         rows = torch.as_tensor(pi.sample.rows, device=pi.dev)
@@ -116,6 +121,7 @@ def test_drift_report(wi, window, n_sample):
             Si = pi.pool.read(all_slots)
             Sc = pc.pool.read(all_slots)
             Sk = pk.pool.read(all_slots)
+            Sr = pr.pool.read(all_slots)
             g_s = float((Si - Se).norm() / Se.norm())
             g_d = _head_relmax(Sd.reshape(-1, 128, 128), Se.reshape(-1, 128, 128))
             gse, gsi = _rows_view(Se, pe), _rows_view(Si, pi)
@@ -124,6 +130,8 @@ def test_drift_report(wi, window, n_sample):
             oi = pi.orc.logical(pi.sample.state_idx)
             oc = pc.orc.logical(pc.sample.state_idx)
             ok = pk.orc.logical(pk.sample.state_idx)
+            orr = pr.orc.logical(pr.sample.state_idx)
+            gsr = _rows_view(Sr, pr)
             gsc = _rows_view(Sc, pc)
             gsk = _rows_view(Sk, pk)
             o_s = H.rel_l2(oi, oe)
@@ -137,7 +145,9 @@ def test_drift_report(wi, window, n_sample):
                            "state_int8_smoothed_vs_fp32": float((Sc - Se).norm() / Se.norm()),
                            "y_int8_smoothed_vs_fp32": (acc["gcy_num"] / acc["gy_den"]) ** 0.5,
                            "state_int8_comp_vs_fp32": float((Sk - Se).norm() / Se.norm()),
-                           "y_int8_comp_vs_fp32": (acc["gky_num"] / acc["gy_den"]) ** 0.5},
+                           "y_int8_comp_vs_fp32": (acc["gky_num"] / acc["gy_den"]) ** 0.5,
+                           "state_int8_fp16rec_vs_fp32": float((Sr - Se).norm() / Se.norm()),
+                           "y_int8_fp16rec_vs_fp32": (acc["gry_num"] / acc["gy_den"]) ** 0.5},
                    "oracle": {"state_int8_vs_fp32": o_s,
                               "y_int8_vs_fp32": (acc["oy_num"] / acc["oy_den"]) ** 0.5,
                               "deferred_vs_eager_state_relmax": o_d,
@@ -145,7 +155,9 @@ def test_drift_report(wi, window, n_sample):
                               "state_int8_smoothed_vs_fp32": H.rel_l2(oc, oe),
                               "y_int8_smoothed_vs_fp32": (acc["ocy_num"] / acc["oy_den"]) ** 0.5,
                               "state_int8_comp_vs_fp32": H.rel_l2(ok, oe),
-                              "y_int8_comp_vs_fp32": (acc["oky_num"] / acc["oy_den"]) ** 0.5}}
+                              "y_int8_comp_vs_fp32": (acc["oky_num"] / acc["oy_den"]) ** 0.5,
+                              "state_int8_fp16rec_vs_fp32": H.rel_l2(orr, oe),
+                              "y_int8_fp16rec_vs_fp32": (acc["ory_num"] / acc["oy_den"]) ** 0.5}}
             blocks.append(blk)
             run["g_s_num"] += float(((gsi - gse) ** 2).sum())
             run["g_s_den"] += float((gse ** 2).sum())
@@ -156,13 +168,15 @@ def test_drift_report(wi, window, n_sample):
             run["oc_s_num"] += float(((oc - oe) ** 2).sum())
             run["gk_s_num"] += float(((gsk - gse) ** 2).sum())
             run["ok_s_num"] += float(((ok - oe) ** 2).sum())
+            run["gr_s_num"] += float(((gsr - gse) ** 2).sum())
+            run["or_s_num"] += float(((orr - oe) ** 2).sum())
             run["o_y_num"] += acc["oy_num"]
             run["o_y_den"] += acc["oy_den"]
             acc = None
     report = {"workload": w.name, "int8_window": window, "deferred_merge_interval": w.merge_interval,
               "sampled_heads": int(len(pi.sample.rows)), "blocks": blocks}
     print("drift-report " + json.dumps(report))
-    for p in (pe, pd, pi, pc, pk):
+    for p in (pe, pd, pi, pc, pk, pr):
         assert p.pool.status() == 0
     # deferred FP32 stays on the eager trajectory (both are FP32 recurrences
     # of the same state), on the GPU and in the oracle
@@ -184,3 +198,6 @@ def test_drift_report(wi, window, n_sample):
     gk_s = (run["gk_s_num"] / run["g_s_den"]) ** 0.5
     ok_s = (run["ok_s_num"] / run["o_s_den"]) ** 0.5
     assert gk_s <= 1.25 * ok_s + 1e-6, (gk_s, ok_s)
+    gr_s = (run["gr_s_num"] / run["g_s_den"]) ** 0.5
+    or_s = (run["or_s_num"] / run["o_s_den"]) ** 0.5
+    assert gr_s <= 1.25 * or_s + 1e-6, (gr_s, or_s)
