@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define LS_ABI_VERSION 4
+#define LS_ABI_VERSION 5
 
 /* status codes */
 #define LS_OK 0
@@ -70,6 +70,8 @@ extern "C" {
 #define LS_DEV_TIMEOUT 2    /* a bounded wait on an asynchronous copy gave up  */
 #define LS_DEV_BAD_STATE 4  /* a state's log length was out of range (its pool
                                memory was overwritten); the state was skipped */
+#define LS_DEV_SLOT_DUP 8   /* a slot list held one slot more than once
+                               (pools created with LS_CHECK_SLOTS)            */
 
 typedef struct ls_pool ls_pool; /* opaque host handle */
 
@@ -147,6 +149,19 @@ typedef enum {
  * 1028.  Values beyond the binary16 range become infinite (not checked).
  */
 #define LS_INT8_FP16_RECORDS (1u << 14)
+
+/*
+ * ls_pool_desc.flags: LS_CHECK_SLOTS (every variant): a checking mode for
+ * callers.  Every call that changes states -- the decode steps,
+ * ls_pool_load, ls_pool_reset_slots, ls_window_commit of a log variant --
+ * first checks on the device that its slot list names no slot twice: one
+ * extra launch of one CTA, which counts each slot in a per-slot array of the
+ * pool, tests the counts and clears them.  A repeated slot sets
+ * LS_DEV_SLOT_DUP in the status word (ls_pool_status).  The call itself
+ * still runs, so the states of a repeated slot are then undefined, as
+ * without the flag.  The pool holds 4 more bytes per slot.
+ */
+#define LS_CHECK_SLOTS (1u << 15)
 #define LS_INT8_COMPENSATORS(r) ((uint32_t)(r) << 8)
 
 typedef struct {

@@ -20,6 +20,7 @@ LS_ERR_SIZE = -5
 LS_DEV_SLOT_RANGE = 1
 LS_DEV_TIMEOUT = 2
 LS_DEV_BAD_STATE = 4
+LS_DEV_SLOT_DUP = 8
 
 LS_EAGER_FP32 = 0
 LS_DEFERRED_FP32 = 1
@@ -34,12 +35,13 @@ LS_MAX_COMPENSATORS = 8
 LS_PLAIN_UPDATE = 1 << 12
 LS_LOG_BF16_K = 1 << 13
 LS_INT8_FP16_RECORDS = 1 << 14
+LS_CHECK_SLOTS = 1 << 15
 LS_SPLIT_STATIC_SCRATCH_BYTES = 16 << 20
 
 
 def LS_INT8_COMPENSATORS(r: int) -> int:
     return int(r) << 8
-LS_ABI_VERSION = 4  # the include/ls.h these prototypes follow
+LS_ABI_VERSION = 5  # the include/ls.h these prototypes follow
 
 # Every symbol include/ls.h declares.
 EXPORTS = (

@@ -29,7 +29,7 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 bool is_log_variant(int32_t v) { return v == LS_DEFERRED_FP32 || v == LS_WINDOW_INT8; }
 
 struct Layout {
-    size_t status, base, scale, colf, lbar, len, klog, ulog, lamlog, foldq, total;
+    size_t status, base, scale, colf, lbar, len, klog, ulog, lamlog, foldq, mark, total;
 };
 
 // INT8 pools with per-row scales and no compensator pairs close their windows
@@ -44,7 +44,8 @@ int make_layout(const ls_pool_desc* d, Layout* L) {
     if (d == nullptr || L == nullptr) return LS_ERR_INVALID;
     if (d->variant < LS_EAGER_FP32 || d->variant > LS_WINDOW_INT8) return LS_ERR_INVALID;
     const uint32_t int8_flags = LS_INT8_COLUMN_SCALES | LS_INT8_COMPENSATORS(15);
-    if ((d->flags & ~(int8_flags | LS_PLAIN_UPDATE | LS_LOG_BF16_K | LS_INT8_FP16_RECORDS)) != 0)
+    if ((d->flags & ~(int8_flags | LS_PLAIN_UPDATE | LS_LOG_BF16_K | LS_INT8_FP16_RECORDS |
+                      LS_CHECK_SLOTS)) != 0)
         return LS_ERR_INVALID;
     if ((d->flags & LS_INT8_FP16_RECORDS) &&
         (d->variant != LS_WINDOW_INT8 || (d->flags & LS_LOG_BF16_K)))
@@ -91,6 +92,9 @@ int make_layout(const ls_pool_desc* d, Layout* L) {
     // window-end queue of the tensor-core fold (INT8, per-row scales, no pairs)
     L->foldq = off;
     off = align_up(off + (int8_mma_fold(d) ? 16 + nh * 4 : 0));
+    // per-slot counts of the duplicate-slot check
+    L->mark = off;
+    off = align_up(off + ((d->flags & LS_CHECK_SLOTS) ? static_cast<size_t>(d->num_slots) * 4 : 0));
     L->total = off;
     return LS_OK;
 }
@@ -119,6 +123,7 @@ ls::PoolView make_view(const ls_pool_desc& d, const Layout& L, unsigned char* m)
     v.lam_stride = d.gate == LS_GATE_PER_KEY ? v.cap * kD : (v.cap + 3) / 4 * 4;
     v.foldq = int8_mma_fold(&d) ? reinterpret_cast<int32_t*>(m + L.foldq) : nullptr;
     v.fold_grid = 1;
+    v.mark = (d.flags & LS_CHECK_SLOTS) ? reinterpret_cast<int32_t*>(m + L.mark) : nullptr;
     return v;
 }
 
@@ -145,6 +150,13 @@ int check_slot_list(const ls_pool* p, const int32_t* d_slots, int32_t n) {
     if (!aligned(d_slots, 4)) return LS_ERR_ALIGN;
     if (n > p->desc.num_slots) return LS_ERR_SLOT;
     return LS_OK;
+}
+
+// LS_CHECK_SLOTS: the device check of a slot list for repeats, launched
+// before the call that uses it.
+int check_distinct(const ls_pool* p, const int32_t* d_slots, int32_t n, void* stream) {
+    if (p->view.mark == nullptr) return LS_OK;
+    return cuda_status(ls::launch_slot_check(p->view, d_slots, n, static_cast<cudaStream_t>(stream)));
 }
 
 ls::AuxArgs aux_args(const ls_pool* p, const int32_t* d_slots, int32_t n) {
@@ -269,6 +281,7 @@ int ls_pool_load(ls_pool* pool, const int32_t* d_slots, int32_t n, const float* 
     if (rc != LS_OK || n == 0) return rc;
     if (d_state == nullptr) return LS_ERR_INVALID;
     if (!aligned(d_state, 16)) return LS_ERR_ALIGN;
+    if ((rc = check_distinct(pool, d_slots, n, stream)) != LS_OK) return rc;
     ls::AuxArgs a = aux_args(pool, d_slots, n);
     a.state_in = d_state;
     return cuda_status(ls::launch_load(a, pool->desc.variant == LS_WINDOW_INT8,
@@ -279,6 +292,7 @@ int ls_pool_load(ls_pool* pool, const int32_t* d_slots, int32_t n, const float* 
 int ls_pool_reset_slots(ls_pool* pool, const int32_t* d_slots, int32_t n, void* stream) {
     int rc = check_slot_list(pool, d_slots, n);
     if (rc != LS_OK || n == 0) return rc;
+    if ((rc = check_distinct(pool, d_slots, n, stream)) != LS_OK) return rc;
     return cuda_status(ls::launch_reset(aux_args(pool, d_slots, n),
                                         pool->desc.variant == LS_WINDOW_INT8,
                                         is_log_variant(pool->desc.variant),
@@ -289,8 +303,9 @@ int ls_decode_step(ls_pool* pool, const int32_t* d_slot_idx, int32_t batch, cons
                    const float* k, const float* v, const float* log_decay, const float* beta,
                    float* y, void* stream) {
     ls::StepArgs a{};
-    const int rc = step_args(pool, d_slot_idx, batch, q, k, v, log_decay, beta, y, &a);
+    int rc = step_args(pool, d_slot_idx, batch, q, k, v, log_decay, beta, y, &a);
     if (rc != LS_OK || batch == 0) return rc;
+    if ((rc = check_distinct(pool, d_slot_idx, batch, stream)) != LS_OK) return rc;
     return launch_step(pool, a, static_cast<cudaStream_t>(stream));
 }
 
@@ -305,13 +320,14 @@ int ls_decode_step_split(ls_pool* pool, const int32_t* d_slot_idx, int32_t batch
                          const float* k, const float* v, const float* log_decay, const float* beta,
                          float* y, void* d_scratch, size_t scratch_bytes, void* stream) {
     ls::StepArgs a{};
-    const int rc = step_args(pool, d_slot_idx, batch, q, k, v, log_decay, beta, y, &a);
+    int rc = step_args(pool, d_slot_idx, batch, q, k, v, log_decay, beta, y, &a);
     if (rc != LS_OK || batch == 0) return rc;
     if (!is_log_variant(pool->desc.variant) || d_scratch == nullptr) return LS_ERR_INVALID;
     if (!aligned(d_scratch, 16)) return LS_ERR_ALIGN;
     size_t need = 0;
     ls_split_scratch_bytes(pool, batch, &need);
     if (scratch_bytes < need) return LS_ERR_SIZE;
+    if ((rc = check_distinct(pool, d_slot_idx, batch, stream)) != LS_OK) return rc;
     a.coef = static_cast<float2*>(d_scratch);
     a.cstride = split_stride(pool);
     return cuda_status(ls::launch_log_step_split(a, pool->desc.variant == LS_WINDOW_INT8,
@@ -385,6 +401,7 @@ int ls_window_commit(ls_pool* pool, const int32_t* d_slots, int32_t n, void* str
     if (rc != LS_OK || n == 0) return rc;
     const ls_pool_desc& d = pool->desc;
     if (!is_log_variant(d.variant)) return LS_OK;  // eager: always materialized
+    if ((rc = check_distinct(pool, d_slots, n, stream)) != LS_OK) return rc;
     return cuda_status(ls::launch_fold(aux_args(pool, d_slots, n), d.variant == LS_WINDOW_INT8,
                                        d.gate == LS_GATE_PER_KEY, true,
                                        static_cast<cudaStream_t>(stream)));

@@ -345,6 +345,32 @@ cudaError_t launch_read_comp(const AuxArgs& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// LS_CHECK_SLOTS: one CTA counts every in-range slot of a slot list in
+// pv.mark, flags a count above one, and clears the counts for the next call.
+// Slots out of range are left to the call that follows, which flags them.
+__global__ void __launch_bounds__(1024) slot_check_kernel(const PoolView pv, const int32_t* slots, int32_t n) {
+    for (int b = threadIdx.x; b < n; b += blockDim.x) {
+        const int s = __ldg(slots + b);
+        if (s >= 0 && s < pv.P) atomicAdd(pv.mark + s, 1);
+    }
+    __syncthreads();
+    bool dup = false;
+    for (int b = threadIdx.x; b < n; b += blockDim.x) {
+        const int s = __ldg(slots + b);
+        if (s >= 0 && s < pv.P && __ldcg(pv.mark + s) > 1) dup = true;
+    }
+    if (__syncthreads_or(dup) && threadIdx.x == 0) flag_status(pv.status, kDevSlotDup);
+    for (int b = threadIdx.x; b < n; b += blockDim.x) {
+        const int s = __ldg(slots + b);
+        if (s >= 0 && s < pv.P) pv.mark[s] = 0;
+    }
+}
+
+cudaError_t launch_slot_check(const PoolView& pv, const int32_t* slots, int32_t n, cudaStream_t s) {
+    slot_check_kernel<<<1, 1024, 0, s>>>(pv, slots, n);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_read_log_meta(const AuxArgs& a, cudaStream_t s) {
     const dim3 grid(static_cast<unsigned>(a.n) * static_cast<unsigned>(a.pv.H));
     read_log_meta_kernel<<<grid, 128, 0, s>>>(a);

@@ -20,6 +20,7 @@ constexpr int kSplitEntries = 6;  // split replay: log entries per streamed chun
 constexpr int32_t kDevSlotRange = 1;
 constexpr int32_t kDevTimeout = 2;
 constexpr int32_t kDevBadState = 4;
+constexpr int32_t kDevSlotDup = 8;
 
 // Device pointers into one pool (caller-owned memory).  "hd" below is the
 // state index slot * H + h.
@@ -63,6 +64,8 @@ struct PoolView {
                            //   [3] unused, [4 ..] state indices (the tensor-core
                            //   fold kernel's work list); nullptr otherwise
     int32_t fold_grid;     // CTAs of the window-end fold kernel (the SM count)
+    int32_t* mark;         // LS_CHECK_SLOTS: [P] per-slot counts of the slot
+                           //   check, zero between calls; nullptr otherwise
 };
 
 struct StepArgs {
@@ -146,5 +149,6 @@ cudaError_t launch_read_colf(const AuxArgs& a, cudaStream_t s);
 cudaError_t launch_read_comp(const AuxArgs& a, cudaStream_t s);
 cudaError_t launch_init_comp(const PoolView& pv, cudaStream_t s);
 cudaError_t launch_read_log_meta(const AuxArgs& a, cudaStream_t s);
+cudaError_t launch_slot_check(const PoolView& pv, const int32_t* slots, int32_t n, cudaStream_t s);
 
 }  // namespace ls

@@ -40,18 +40,18 @@ def _need(t: torch.Tensor, name: str, dtype, device, shape=None):
 
 
 def _flags(col_scales: bool, compensators: int, plain: bool = False, k16: bool = False,
-           r16: bool = False) -> int:
+           r16: bool = False, check_slots: bool = False) -> int:
     return ((N.LS_INT8_COLUMN_SCALES if col_scales else 0) | N.LS_INT8_COMPENSATORS(compensators)
             | (N.LS_PLAIN_UPDATE if plain else 0) | (N.LS_LOG_BF16_K if k16 else 0)
-            | (N.LS_INT8_FP16_RECORDS if r16 else 0))
+            | (N.LS_INT8_FP16_RECORDS if r16 else 0) | (N.LS_CHECK_SLOTS if check_slots else 0))
 
 
 def required_bytes(num_slots, num_heads, variant="eager", gate="scalar", window=0,
                    d_k=128, d_v=128, col_scales=False, compensators=0, plain=False,
-                   k16=False, r16=False) -> int:
+                   k16=False, r16=False, check_slots=False) -> int:
     lib = N.load()
     d = N.LsDesc(num_slots, num_heads, d_k, d_v, VARIANTS[variant], GATES[gate], window,
-                 _flags(col_scales, compensators, plain, k16, r16))
+                 _flags(col_scales, compensators, plain, k16, r16, check_slots))
     out = C.c_size_t(0)
     N.check(lib.ls_pool_required_bytes(C.byref(d), C.byref(out)), "ls_pool_required_bytes")
     return int(out.value)
@@ -71,12 +71,16 @@ class StatePool:
     k16 (deferred / int8): bfloat16 key-side log factors (DeltaLog §3.4).
     r16 (int8): the window's records (k, u) and compensator pairs in IEEE
     binary16 (LeapQuant §4.1, §4.3).
+    check_slots: every call that changes states first checks on the device
+    that its slot list repeats no slot, and flags LS_DEV_SLOT_DUP if it does
+    (read by ``status()``); one extra launch per call.
     """
 
     def __init__(self, num_slots: int, num_heads: int, variant: str = "eager",
                  gate: str = "scalar", window: int = 0, d_k: int = 128, d_v: int = 128,
                  device=None, stream=None, col_scales: bool = False, compensators: int = 0,
-                 plain: bool = False, k16: bool = False, r16: bool = False):
+                 plain: bool = False, k16: bool = False, r16: bool = False,
+                 check_slots: bool = False):
         self.lib = N.load()
         self.variant, self.gate = variant, gate
         self.P, self.H, self.d_k, self.d_v = int(num_slots), int(num_heads), int(d_k), int(d_v)
@@ -93,9 +97,10 @@ class StatePool:
         self.plain = bool(plain)
         self.k16 = bool(k16)
         self.r16 = bool(r16)
+        self.check_slots = bool(check_slots)
         self.desc = N.LsDesc(self.P, self.H, self.d_k, self.d_v, VARIANTS[variant], GATES[gate],
                              self.window, _flags(self.col_scales, self.compensators, self.plain,
-                                                 self.k16, self.r16))
+                                                 self.k16, self.r16, self.check_slots))
         nbytes = C.c_size_t(0)
         N.check(self.lib.ls_pool_required_bytes(C.byref(self.desc), C.byref(nbytes)),
                 "ls_pool_required_bytes")

@@ -145,6 +145,21 @@ def test_fp16_record_flag(lib):
     assert _bytes(lib, _desc(flags=N.LS_INT8_FP16_RECORDS | N.LS_LOG_BF16_K))[0] == N.LS_ERR_INVALID
 
 
+def test_check_slots_flag(lib):
+    """LS_CHECK_SLOTS: every variant and format; one int32 count per slot at
+    the end of the layout, nothing else changes."""
+    from recurrent_state_quantization_gb300 import _native as N
+    P = 4
+    al = lambda x: (x + 255) // 256 * 256
+    for variant, flags in ((N.LS_EAGER_FP32, 0), (N.LS_DEFERRED_FP32, N.LS_LOG_BF16_K),
+                           (N.LS_WINDOW_INT8, 0), (N.LS_WINDOW_INT8, N.LS_INT8_COLUMN_SCALES),
+                           (N.LS_WINDOW_INT8, N.LS_INT8_COMPENSATORS(2) | N.LS_INT8_FP16_RECORDS)):
+        rc0, b0 = _bytes(lib, _desc(variant=variant, flags=flags))
+        rc1, b1 = _bytes(lib, _desc(variant=variant, flags=flags | N.LS_CHECK_SLOTS))
+        assert rc0 == rc1 == 0 and b1 == b0 + al(P * 4)
+    assert _bytes(lib, _desc(flags=N.LS_CHECK_SLOTS << 1))[0] == N.LS_ERR_INVALID
+
+
 def test_compensator_flag(lib):
     """LS_INT8_COMPENSATORS(r): INT8 only, r <= 8; the log holds W + r entries
     (K, U, and the scalar-gate snapshots padded to 4)."""
@@ -190,7 +205,7 @@ def test_error_strings(lib):
         s = lib.ls_error_string(code)
         assert isinstance(s, bytes) and len(s) > 0
     from recurrent_state_quantization_gb300 import _native as N
-    assert lib.ls_abi_version() == N.LS_ABI_VERSION == 4
+    assert lib.ls_abi_version() == N.LS_ABI_VERSION == 5
 
 
 def test_split_entry_points_reject_null_before_any_launch(lib):

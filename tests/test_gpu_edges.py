@@ -67,6 +67,57 @@ def test_out_of_range_slot_is_flagged_and_skipped(variant, window):
     assert pool.status() == 0  # cleared by the previous read
 
 
+@pytest.mark.parametrize("variant,window", [("eager", 0), ("deferred", 2), ("int8", 2)])
+def test_check_slots_passes_distinct_lists(variant, window):
+    """LS_CHECK_SLOTS: with distinct slot lists every state-changing call runs
+    unflagged, and the outputs and states equal an unchecked pool's bit for
+    bit (the check only counts slots)."""
+    _, _, StatePool, _, wl, _ = _mods()
+    w = wl.custom(batch=3, heads=2, num_slots=4, seed=6)
+    a = StatePool(4, 2, variant, "scalar", window, check_slots=True)
+    b = StatePool(4, 2, variant, "scalar", window)
+    slots = torch.tensor([3, 0, 2], dtype=torch.int32, device="cuda")
+    init = torch.randn(1, 2, D, D, device="cuda", generator=torch.Generator("cuda").manual_seed(4))
+    for p in (a, b):
+        p.load([1], init)
+    for t in range(5):
+        ins = _inputs(w, t, "cuda")
+        ya, yb = a.decode_step(slots, *ins), b.decode_step(slots, *ins)
+        assert torch.equal(ya, yb), t
+    for p in (a, b):
+        p.window_commit([0, 2])
+        p.reset([3])
+        if variant != "eager":
+            p.decode_step_split_static(slots, *_inputs(w, 5, "cuda"))
+    assert torch.equal(a.read(range(4)), b.read(range(4)))
+    assert a.status() == 0 and b.status() == 0
+
+
+def test_check_slots_flags_a_repeated_slot():
+    """LS_CHECK_SLOTS: a slot named twice in one call sets LS_DEV_SLOT_DUP;
+    the counts are cleared, so the next distinct list is not flagged.  Only
+    calls whose repeated writes are harmless run here: the eager step (two
+    warps update one dense state) and reset (two CTAs write the same zeros)."""
+    _, _, StatePool, _, wl, N = _mods()
+    w = wl.custom(batch=3, heads=2, num_slots=4, seed=7)
+    ins = _inputs(w, 0, "cuda")
+    pool = StatePool(4, 2, "eager", "scalar", 0, check_slots=True)
+    pool.decode_step(torch.tensor([1, 2, 1], dtype=torch.int32, device="cuda"), *ins)
+    assert pool.status() == N.LS_DEV_SLOT_DUP
+    pool.decode_step(torch.tensor([1, 2, 3], dtype=torch.int32, device="cuda"), *ins)
+    assert pool.status() == 0
+    for variant, window in (("eager", 0), ("deferred", 2), ("int8", 2)):
+        p = StatePool(4, 2, variant, "scalar", window, check_slots=True)
+        p.reset([0, 3, 0])
+        assert p.status() == N.LS_DEV_SLOT_DUP
+        p.reset([0, 3])
+        assert p.status() == 0
+    # an out-of-range slot is not counted; the reset flags it itself
+    p = StatePool(4, 2, "deferred", "scalar", 2, check_slots=True)
+    p.reset([2, 7])
+    assert p.status() == N.LS_DEV_SLOT_RANGE
+
+
 def test_argument_errors():
     _, _, StatePool, LsError, wl, N = _mods()
     pool = StatePool(2, 2, "eager", "scalar", 0)

@@ -440,7 +440,7 @@ def test_split_scratch_bytes_and_errors():
     eager = StatePool(4, 3, "eager", "scalar", 0, device=dev)
     with pytest.raises(RuntimeError, match="invalid"):
         eager.split_scratch_bytes(4)
-    assert N.LS_ABI_VERSION == 4
+    assert N.LS_ABI_VERSION == 5
 
 
 @pytest.mark.parametrize("variant,window", [("eager", 0), ("deferred", 16)])
