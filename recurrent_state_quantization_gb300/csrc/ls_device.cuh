@@ -221,6 +221,11 @@ __host__ __device__ __forceinline__ uint32_t key_bytes(const PoolView& pv) {
 }
 __host__ __device__ __forceinline__ uint32_t val_bytes(const PoolView& pv) { return pv.rec16 ? 2u : 4u; }
 
+// Hint: bring the 128-byte line holding p into L2 (no register result).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void flag_status(int32_t* status, int32_t bit) {
     atomicOr(status, bit);
 }

@@ -498,7 +498,21 @@ __global__ void __launch_bounds__(kThreads, 2) log_step_kernel(const StepArgs a)
         const size_t st = static_cast<size_t>(h);
         if (ok) {
             long long next = -1;
-            for (int w2 = w + 1; w2 < kWarps && next < 0; ++w2) next = fold_hd[w2];
+            int next_w = w;
+            for (int w2 = w + 1; w2 < kWarps && next < 0; ++w2) {
+                next = fold_hd[w2];
+                next_w = w2;
+            }
+            if constexpr (!INT8) {
+                // the next merging head's token vectors, into L2 one head ahead
+                // (k, q, v, and for the per-key gate lambda and lbar: 4 lines each)
+                if (next >= 0 && threadIdx.x < (PER_KEY ? 20 : 12)) {
+                    const int vec = threadIdx.x >> 2;
+                    const float* src = vec == 0 ? a.k : vec == 1 ? a.q : vec == 2 ? a.v : vec == 3 ? a.lam : pv.lbar;
+                    const size_t row = vec == 4 ? static_cast<size_t>(next) : static_cast<size_t>(blockIdx.x * kWarps + next_w);
+                    prefetch_l2(src + row * kD + 32 * (threadIdx.x & 3));
+                }
+            }
             const TokenIn tok{a.k, a.q, a.v, a.lam, __ldg(a.beta + r), a.y, static_cast<size_t>(r) * kD};
             const float* lbg = pv.lbar + st * (PER_KEY ? kD : 1);
             if constexpr (INT8)
