@@ -21,6 +21,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import re
 import statistics
@@ -295,6 +296,19 @@ def run_native(args, rank, world, local):
                       "parallelism": f"{world} independent replica(s), no collective"},
            "gpu_launches": launches_per_step * args.steps,
            "variants": per_variant}
+
+    # five repeats inside the timed region: consecutive blocks of whole windows
+    # (the slowest token of each window is its window end), ms per step each
+    period = 1
+    for _, W in variants:
+        if W:
+            period = period * W // math.gcd(period, W)
+    blk = args.steps // 5 // period * period
+    if blk > 0:
+        block_ms = [evs[r * blk][0][0].elapsed_time(evs[(r + 1) * blk - 1][-1][1]) / blk
+                    for r in range(5)]
+        out["repeats"] = {"blocks": 5, "steps_per_block": blk, "ms_per_step": block_ms,
+                          "median_ms_per_step": statistics.median(block_ms)}
 
     # roofline of the dominant kernel: the eager step (one launch per call)
     if "eager" in per_variant:
@@ -582,10 +596,23 @@ def cpu_baseline(w, variants, budget_s=6.0, steps=None):
         total_hs += w.heads * t
         total_s += t_spent
     return {"value": total_hs / total_s, "unit": UNIT, "cores": oracle.max_threads(),
-            "kind": "oracle",
+            "kind": "oracle", "host_cpu": cpu_model(), "nproc": os.cpu_count(),
             "sample": f"the {w.heads} heads of one slot of {w.name}, "
                       + ", ".join(f"{n}: {toks[n]} tokens" for n, _ in variants)
                       + "; double precision, OpenMP over heads; host time of the oracle calls"}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name, as lscpu reports it (else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
 
 
 def run_reference(args):
@@ -610,7 +637,8 @@ def run_reference(args):
                        "variants": ["eager", "deferred window=16", "int8 window=16"],
                        "sample_per_step": f"{w.heads} heads of one slot x 3 variants"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": res["cores"],
-                             "kind": "oracle", "sample": res["sample"]},
+                             "kind": "oracle", "sample": res["sample"],
+                             "host_cpu": res["host_cpu"], "nproc": res["nproc"]},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "wall_s": wall}
