@@ -176,7 +176,7 @@ typedef struct {
     uint32_t flags;    /* 0; for LS_WINDOW_INT8 also LS_INT8_COLUMN_SCALES,
                           LS_INT8_COMPENSATORS(r) and LS_INT8_FP16_RECORDS; for
                           the FP32 variants also LS_PLAIN_UPDATE; LS_LOG_BF16_K
-                          for the log variants */
+                          for the log variants; LS_CHECK_SLOTS for any */
 } ls_pool_desc;
 
 /* Human-readable name of a status code.  Never NULL. */
