@@ -231,10 +231,15 @@ class StatePool:
         """ls_decode_step_host: host (pinned) inputs and output; the copies run
         inside the library on ``stream``.  Synchronize before reading y."""
         B = int(slot_idx.numel())
-        for name, t in (("slot_idx", slot_idx), ("q", q), ("k", k), ("v", v),
-                        ("log_decay", log_decay), ("beta", beta), ("y", y)):
-            if t.device.type != "cpu" or not t.is_contiguous():
-                raise ValueError(f"{name} must be a contiguous host tensor")
+        cpu, f32 = torch.device("cpu"), torch.float32
+        _need(slot_idx, "slot_idx", torch.int32, cpu, (B,))
+        _need(q, "q", f32, cpu, (B, self.H, self.d_k))
+        _need(k, "k", f32, cpu, (B, self.H, self.d_k))
+        _need(v, "v", f32, cpu, (B, self.H, self.d_v))
+        _need(log_decay, "log_decay", f32, cpu,
+              (B, self.H) if self.dl == 1 else (B, self.H, self.d_k))
+        _need(beta, "beta", f32, cpu, (B, self.H))
+        _need(y, "y", f32, cpu, (B, self.H, self.d_v))
         need = self.staging_bytes(B)
         if self._staging is None or self._staging.numel() < need + 256:
             self._staging = torch.empty(need + 256, dtype=torch.uint8, device=self.device)
