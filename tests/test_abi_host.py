@@ -200,6 +200,22 @@ def test_null_arguments_are_rejected(lib):
     assert lib.ls_pool_create(C.byref(d), None, 0, None, C.byref(h)) == N.LS_ERR_INVALID
 
 
+def test_pool_create_checks_memory_before_cuda(lib):
+    """Too few bytes or a misaligned pointer are refused on the host, before
+    any CUDA call and without touching the memory (the pointer here is not a
+    device pointer at all)."""
+    from recurrent_state_quantization_gb300 import _native as N
+    d = _desc()
+    rc, need = _bytes(lib, d)
+    assert rc == 0
+    h = C.c_void_p()
+    fake = C.c_void_p(1 << 20)
+    assert lib.ls_pool_create(C.byref(d), fake, need - 1, None, C.byref(h)) == N.LS_ERR_SIZE
+    assert lib.ls_pool_create(C.byref(d), C.c_void_p((1 << 20) + 16), need, None,
+                              C.byref(h)) == N.LS_ERR_ALIGN
+    assert not h.value
+
+
 def test_error_strings(lib):
     for code in (0, -1, -2, -3, -4, -5, -99):
         s = lib.ls_error_string(code)

@@ -118,6 +118,38 @@ def test_check_slots_flags_a_repeated_slot():
     assert p.status() == N.LS_DEV_SLOT_RANGE
 
 
+@pytest.mark.parametrize("gate", ["scalar", "per_key"])
+@pytest.mark.parametrize("variant,window", [("eager", 0), ("deferred", 3), ("int8", 3)])
+def test_nan_input_stays_in_its_head(gate, variant, window):
+    """Non-finite inputs are not checked, but their effect stays in the head
+    that received them: with a NaN in one head's v, every other (request,
+    head) gives bit-identical outputs and states to a run with finite inputs,
+    across window ends (the per-CTA merge and the tensor-core fold process
+    heads that share shared memory or a queue with the poisoned one)."""
+    _, _, StatePool, _, wl, _ = _mods()
+    w = wl.custom(gate=gate, batch=3, heads=2, num_slots=4, seed=9)
+    a = StatePool(4, 2, variant, gate, window)
+    b = StatePool(4, 2, variant, gate, window)
+    slots = torch.tensor([3, 1, 0], dtype=torch.int32, device="cuda")
+    keep = torch.ones(3, 2, dtype=torch.bool, device="cuda")
+    keep[1, 0] = False  # request 1 (slot 1), head 0
+    for t in range(8):
+        q, k, v, lam, beta = _inputs(w, t, "cuda")
+        ya = a.decode_step(slots, q, k, v, lam, beta)
+        if t == 1:
+            v = v.clone()
+            v[1, 0, 5] = float("nan")
+        yb = b.decode_step(slots, q, k, v, lam, beta)
+        assert torch.equal(ya[keep], yb[keep]), t
+        if t == 1:
+            assert torch.isnan(yb[1, 0, 5])
+    sa, sb = a.read(range(4)), b.read(range(4))
+    for slot in (0, 2, 3):
+        assert torch.equal(sa[slot], sb[slot])
+    assert torch.equal(sa[1, 1], sb[1, 1])
+    assert a.status() == 0 and b.status() == 0
+
+
 def test_argument_errors():
     _, _, StatePool, LsError, wl, N = _mods()
     pool = StatePool(2, 2, "eager", "scalar", 0)
