@@ -31,9 +31,12 @@ namespace {
 //         is the window readout of LeapQuant App. B.2 eq. 9 / DeltaLog eq. 7)
 //   u  = beta (v - r),   y = y0 + (k.q) u
 //   append (K, U, Lam)[L] = (k, u, lp), lbar = lp, L += 1     (DeltaLog eq. 5)
-//   on the window's last token the W entries are folded into the base right
-//   away by the same warp (DeltaLog eq. 6; LeapQuant eq. 4 + requantization),
-//   after y was formed from the unquantized state.
+//   on the window's last token the log is folded into the base (DeltaLog
+//   eq. 6; LeapQuant eq. 4 + requantization), with y formed from the
+//   unquantized state: a deferred pool's CTA decodes that token in one pass
+//   over each closing head; an INT8 pool's warp appends the token, then the
+//   head is queued for the tensor-core fold kernel (per-row scales, no
+//   compensator pairs) or folded by the CTA (the other INT8 formats).
 //
 // Data movement: every warp streams its head through a private ring of
 // kRing shared-memory stages with 1-D bulk asynchronous copies (TMA,
