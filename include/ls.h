@@ -296,8 +296,9 @@ int ls_split_scratch_bytes(const ls_pool *pool, int32_t batch, size_t *bytes);
  * cannot provide device scratch.  The coefficients go to one fixed device
  * array of LS_SPLIT_STATIC_SCRATCH_BYTES per device (library-owned, placed
  * by the CUDA runtime when the library's module loads); its address is
- * looked up once per device, the current device being the pool's.  The call
- * allocates nothing.  No part of the array has to start at zero.
+ * looked up once per device.  The pool's device (the one current at
+ * ls_pool_create) must be the current device: otherwise the call returns
+ * LS_ERR_INVALID and launches nothing.  The call allocates nothing.  No part of the array has to start at zero.
  * Overlapping calls race: every call on a device uses the same array, so
  * two calls whose kernels may run at the same time (different streams,
  * different host threads) corrupt each other's coefficients; order them on

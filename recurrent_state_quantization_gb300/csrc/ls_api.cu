@@ -16,6 +16,7 @@ struct ls_pool {
     size_t bytes;
     ls::PoolView view;
     int num_sms;
+    int device;  // current device at ls_pool_create: the device of dev_mem
 };
 
 namespace {
@@ -212,6 +213,8 @@ int launch_step(ls_pool* p, const ls::StepArgs& a, cudaStream_t s) {
 
 }  // namespace
 
+int ls::pool_device(const ls_pool* p) { return p->device; }
+
 extern "C" {
 
 const char* ls_error_string(int status) {
@@ -260,6 +263,7 @@ int ls_pool_create(const ls_pool_desc* desc, void* dev_mem, size_t bytes, void* 
     p->bytes = bytes;
     p->view = make_view(*desc, L, p->mem);
     p->num_sms = sms > 0 ? sms : 1;
+    p->device = dev;
     p->view.fold_grid = p->num_sms;
     if (cudaMemsetAsync(dev_mem, 0, L.total, static_cast<cudaStream_t>(stream)) != cudaSuccess ||
         (p->view.R > 0 && ls::launch_init_comp(p->view, static_cast<cudaStream_t>(stream)) != cudaSuccess)) {

@@ -9,7 +9,12 @@
 
 #include <utility>
 
+struct ls_pool;  // the opaque handle of ls.h
+
 namespace ls {
+
+// The device that was current when the pool was created (its memory's device).
+int pool_device(const ::ls_pool* p);
 
 constexpr int kD = 128;         // d_k = d_v
 constexpr int kThreads = 256;   // threads of every CTA (8 warps)

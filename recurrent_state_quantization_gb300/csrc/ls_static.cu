@@ -4,12 +4,15 @@
 //
 // The array is module-scope device storage: the CUDA runtime places one
 // copy on every device the module is loaded on, zero-filled.  Its address
-// is looked up once per device, with that device current, and kept.
+// is looked up once per device, with that device current, and kept.  A call
+// is refused (LS_ERR_INVALID) unless the pool's device is the current one,
+// so the array used is always the one on the device of the pool's memory.
 #include <cuda_runtime.h>
 
 #include <mutex>
 
 #include "ls.h"
+#include "ls_internal.cuh"
 
 namespace {
 
@@ -19,10 +22,11 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_addr[kMaxDevices] = {};
 
-// Address of g_split_scratch on the current device.
-int static_scratch(void** out) {
+// Address of g_split_scratch on the pool's device, which must be current.
+int static_scratch(const ls_pool* pool, void** out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return LS_ERR_CUDA;
+    if (dev != ls::pool_device(pool)) return LS_ERR_INVALID;
     if (dev < 0 || dev >= kMaxDevices) return LS_ERR_INVALID;
     std::lock_guard<std::mutex> lock(g_mu);
     if (g_addr[dev] == nullptr) {
@@ -47,9 +51,11 @@ extern "C" int ls_decode_step_split_static(ls_pool* pool, const int32_t* d_slot_
     if (rc != LS_OK) return rc;
     if (need > LS_SPLIT_STATIC_SCRATCH_BYTES) return LS_ERR_SIZE;
     void* scratch = nullptr;
-    if ((rc = static_scratch(&scratch)) != LS_OK) return rc;
+    if ((rc = static_scratch(pool, &scratch)) != LS_OK) return rc;
     // nothing in the array has to start at zero: every coefficient the step
-    // reads was written by the prepare kernel of the same call
+    // reads was written by the prepare kernel of the same call (a log chunk
+    // copies the coefficients of whole 6-entry groups, but the step reads
+    // only those of the chunk's live entries)
     return ls_decode_step_split(pool, d_slot_idx, batch, q, k, v, log_decay, beta, y, scratch,
                                 LS_SPLIT_STATIC_SCRATCH_BYTES, stream);
 }

@@ -378,6 +378,8 @@ __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, 
             const int e0 = (it - 1 - P::NT) * P::EPC;
             const int n = min(P::EPC, L - e0);
             const float2* cf = reinterpret_cast<const float2*>(st + P::EPC * kVecBytes);
+            // the chunk carries the coefficients of all EPC entries; only the
+            // first n (written by this call's prepare kernel) are read
             for (int e = 0; e < n; ++e) {
                 const float4 U4 = rec_val4<REC>(st, static_cast<size_t>(e) * kD + 4 * lane);
                 const float2 c = cf[e];

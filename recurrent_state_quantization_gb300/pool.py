@@ -215,9 +215,10 @@ class StatePool:
         if need > N.LS_SPLIT_STATIC_SCRATCH_BYTES:
             raise ValueError(f"batch {B} needs {need} bytes of split-replay scratch; the static "
                              f"array holds {N.LS_SPLIT_STATIC_SCRATCH_BYTES}")
-        rc = self.lib.ls_decode_step_split_static(self.handle, _ptr(slot_idx), B, _ptr(q), _ptr(k),
-                                                  _ptr(v), _ptr(log_decay), _ptr(beta), _ptr(y),
-                                                  C.c_void_p(_stream(stream)))
+        with torch.cuda.device(self.device):  # the library checks that the pool's device is current
+            rc = self.lib.ls_decode_step_split_static(self.handle, _ptr(slot_idx), B, _ptr(q),
+                                                      _ptr(k), _ptr(v), _ptr(log_decay), _ptr(beta),
+                                                      _ptr(y), C.c_void_p(_stream(stream)))
         N.check(rc, "ls_decode_step_split_static")
         return y
 

@@ -12,6 +12,17 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    """Runs alone in a fresh process as well as after the other GPU tests:
+    skip without a GPU, build the library, make device 0 current."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
 def _twins(variant, gate, window, pre, **fmt):
     from recurrent_state_quantization_gb300 import StatePool
     from recurrent_state_quantization_gb300 import workloads as wl
@@ -77,3 +88,43 @@ def test_static_scratch_rejects_oversize_batch():
     small = pool.decode_step_split_static(slots[:8], x[:8], x[:8], x[:8], s[:8], s[:8])
     torch.cuda.synchronize()
     assert small.shape == (8, Hh, 128) and pool.status() == 0
+
+
+def _c_call(pool, slots, x, y):
+    """One ls_decode_step_split_static call through the C ABI, every buffer
+    allocated beforehand by the caller."""
+    p = lambda t: C.c_void_p(t.data_ptr())
+    q, k, v, lam, beta = x
+    return pool.lib.ls_decode_step_split_static(pool.handle, p(slots), int(slots.numel()), p(q), p(k),
+                                                p(v), p(lam), p(beta), p(y),
+                                                C.c_void_p(torch.cuda.current_stream().cuda_stream))
+
+
+def test_static_scratch_call_allocates_no_device_memory():
+    """After one warm call (which loads the kernels), further calls leave the
+    device's free memory unchanged: the scratch is the library's fixed array."""
+    from recurrent_state_quantization_gb300 import _native as N
+    a, b, slots, ins, _ = _twins("int8", "scalar", 3, 1)
+    y = torch.empty(slots.numel(), b.H, 128, device=slots.device)
+    assert _c_call(b, slots, ins[0], y) == N.LS_OK
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    assert _c_call(b, slots, ins[1], y) == N.LS_OK  # closes the window: both kernels of the call
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert b.status() == 0
+
+
+def test_static_scratch_refuses_another_current_device():
+    """The array used is the one on the pool's device: with another device
+    current the call returns LS_ERR_INVALID and launches nothing."""
+    if torch.cuda.device_count() < 2:
+        pytest.skip("needs two GPUs")
+    from recurrent_state_quantization_gb300 import _native as N
+    a, b, slots, ins, _ = _twins("deferred", "scalar", 5, 2)
+    y = torch.full((slots.numel(), b.H, 128), 7.0, device=slots.device)
+    with torch.cuda.device(1):
+        assert _c_call(b, slots, ins[0], y) == N.LS_ERR_INVALID
+    torch.cuda.synchronize()
+    assert bool((y == 7.0).all())
+    assert _c_call(b, slots, ins[0], y) == N.LS_OK
