@@ -267,17 +267,39 @@ def run_native(args, rank, world, local):
     elapsed_ms = reduce_max(start.elapsed_time(stop), world, dev)
 
     hbm_peak, peak_kind = peaks()
+    # per-variant figures: each variant timed on its own over whole windows
+    # (a multiple of every window / merge interval), so they do not depend on
+    # how --steps meets the windows; the headline stays the timed region above
+    period = 1
+    for _, W in variants:
+        if W:
+            period = period * W // math.gcd(period, W)
+    per_tokens = period * max(1, -(-64 // period))
     per_variant = {}
-    for vi, (n, W) in enumerate(variants):
-        ms = sum(evs[t][vi][0].elapsed_time(evs[t][vi][1]) for t in range(args.steps))
-        hs = heads * w.pools * args.steps
+    for n, W in variants:
+        a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = args.warmup + args.steps
+        torch.cuda.synchronize()
+        a_ev.record(stream)
+        for t in range(per_tokens):
+            for p in range(w.pools):
+                pools[n][p].decode_step(slot_idx, *inputs[p][(t0 + t) % ring], y=ys[n][p])
+        b_ev.record(stream)
+        torch.cuda.synchronize()
+        ms = a_ev.elapsed_time(b_ev)
+        hs = heads * w.pools * per_tokens
         bytes_ = bm.variant_bytes(n, w.gate, W) * hs
         gbs = bytes_ / (ms * 1e-3) / 1e9
-        per_variant[n] = {"window": W or None, "ms_per_token_all_pools": ms / args.steps,
+        per_variant[n] = {"window": W or None, "tokens": per_tokens,
+                          "ms_per_token_all_pools": ms / per_tokens,
                           "head_steps_per_s": hs / (ms * 1e-3),
                           "algorithmic_bytes_per_head_step": bm.variant_bytes(n, w.gate, W),
                           "achieved_gbs": gbs, "frac_of_" + peak_kind + "_hbm": gbs / hbm_peak}
     value = job_throughput(heads * w.pools * len(variants) * args.steps, world, elapsed_ms)
+    # windows that close inside the headline's timed region: the pools start
+    # at a boundary, so token t closes a window when (t + 1) % W == 0
+    window_ends = {n: sum(1 for t in range(args.warmup, args.warmup + args.steps) if (t + 1) % W == 0)
+                   for n, W in variants if W}
     # kernel launches per decode call: one step kernel; an INT8 pool with
     # per-row scales also launches the tensor-core window-end fold after it
     # (every token; it returns at once unless a window closed)
@@ -293,33 +315,55 @@ def run_native(args, rank, world, local):
                       "prewarm_tokens": w.prewarm_tokens, "distinct_token_inputs": ring,
                       "l2": "inputs larger than L2: every pool's state is 0.2-0.8 GB and the "
                             "step streams 4 pools x 3 variants (about 5 GB) per token",
-                      "parallelism": f"{world} independent replica(s), no collective"},
+                      "parallelism": f"{world} independent replica(s), no collective",
+                      "window_ends_in_timed_region": window_ends,
+                      "per_variant_timing": f"each variant alone over {per_tokens} tokens "
+                                            f"(whole windows), after the timed region"},
            "gpu_launches": launches_per_step * args.steps,
            "variants": per_variant}
 
     # five repeats inside the timed region: consecutive blocks of whole windows
-    # (the slowest token of each window is its window end), ms per step each
-    period = 1
-    for _, W in variants:
-        if W:
-            period = period * W // math.gcd(period, W)
+    # (the slowest token of each window is its window end), ms per step each;
+    # a region shorter than five whole windows is cut into five equal blocks
     blk = args.steps // 5 // period * period
+    whole = blk > 0
+    if not whole:
+        blk = args.steps // 5
     if blk > 0:
         block_ms = [evs[r * blk][0][0].elapsed_time(evs[(r + 1) * blk - 1][-1][1]) / blk
                     for r in range(5)]
         out["repeats"] = {"blocks": 5, "steps_per_block": blk, "ms_per_step": block_ms,
-                          "median_ms_per_step": statistics.median(block_ms)}
+                          "median_ms_per_step": statistics.median(block_ms),
+                          "blocks_are": "whole windows" if whole else
+                                        "equal token blocks (fewer than five whole windows timed)"}
 
-    # roofline of the dominant kernel: the eager step (one launch per call)
+    # roofline of the dominant kernel, the eager step (one launch per call):
+    # a run of back-to-back eager launches (every pool, several tokens), so
+    # the state each launch leaves dirty in L2 is written back inside the run
+    # and the average launch carries its full read and write traffic
     if "eager" in per_variant:
-        e = per_variant["eager"]
-        launch_ms = e["ms_per_token_all_pools"] / w.pools
+        runs = 16 * w.pools
+        a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a_ev.record(stream)
+        for t in range(runs // w.pools):
+            for p in range(w.pools):
+                pools["eager"][p].decode_step(slot_idx, *inputs[p][t % ring], y=ys["eager"][p])
+        b_ev.record(stream)
+        torch.cuda.synchronize()
+        launch_ms = a_ev.elapsed_time(b_ev) / runs
+        in_step_ms = sum(evs[t][0][0].elapsed_time(evs[t][0][1]) for t in range(args.steps)) / (
+            args.steps * w.pools) if variants[0][0] == "eager" else None
         bytes_launch = bm.eager_bytes(w.gate) * heads
         achieved = bytes_launch / (launch_ms * 1e-3) / 1e9
         out["roofline"] = {"bound": "hbm", "kernel": "eager_step_kernel", "achieved": achieved,
                            "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
                            "frac": achieved / hbm_peak,
                            "algorithmic_bytes_per_launch": bytes_launch,
+                           "launch_ms": launch_ms,
+                           "timing": f"{runs} back-to-back launches (CUDA events on the launching "
+                                     f"stream), after the timed region",
+                           "launch_ms_in_timed_region": in_step_ms,
                            "traffic": ncu_traffic("eager_step_kernel", heads)}
     if clk is not None:
         out["clocks"] = clk

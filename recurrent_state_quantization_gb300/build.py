@@ -19,8 +19,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libls.so")
-SOURCES = ["ls_api.cu", "ls_eager.cu", "ls_step.cu", "ls_fold.cu", "ls_aux.cu", "ls_static.cu",
-           "ls_mma_fold.cu"]
+SOURCES = ["ls_api.cu", "ls_eager.cu", "ls_step.cu", "ls_int8_step.cu", "ls_fold.cu", "ls_aux.cu",
+           "ls_static.cu", "ls_mma_fold.cu"]
 HEADERS = ["ls_internal.cuh", "ls_device.cuh", "ls_warp.cuh", "ls_umma.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2",

@@ -137,6 +137,7 @@ int prepare_all() {
     if (ls::prepare_fold_kernels() != cudaSuccess) return LS_ERR_CUDA;
     if (ls::prepare_aux_kernels() != cudaSuccess) return LS_ERR_CUDA;
     if (ls::prepare_window_fold_kernels() != cudaSuccess) return LS_ERR_CUDA;
+    if (ls::prepare_int8_step_kernels() != cudaSuccess) return LS_ERR_CUDA;
     return LS_OK;
 }
 

@@ -105,6 +105,13 @@ __device__ __forceinline__ float warp_sum(float x) {
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
     return x;
 }
+// max over the warp's 32 lanes of |x| (one redux; NaN inputs are ignored).
+__device__ __forceinline__ float warp_absmax_redux(float x) {
+    float r;
+    asm volatile("redux.sync.max.abs.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 // Sum over the 8 lanes of a lane group (lanes that differ in bits 0..2).
 __device__ __forceinline__ float group8_sum(float x) {
     x += __shfl_xor_sync(0xffffffffu, x, 1);
@@ -220,6 +227,26 @@ __host__ __device__ __forceinline__ uint32_t key_bytes(const PoolView& pv) {
     return (pv.k16 || pv.rec16) ? 2u : 4u;
 }
 __host__ __device__ __forceinline__ uint32_t val_bytes(const PoolView& pv) { return pv.rec16 ? 2u : 4u; }
+
+// Log record formats, a template parameter of the step kernels so that the
+// per-entry replay carries no format branches: FP32 key and value factors,
+// bfloat16 keys (DeltaLog §3.4), or binary16 keys and values (LeapQuant
+// §4.1, §4.3).  The pool view's k16 / rec16 select the instantiation.
+constexpr int kRecFP32 = 0, kRecBF16K = 1, kRecFP16 = 2;
+__host__ __device__ constexpr uint32_t rec_key_bytes(int rec) { return rec == kRecFP32 ? 4u : 2u; }
+__host__ __device__ constexpr uint32_t rec_val_bytes(int rec) { return rec == kRecFP16 ? 2u : 4u; }
+
+template <int REC>
+__device__ __forceinline__ float4 rec_key4(const void* p, size_t e) {
+    if constexpr (REC == kRecBF16K) return bf16x4_to_float4(reinterpret_cast<const uint2*>(p)[e >> 2]);
+    else if constexpr (REC == kRecFP16) return half4_to_float4(reinterpret_cast<const uint2*>(p)[e >> 2]);
+    else return reinterpret_cast<const float4*>(p)[e >> 2];
+}
+template <int REC>
+__device__ __forceinline__ float4 rec_val4(const void* p, size_t e) {
+    if constexpr (REC == kRecFP16) return half4_to_float4(reinterpret_cast<const uint2*>(p)[e >> 2]);
+    else return reinterpret_cast<const float4*>(p)[e >> 2];
+}
 
 // Hint: bring the 128-byte line holding p into L2 (no register result).
 __device__ __forceinline__ void prefetch_l2(const void* p) {

@@ -136,10 +136,14 @@ cudaError_t prepare_log_step_kernels();
 cudaError_t prepare_fold_kernels();
 cudaError_t prepare_aux_kernels();
 cudaError_t prepare_window_fold_kernels();
+cudaError_t prepare_int8_step_kernels();
 
 cudaError_t launch_eager_step(const StepArgs& a, bool per_key, cudaStream_t s);
 cudaError_t launch_log_step(const StepArgs& a, bool int8, bool per_key, cudaStream_t s);
 cudaError_t launch_log_step_split(const StepArgs& a, bool int8, bool per_key, cudaStream_t s);
+// INT8 pools with a window-end queue: the lean INT8 step kernel (fused or
+// split replay), then the window-end fold.
+cudaError_t launch_int8_step(const StepArgs& a, bool per_key, bool split, cudaStream_t s);
 // INT8 pools with a window-end queue: fold every state the step just queued
 // (a no-op launch when the queue is empty).
 cudaError_t launch_window_fold(const PoolView& pv, bool per_key, cudaStream_t s);

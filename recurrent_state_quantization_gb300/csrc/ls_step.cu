@@ -92,26 +92,6 @@ struct Plan {
 };
 static_assert(kSplitEntries * (kVecBytes + 8) <= kStage, "a split log chunk fits a stage");
 
-// Log record formats, a template parameter of the step kernels so that the
-// per-entry replay carries no format branches: FP32 key and value factors,
-// bfloat16 keys (DeltaLog §3.4), or binary16 keys and values (LeapQuant
-// §4.1, §4.3).  The pool view's k16 / rec16 select the instantiation.
-constexpr int kRecFP32 = 0, kRecBF16K = 1, kRecFP16 = 2;
-__host__ __device__ constexpr uint32_t rec_key_bytes(int rec) { return rec == kRecFP32 ? 4u : 2u; }
-__host__ __device__ constexpr uint32_t rec_val_bytes(int rec) { return rec == kRecFP16 ? 2u : 4u; }
-
-template <int REC>
-__device__ __forceinline__ float4 rec_key4(const void* p, size_t e) {
-    if constexpr (REC == kRecBF16K) return bf16x4_to_float4(reinterpret_cast<const uint2*>(p)[e >> 2]);
-    else if constexpr (REC == kRecFP16) return half4_to_float4(reinterpret_cast<const uint2*>(p)[e >> 2]);
-    else return reinterpret_cast<const float4*>(p)[e >> 2];
-}
-template <int REC>
-__device__ __forceinline__ float4 rec_val4(const void* p, size_t e) {
-    if constexpr (REC == kRecFP16) return half4_to_float4(reinterpret_cast<const uint2*>(p)[e >> 2]);
-    else return reinterpret_cast<const float4*>(p)[e >> 2];
-}
-
 // Issue item `it` of head hd into stage it % kRing (lane 0 only).
 template <bool INT8, bool PER_KEY, bool SPLIT, int REC>
 __device__ __forceinline__ void issue_item(WarpSmem& ws, const StepArgs& a, int row, size_t hd,
@@ -666,11 +646,10 @@ cudaError_t launch_log_step(const StepArgs& a, bool int8, bool per_key, cudaStre
     const int64_t rows = static_cast<int64_t>(a.batch) * a.pv.H;
     const dim3 grid(static_cast<unsigned>((rows + kWarps - 1) / kWarps));
     if (!int8) return launch_step_kernel<false, false, false>(a, per_key, grid, s);
+    if (a.pv.foldq != nullptr) return launch_int8_step(a, per_key, false, s);
     if (a.pv.R > 0)  // compensator pairs: the kernel that also fits them
         return launch_step_kernel<true, true, false>(a, per_key, grid, s);
-    const cudaError_t e = launch_step_kernel<true, false, false>(a, per_key, grid, s);
-    if (e != cudaSuccess || a.pv.foldq == nullptr) return e;
-    return launch_window_fold(a.pv, per_key, s);
+    return launch_step_kernel<true, false, false>(a, per_key, grid, s);
 }
 
 cudaError_t launch_log_step_split(const StepArgs& a, bool int8, bool per_key, cudaStream_t s) {
@@ -685,10 +664,9 @@ cudaError_t launch_log_step_split(const StepArgs& a, bool int8, bool per_key, cu
                              grid, 0, s, a);
     if (e != cudaSuccess) return e;
     if (!int8) return launch_step_kernel<false, false, true>(a, per_key, grid, s);
+    if (a.pv.foldq != nullptr) return launch_int8_step(a, per_key, true, s);
     if (a.pv.R > 0) return launch_step_kernel<true, true, true>(a, per_key, grid, s);
-    e = launch_step_kernel<true, false, true>(a, per_key, grid, s);
-    if (e != cudaSuccess || a.pv.foldq == nullptr) return e;
-    return launch_window_fold(a.pv, per_key, s);
+    return launch_step_kernel<true, false, true>(a, per_key, grid, s);
 }
 
 }  // namespace ls

@@ -118,13 +118,6 @@ __device__ __forceinline__ void named_barrier(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// max over the warp's 32 lanes of |x|.
-__device__ __forceinline__ float warp_absmax_redux(float x) {
-    float r;
-    asm volatile("redux.sync.max.abs.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
-    return r;
-}
-
 // Round to TF32 (nearest, ties away), as an FP32 bit pattern with the low 13
 // mantissa bits zero.
 __device__ __forceinline__ float tf32_rna(float x) {
