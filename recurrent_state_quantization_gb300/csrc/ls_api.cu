@@ -92,7 +92,7 @@ int make_layout(const ls_pool_desc* d, Layout* L) {
     off = align_up(off + nh * (dl == 1 ? (W + 3) / 4 * 4 : W * dl) * 4);
     // window-end queue of the tensor-core fold (INT8, per-row scales, no pairs)
     L->foldq = off;
-    off = align_up(off + (int8_mma_fold(d) ? 16 + nh * 4 : 0));
+    off = align_up(off + (int8_mma_fold(d) ? 16 + nh * 8 : 0));
     // per-slot counts of the duplicate-slot check
     L->mark = off;
     off = align_up(off + ((d->flags & LS_CHECK_SLOTS) ? static_cast<size_t>(d->num_slots) * 4 : 0));

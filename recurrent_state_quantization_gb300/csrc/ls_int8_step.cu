@@ -1,9 +1,9 @@
 // ls_int8_step.cu -- per-window INT8 decode step of libls (sm_103a).
 //
 // One warp per (request, head), as in the deferred step kernel, but with
-// nothing of the window end in it: a closing state is queued for
-// window_fold_kernel (ls_mma_fold.cu), which runs right after this kernel on
-// the same stream.  CTAs of four warps, four per SM (16 warps, up to 128
+// nothing of the window end in it: a token that closes its state's window is
+// queued, (state, request row), for window_fold_kernel (ls_mma_fold.cu),
+// which runs right after this kernel on the same stream and decodes it there.  CTAs of four warps, four per SM (16 warps, up to 128
 // registers per thread, 53 KiB of shared memory per CTA): measured on GB300
 // against three CTAs of eight warps with a two-stage ring, two CTAs of eight
 // warps, and five or six CTAs of four warps, this shape keeps the most bytes
@@ -218,28 +218,34 @@ __global__ void __launch_bounds__(kI8Threads, 4) int8_step_kernel(const StepArgs
         return;
     }
     const size_t hd = static_cast<size_t>(slot) * H + h;
+    const int L = pv.len[hd];
+    if (L < 0 || L >= W) {  // the pool memory of this state was overwritten
+        if (lane == 0) flag_status(pv.status, kDevBadState);
+        st4(a.y + ro, nan4);
+        return;
+    }
+    if (L + 1 == W) {
+        // the token closes the state's window: the whole token (its output, the
+        // fold of the W - 1 stored records and the requantization) is left to
+        // the window-end kernel, which reads the codes and records once
+        if (lane == 0) {
+            const int i = atomicAdd(pv.foldq, 1);
+            reinterpret_cast<int2*>(pv.foldq + 4)[i] = make_int2(static_cast<int>(hd), row);
+        }
+        return;
+    }
     if (lane == 0) {
 #pragma unroll
         for (int s = 0; s < kI8Ring; ++s) mbar_init(&ws.bar[s], 1);
         mbar_fence_init();
-        // the first kI8Ring items are never log chunks, so L is not needed yet
+        // the first kI8Ring items are never log chunks
 #pragma unroll
-        for (int it = 0; it < kI8Ring; ++it) i8_issue<PER_KEY, SPLIT, REC>(ws, a, row, hd, 0, it);
+        for (int it = 0; it < kI8Ring; ++it) i8_issue<PER_KEY, SPLIT, REC>(ws, a, row, hd, L, it);
     }
-    const int L = pv.len[hd];
     const float beta = __ldg(a.beta + row);
     float lp_scalar = 0.0f;
     if constexpr (!PER_KEY) lp_scalar = pv.lbar[hd] + __ldg(a.lam + row);
     __syncwarp();
-    if (L < 0 || L >= W) {  // the pool memory of this state was overwritten
-        if (lane == 0) {
-            flag_status(pv.status, kDevBadState);
-            for (int s = 0; s < kI8Ring; ++s) mbar_wait_bounded(&ws.bar[s], 0);
-        }
-        __syncwarp();
-        st4(a.y + ro, nan4);
-        return;
-    }
     const int NI = kI8LogItem0 + (L + EPC - 1) / EPC;
 
     float4 k4, q4, v4, lp4;
@@ -406,16 +412,7 @@ __global__ void __launch_bounds__(kI8Threads, 4) int8_step_kernel(const StepArgs
         pv.lamlog[lb0 + L] = lp4.x;
         pv.lbar[hd] = lp4.x;
     }
-    if (lane == 0) {
-        if (L + 1 < W) {
-            pv.len[hd] = L + 1;
-        } else {
-            // window end, folded by the tensor-core kernel launched after this
-            // one: the log is full (len = W) until that kernel resets it
-            pv.len[hd] = W;
-            pv.foldq[4 + atomicAdd(pv.foldq, 1)] = static_cast<int32_t>(hd);
-        }
-    }
+    if (lane == 0) pv.len[hd] = L + 1;
 }
 
 // Shared memory per CTA, and the largest shared-memory carveout so that four
@@ -476,7 +473,7 @@ cudaError_t launch_int8_step(const StepArgs& a, bool per_key, bool split, cudaSt
     const dim3 grid(static_cast<unsigned>((rows + kI8Warps - 1) / kI8Warps));
     const cudaError_t e = split ? launch_format<true>(a, per_key, grid, s) : launch_format<false>(a, per_key, grid, s);
     if (e != cudaSuccess) return e;
-    return launch_window_fold(a.pv, per_key, s);
+    return launch_window_fold(a, per_key, s);
 }
 
 }  // namespace ls

@@ -66,8 +66,9 @@ struct PoolView {
     int32_t lam_stride;    // floats per state in lamlog
     int32_t* foldq;        // INT8 with per-row scales and no compensator pairs:
                            //   window-end queue [0] count, [1] next, [2] done,
-                           //   [3] unused, [4 ..] state indices (the tensor-core
-                           //   fold kernel's work list); nullptr otherwise
+                           //   [3] unused, [4 ..] (state index, request row)
+                           //   pairs (the tensor-core window-end kernel's work
+                           //   list); nullptr otherwise
     int32_t fold_grid;     // CTAs of the window-end fold kernel (the SM count)
     int32_t* mark;         // LS_CHECK_SLOTS: [P] per-slot counts of the slot
                            //   check, zero between calls; nullptr otherwise
@@ -144,9 +145,10 @@ cudaError_t launch_log_step_split(const StepArgs& a, bool int8, bool per_key, cu
 // INT8 pools with a window-end queue: the lean INT8 step kernel (fused or
 // split replay), then the window-end fold.
 cudaError_t launch_int8_step(const StepArgs& a, bool per_key, bool split, cudaStream_t s);
-// INT8 pools with a window-end queue: fold every state the step just queued
-// (a no-op launch when the queue is empty).
-cudaError_t launch_window_fold(const PoolView& pv, bool per_key, cudaStream_t s);
+// INT8 pools with a window-end queue: decode the tokens the step kernel just
+// queued, fold each state's log and requantize it (a no-op launch when the
+// queue is empty).
+cudaError_t launch_window_fold(const StepArgs& a, bool per_key, cudaStream_t s);
 // deferred / INT8: fold the live log into the base (commit) or into a caller
 // buffer (read) for n slots.
 cudaError_t launch_fold(const AuxArgs& a, bool int8, bool per_key, bool commit, cudaStream_t s);

@@ -1,20 +1,25 @@
 // ls_mma_fold.cu -- INT8 window ends on the 5th-generation tensor cores
 // (tcgen05, sm_103a).
 //
-// At a window end of an INT8 pool with per-row scales and no compensator
-// pairs, the step kernel appends the closing token (the log then holds all W
-// records) and queues the state.  This kernel, launched after every such
-// step, folds each queued state and requantizes it:
-//     S[i][j] = exp(lb_i) s_i Z_ij + sum_{l<W} exp(lb_i - Lam_l,i) K_l,i U_l,j
-//     B_i = max_j |S_ij|,  s_i = B_i / 127,  Z_ij = rint(S_ij 127 / B_i)
-// ("LeapQuant: Efficient Linear Attention with Accurate Recurrent State
-// Quantization", §3.2 eq. 4 and App. B.3; "DeltaLog: Deferred Materialization
-// of Recurrent States for Linear Attention Decoding", §3.2 eq. 6: the merge
-// as base decay plus the decayed records), then resets lbar and the log.
+// A token that closes an INT8 state's window (per-row scales, no
+// compensator pairs) is not decoded by the step kernel: it queues (state,
+// request row), and this kernel, launched right after every such step,
+// decodes it in one pass over the state (LeapQuant §3.2 eq. 3-4 with App. A;
+// DeltaLog §3.2 eq. 6, the merge that includes the current update):
+//     lp   = lbar + lambda                          (cumulative log-decay)
+//     S    = exp(lp_i) s_i Z_ij + sum_{l<n} exp(lp_i - Lam_l,i) K_l,i U_l,j
+//          = D_t S_{t-1}, the decayed logical state (n = W - 1 stored records)
+//     r    = S^T k,  y0 = S^T q,  u = beta (v - r),  y = y0 + (k.q) u
+//     S   += k u^T   (with bfloat16 keys or binary16 records: the factors as a
+//                     record would store them; y uses k and u themselves)
+//     B_i  = max_j |S_ij|,  s_i = B_i / 127,  Z_ij = rint(S_ij 127 / B_i)
+// (App. B.3), then lbar = 0 and the log is emptied.  y is read from the
+// unquantized state.  The codes and the records of a closing state are read
+// once, here.
 //
-// The rank-W part is a GEMM, D = U^T A with D[j][i] (value column j in
-// tensor-memory lane j, key row i in column i), A[i][l] = exp(lb_i - Lam_l,i)
-// K_l,i and U[j][l] = U_l,j: M = N = 128, K = W, 16 records per chunk.  Each
+// The rank-n part is a GEMM, D = U^T A with D[j][i] (value column j in
+// tensor-memory lane j, key row i in column i), A[i][l] = exp(lp_i - Lam_l,i)
+// K_l,i and U[j][l] = U_l,j: M = N = 128, K = n, 16 records per chunk.  Each
 // FP32 operand is split into its TF32 rounding and the exact FP32 remainder,
 // x = x_h + x_r, and D accumulates U_h A_h + U_h A_r + U_r A_h (three
 // kind::tf32 MMAs per 8 records).  The dropped U_r A_r term and the TF32
@@ -26,26 +31,30 @@
 // memory), so this kernel is persistent, one CTA of 512 threads per SM, and
 // the step kernel carries no tcgen05 code at all.  The CTA holds four
 // independent groups of 128 threads.  A group takes the next queued state;
-// its records and codes were staged in shared memory by bulk copies while
-// the group finished the previous state.  Each thread reads its row of the
-// raw records, the group builds the split operands in place (K-major core
-// matrices, see ls_umma.cuh), one thread issues the MMAs into the group's 128
-// tensor-memory columns and commits them to the group's mbarrier, and the
-// copies of the next state start as soon as the MMAs have read the operands.
-// The epilogue runs on the CUDA cores: thread t of a group owns value column
-// j = t (the tensor-memory lanes its warp may read) for all 128 key rows.
-// The INT8 words of a state hold 4 key rows of one value column, so each
-// thread reads and writes 32 whole words and a warp 128 contiguous bytes per
-// access; a key row's absmax over a warp's 32 columns is one redux.sync, over
-// the group's 4 warps a shared-memory max.
-// S goes back to tensor memory between the absmax pass and the quantization
-// pass, so no thread holds more than 32 of its 128 values.
+// its header (the token's k, q, v, the state's scales, and for the per-key
+// gate lambda and lbar), codes and first records were staged in shared
+// memory by bulk copies while the group finished the previous state.  Each
+// thread reads its row of the raw records, the group builds the split
+// operands in place (K-major core matrices, see ls_umma.cuh), one thread
+// issues the MMAs into the group's 128 tensor-memory columns and commits them
+// to the group's mbarrier, and the copies of the next state start as soon as
+// the MMAs have read the operands (records) and pass 2 is done with the
+// codes (codes, header).  The epilogue runs on the CUDA cores: thread t of a group
+// owns value column j = t (the tensor-memory lanes its warp may read) for
+// all 128 key rows, so r_j, y0_j and u_j are thread-local sums.  The INT8
+// words of a state hold 4 key rows of one value column, so each thread reads
+// and writes 32 whole words and a warp 128 contiguous bytes per access; a
+// key row's absmax over a warp's 32 columns is one redux.sync, over the
+// group's 4 warps a shared-memory max.  Pass 1 forms S (32 key rows at a
+// time) and the readouts and puts S back in tensor memory; pass 2 adds
+// k u^T, takes the row maxima and puts S back again; pass 3 writes the
+// codes, so no thread holds more than 32 of its 128 values.
 //
 // Queue protocol (pool memory, zeroed at creation): the step kernel appends
-// state indices after atomically incrementing count; here groups take items
-// by atomically incrementing next; the last CTA to finish resets count, next
-// and done to zero for the next token.  With an empty queue every CTA returns
-// at once.
+// (state, row) pairs after atomically incrementing count; here groups take
+// items by atomically incrementing next; the last CTA to finish resets
+// count, next and done to zero for the next token.  With an empty queue
+// every CTA returns at once.
 #include <cuda_runtime.h>
 
 #include "ls_device.cuh"
@@ -71,17 +80,26 @@ constexpr uint32_t kCodeBytes = kD * kD;                     // INT8 codes of on
 struct alignas(128) GroupSmem {
     unsigned char ops[4][kOperandBytes];  // U head, U remainder, A head, A remainder
     uint32_t codes[kCodeBytes / 4];       // old codes of the state being folded
-    float vs[kD];                         // staged old scales s_i
-    float vl[kD];                         // staged lbar (per-key gate)
-    float es[kD];                         // exp(lb_i) s_i
+    float hk[kD];                         // header of the state: its closing token's
+    float hq[kD];                         //   k, q, v, its key-row scales s, and for
+    float hv[kD];                         //   the per-key gate lambda and lbar
+    float hs[kD];
+    float hlam[kD];
+    float hlb[kD];
+    float kk[kD];                         // the key of the state update, as a record
+                                          //   stores it (the header is restaged
+                                          //   after pass 2)
+    float es[kD];                         // exp(lp_i) s_i
     float red[4][kD];                     // per-warp absmax of each key row
     float fq[kD];                         // 127 / B_i
-    float gl[kChunkRecords];              // scalar gate: exp(lb - Lam_l) of the chunk
-    uint64_t ld_bar;                      // records (+ s, lbar) of a chunk
-    uint64_t cw_bar;                      // codes
+    float gl[kChunkRecords];              // scalar gate: exp(lp - Lam_l) of the chunk
+    float kqp[4];                         // per-warp partial sums of k.q
+    uint64_t rec_bar;                     // records of a chunk
+    uint64_t st_bar;                      // codes + header of a state
     uint64_t mma_bar;                     // MMA completion
     int32_t next_item;                    // queue position of the next state
-    float next_lb;                        // scalar gate: lbar of the next state
+    int32_t next_hd, next_row;            // the next state and its request row
+    float next_lb, next_lam, next_beta;   // its lbar, lambda (scalar gate) and beta
 };
 
 constexpr size_t window_fold_smem_bytes() { return kGroups * sizeof(GroupSmem); }
@@ -105,8 +123,12 @@ __device__ __forceinline__ bool named_barrier_or(int id, int nthreads, bool pred
     return r != 0;
 }
 
-// Stage records c0 .. c0 + nl - 1 of state hd (and, for the first chunk, its
-// scales and per-key lbar) on ld_bar (one thread).
+// Queue item `item`: (state index, request row).
+__device__ __forceinline__ int2 queue_item(const PoolView& pv, int item) {
+    return __ldcg(reinterpret_cast<const int2*>(pv.foldq + 4) + item);
+}
+
+// Stage records c0 .. c0 + nl - 1 of state hd on rec_bar (one thread).
 template <bool PER_KEY>
 __device__ __forceinline__ void stage_records(const PoolView& pv, size_t hd, int c0, int nl, GroupSmem& gs) {
     const size_t eo = (hd * static_cast<size_t>(pv.cap) + c0) * kD;
@@ -115,31 +137,37 @@ __device__ __forceinline__ void stage_records(const PoolView& pv, size_t hd, int
     const uint32_t upart = static_cast<uint32_t>(nl) * kD * val_bytes(pv);
     const size_t lb0 = hd * static_cast<size_t>(pv.lam_stride);
     const uint32_t lam_bytes = PER_KEY ? part : static_cast<uint32_t>((nl + 3) / 4 * 16);
-    uint32_t bytes = upart + kpart + lam_bytes;
-    if (c0 == 0) bytes += kVecBytes + (PER_KEY ? kVecBytes : 0);
     fence_proxy_async();  // the buffers were last used by generic loads and stores
-    mbar_arrive_expect_tx(&gs.ld_bar, bytes);
-    bulk_g2s(gs.ops[1], reinterpret_cast<const unsigned char*>(pv.ulog) + eo * val_bytes(pv), upart, &gs.ld_bar);
-    bulk_g2s(gs.ops[3], reinterpret_cast<const unsigned char*>(pv.klog) + eo * key_bytes(pv), kpart, &gs.ld_bar);
+    mbar_arrive_expect_tx(&gs.rec_bar, upart + kpart + lam_bytes);
+    bulk_g2s(gs.ops[1], reinterpret_cast<const unsigned char*>(pv.ulog) + eo * val_bytes(pv), upart, &gs.rec_bar);
+    bulk_g2s(gs.ops[3], reinterpret_cast<const unsigned char*>(pv.klog) + eo * key_bytes(pv), kpart, &gs.rec_bar);
     if constexpr (PER_KEY)
-        bulk_g2s(gs.ops[2], pv.lamlog + lb0 + static_cast<size_t>(c0) * kD, part, &gs.ld_bar);
+        bulk_g2s(gs.ops[2], pv.lamlog + lb0 + static_cast<size_t>(c0) * kD, part, &gs.rec_bar);
     else
-        bulk_g2s(gs.ops[2], pv.lamlog + lb0 + c0, lam_bytes, &gs.ld_bar);
-    if (c0 == 0) {
-        bulk_g2s(gs.vs, pv.scale + hd * kD, kVecBytes, &gs.ld_bar);
-        if constexpr (PER_KEY) bulk_g2s(gs.vl, pv.lbar + hd * kD, kVecBytes, &gs.ld_bar);
-    }
+        bulk_g2s(gs.ops[2], pv.lamlog + lb0 + c0, lam_bytes, &gs.rec_bar);
 }
 
-// Stage the 16 KiB of codes of state hd on cw_bar (one thread).
-__device__ __forceinline__ void stage_codes(const PoolView& pv, size_t hd, GroupSmem& gs) {
+// Stage the 16 KiB of codes and the header of state hd, whose closing token
+// is request row `row`, on st_bar (one thread).
+template <bool PER_KEY>
+__device__ __forceinline__ void stage_state(const StepArgs& a, size_t hd, int row, GroupSmem& gs) {
+    const PoolView& pv = a.pv;
     const unsigned char* src = reinterpret_cast<const unsigned char*>(pv.base) + hd * kCodeBytes;
+    const size_t ro = static_cast<size_t>(row) * kD;
     fence_proxy_async();
-    mbar_arrive_expect_tx(&gs.cw_bar, kCodeBytes);
+    mbar_arrive_expect_tx(&gs.st_bar, kCodeBytes + (PER_KEY ? 6 : 4) * kVecBytes);
 #pragma unroll
     for (int i = 0; i < 4; ++i)
         bulk_g2s(reinterpret_cast<unsigned char*>(gs.codes) + i * (kCodeBytes / 4), src + i * (kCodeBytes / 4),
-                 kCodeBytes / 4, &gs.cw_bar);
+                 kCodeBytes / 4, &gs.st_bar);
+    bulk_g2s(gs.hk, a.k + ro, kVecBytes, &gs.st_bar);
+    bulk_g2s(gs.hq, a.q + ro, kVecBytes, &gs.st_bar);
+    bulk_g2s(gs.hv, a.v + ro, kVecBytes, &gs.st_bar);
+    bulk_g2s(gs.hs, pv.scale + hd * kD, kVecBytes, &gs.st_bar);
+    if constexpr (PER_KEY) {
+        bulk_g2s(gs.hlam, a.lam + ro, kVecBytes, &gs.st_bar);
+        bulk_g2s(gs.hlb, pv.lbar + hd * kD, kVecBytes, &gs.st_bar);
+    }
 }
 
 // Three MMAs per 8 records of the staged chunk (one thread).
@@ -159,8 +187,8 @@ __device__ __forceinline__ void issue_chunk(const GroupSmem& gs, uint32_t tmem, 
 // Per-group pipeline state: barrier phases and which copies / MMAs are in
 // flight.
 struct GroupPipe {
-    uint32_t ld_ph = 0, cw_ph = 0, mma_ph = 0;
-    bool ld_out = false, cw_out = false, mma_out = false;
+    uint32_t rec_ph = 0, st_ph = 0, mma_ph = 0;
+    bool rec_out = false, st_out = false, mma_out = false;
 };
 
 // Wait (bounded) for one phase of bar; group-uniform result.  On a timeout
@@ -177,43 +205,106 @@ __device__ __forceinline__ bool group_wait(const PoolView& pv, uint64_t* bar, ui
     return true;
 }
 
-// Fold and requantize state hd with the 128 threads of one group (gt = thread
-// in the group, gw = its warp in the group).  On entry the first chunk of its
-// records and its codes are staged or in flight.  Thread 0 takes the next
-// queue item early; once the last MMA has read the operands it stages that
-// state's first chunk, and once pass 1 has read the codes, its codes, so the
-// copies overlap this state's epilogue.  Returns false after a timeout
-// (flagged).
+// The decayed, dequantized codes of key rows 32 qr .. 32 qr + 31 of value
+// column gt added to d (the rank-n fold of those rows).
+__device__ __forceinline__ void add_base_rows(const GroupSmem& gs, int qr, int gt, float (&d)[32]) {
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+        const uint32_t w = gs.codes[(8 * qr + g) * kD + gt] ^ 0x80808080u;
+        const float4 e4 = reinterpret_cast<const float4*>(gs.es)[8 * qr + g];
+        const float2 z01 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7650)),
+                                                  __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7651))),
+                                      make_float2(-kCodeBias, -kCodeBias));
+        const float2 z23 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7652)),
+                                                  __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7653))),
+                                      make_float2(-kCodeBias, -kCodeBias));
+        const float2 s01 = __ffma2_rn(z01, make_float2(e4.x, e4.y), make_float2(d[4 * g], d[4 * g + 1]));
+        const float2 s23 = __ffma2_rn(z23, make_float2(e4.z, e4.w), make_float2(d[4 * g + 2], d[4 * g + 3]));
+        d[4 * g + 0] = s01.x;
+        d[4 * g + 1] = s01.y;
+        d[4 * g + 2] = s23.x;
+        d[4 * g + 3] = s23.y;
+    }
+}
+
+// A key factor as a log record stores it: bfloat16 (k16), binary16 (rec16)
+// or FP32, widened back to FP32.
+__device__ __forceinline__ float stored_key(float k, const PoolView& pv) {
+    if (pv.k16) return __bfloat162float(__float2bfloat16_rn(k));
+    if (pv.rec16) return __half2float(__float2half_rn(k));
+    return k;
+}
+
+// d[c] += k_i u for the 32 key rows i = 32 qr + c (the closing token's
+// rank-one update of value column gt).
+__device__ __forceinline__ void add_token_rows(const GroupSmem& gs, int qr, float u, float (&d)[32]) {
+    const float2 uu = make_float2(u, u);
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+        const float4 k4 = reinterpret_cast<const float4*>(gs.kk)[8 * qr + g];
+        const float2 a = __ffma2_rn(make_float2(k4.x, k4.y), uu, make_float2(d[4 * g], d[4 * g + 1]));
+        const float2 b = __ffma2_rn(make_float2(k4.z, k4.w), uu, make_float2(d[4 * g + 2], d[4 * g + 3]));
+        d[4 * g + 0] = a.x;
+        d[4 * g + 1] = a.y;
+        d[4 * g + 2] = b.x;
+        d[4 * g + 3] = b.y;
+    }
+}
+
+// Decode the closing token of state hd (request row `row`), fold and
+// requantize the state with the 128 threads of one group (gt = thread in the
+// group, gw = its warp in the group).  On entry its header and codes, and its
+// first records, are staged or in flight.  Thread 0 takes the next queue item
+// early; once the last MMA has read the operands it stages that state's first
+// records, and after pass 2 (the codes and the header are consumed) its codes
+// and header, so the copies overlap this state's epilogue.  Returns false after a
+// timeout (flagged).
 template <bool PER_KEY>
-__device__ __forceinline__ bool fold_state(const PoolView& pv, size_t hd, float lb_scalar, GroupSmem& gs,
-                                           GroupPipe& gp, uint32_t tmem, uint32_t tlane, int bar_id, int gt,
-                                           int lane, int gw, int count) {
-    const int n = pv.cap;  // W records (no compensator pairs on this path)
+__device__ __forceinline__ bool fold_state(const StepArgs& a, size_t hd, int row, float lb_scalar,
+                                           float lam_scalar, float beta, GroupSmem& gs, GroupPipe& gp,
+                                           uint32_t tmem, uint32_t tlane, int bar_id, int gt, int lane, int gw,
+                                           int count) {
+    const PoolView& pv = a.pv;
+    const int n = pv.cap - 1;  // stored records; the closing token itself is never stored
     int next_item = 0;
     long long next_hd = -1;
-    float next_lb = 0.0f;
+    int next_row = 0;
+    float next_lb = 0.0f, next_lam = 0.0f, next_beta = 0.0f;
     if (gt == 0) {  // the next state, early: its index is needed once the MMAs are done
         next_item = atomicAdd(pv.foldq + 1, 1);
         if (next_item < count) {
-            next_hd = __ldcg(pv.foldq + 4 + next_item);
-            if constexpr (!PER_KEY) next_lb = __ldcg(pv.lbar + next_hd);
+            const int2 it = queue_item(pv, next_item);
+            next_hd = it.x;
+            next_row = it.y;
+            if constexpr (!PER_KEY) {
+                next_lb = __ldcg(pv.lbar + next_hd);
+                next_lam = __ldg(a.lam + next_row);
+            }
+            next_beta = __ldg(a.beta + next_row);
         }
     }
-    float lb = lb_scalar;  // the cumulative log-decay the log is folded at (row gt)
+    // header and codes: lp of key row gt, exp(lp) s, the token's k.q
+    if (!group_wait(pv, &gs.st_bar, gp.st_ph, gp.st_out, bar_id, gt)) return false;
+    const float lp = PER_KEY ? gs.hlb[gt] + gs.hlam[gt] : lb_scalar + lam_scalar;
+    gs.es[gt] = expf(lp) * gs.hs[gt];
+    // the key of the state update is the one a record would store (bfloat16
+    // keys, binary16 records); the token's own output uses k itself
+    gs.kk[gt] = stored_key(gs.hk[gt], pv);
+    const float vj = gs.hv[gt];
+    {
+        const float kq_part = warp_sum(gs.hk[gt] * gs.hq[gt]);
+        if (lane == 0) gs.kqp[gw] = kq_part;
+    }
 #pragma unroll 1
     for (int c0 = 0; c0 < n; c0 += kChunkRecords) {
         const int nl = min(kChunkRecords, n - c0);
-        if (!group_wait(pv, &gs.ld_bar, gp.ld_ph, gp.ld_out, bar_id, gt)) return false;
-        if (c0 == 0) {
-            if constexpr (PER_KEY) lb = gs.vl[gt];
-            gs.es[gt] = expf(lb) * gs.vs[gt];
-        }
-        // row gt of both operands: U_l[j = gt] and A[i = gt][l] = exp(lb_i - Lam_l,i) K_l,i
+        if (!group_wait(pv, &gs.rec_bar, gp.rec_ph, gp.rec_out, bar_id, gt)) return false;
+        // row gt of both operands: U_l[j = gt] and A[i = gt][l] = exp(lp_i - Lam_l,i) K_l,i
         // (scalar gate: one factor per record, computed once for the group)
         const float* ru = reinterpret_cast<const float*>(gs.ops[1]);
         const float* rl = reinterpret_cast<const float*>(gs.ops[2]);
         float u[kChunkRecords], x[kChunkRecords];
-        if (!PER_KEY && gt < kChunkRecords) gs.gl[gt] = gt < nl ? expf(lb - rl[gt]) : 0.0f;
+        if (!PER_KEY && gt < kChunkRecords) gs.gl[gt] = gt < nl ? expf(lp - rl[gt]) : 0.0f;
 #pragma unroll
         for (int l = 0; l < kChunkRecords; ++l) {
             u[l] = 0.0f;
@@ -225,7 +316,7 @@ __device__ __forceinline__ bool fold_state(const PoolView& pv, size_t hd, float 
                            ? key16_to_float(reinterpret_cast<const unsigned short*>(gs.ops[3])[l * kD + gt],
                                             pv.k16 != 0)
                            : reinterpret_cast<const float*>(gs.ops[3])[l * kD + gt];
-                if constexpr (PER_KEY) x[l] *= expf(lb - rl[l * kD + gt]);
+                if constexpr (PER_KEY) x[l] *= expf(lp - rl[l * kD + gt]);
             }
         }
         named_barrier(bar_id, kGroupThreads);  // every row is in registers: the buffers are free
@@ -260,38 +351,54 @@ __device__ __forceinline__ bool fold_state(const PoolView& pv, size_t hd, float 
         if (gt == 0) {
             if (c0 + kChunkRecords < n) {
                 stage_records<PER_KEY>(pv, hd, c0 + kChunkRecords, min(kChunkRecords, n - c0 - kChunkRecords), gs);
-                gp.ld_out = true;
+                gp.rec_out = true;
             } else if (next_hd >= 0) {
                 stage_records<PER_KEY>(pv, static_cast<size_t>(next_hd), 0, min(kChunkRecords, n), gs);
-                gp.ld_out = true;
+                gp.rec_out = true;
             }
         }
     }
     tc_fence_after();
-    if (!group_wait(pv, &gs.cw_bar, gp.cw_ph, gp.cw_out, bar_id, gt)) return false;
+    if (n == 0) named_barrier(bar_id, kGroupThreads);  // es, kk, k.q complete (with records,
+                                                       // their barriers ordered these)
     // pass 1: S = D + the decayed, dequantized old base, 32 key rows at a
-    // time; each row's absmax over this warp's columns; S back to tensor memory
+    // time; r = S^T k and y0 = S^T q of this thread's column; S back to
+    // tensor memory
+    float2 r2 = make_float2(0.f, 0.f), y2 = r2;
+#pragma unroll
+    for (int qr = 0; qr < 4; ++qr) {
+        float d[32];
+        if (n > 0) {
+            tmem_ld32(tlane + 32u * qr, d);
+        } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) d[c] = 0.0f;
+        }
+        add_base_rows(gs, qr, gt, d);
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+            const float4 k4 = reinterpret_cast<const float4*>(gs.hk)[8 * qr + g];  // k itself
+            const float4 q4 = reinterpret_cast<const float4*>(gs.hq)[8 * qr + g];
+            r2 = __ffma2_rn(make_float2(d[4 * g], d[4 * g + 1]), make_float2(k4.x, k4.y), r2);
+            r2 = __ffma2_rn(make_float2(d[4 * g + 2], d[4 * g + 3]), make_float2(k4.z, k4.w), r2);
+            y2 = __ffma2_rn(make_float2(d[4 * g], d[4 * g + 1]), make_float2(q4.x, q4.y), y2);
+            y2 = __ffma2_rn(make_float2(d[4 * g + 2], d[4 * g + 3]), make_float2(q4.z, q4.w), y2);
+        }
+        tmem_st32(tlane + 32u * qr, d);
+    }
+    const float kq = (gs.kqp[0] + gs.kqp[1]) + (gs.kqp[2] + gs.kqp[3]);
+    // the closing token's correction and output (y from the unquantized state)
+    const float r = r2.x + r2.y, y0 = y2.x + y2.y;
+    const float u_out = beta * (vj - r);
+    a.y[static_cast<size_t>(row) * kD + gt] = fmaf(kq, u_out, y0);
+    const float uj = pv.rec16 ? __half2float(__float2half_rn(u_out)) : u_out;  // as a record stores it
+    // pass 2: S + k u^T back to tensor memory; each key row's absmax over
+    // this warp's columns
 #pragma unroll
     for (int qr = 0; qr < 4; ++qr) {
         float d[32];
         tmem_ld32(tlane + 32u * qr, d);
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-            const uint32_t w = gs.codes[(8 * qr + g) * kD + gt] ^ 0x80808080u;
-            const float4 e4 = reinterpret_cast<const float4*>(gs.es)[8 * qr + g];
-            const float2 z01 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7650)),
-                                                      __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7651))),
-                                          make_float2(-kCodeBias, -kCodeBias));
-            const float2 z23 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7652)),
-                                                      __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7653))),
-                                          make_float2(-kCodeBias, -kCodeBias));
-            const float2 s01 = __ffma2_rn(z01, make_float2(e4.x, e4.y), make_float2(d[4 * g], d[4 * g + 1]));
-            const float2 s23 = __ffma2_rn(z23, make_float2(e4.z, e4.w), make_float2(d[4 * g + 2], d[4 * g + 3]));
-            d[4 * g + 0] = s01.x;
-            d[4 * g + 1] = s01.y;
-            d[4 * g + 2] = s23.x;
-            d[4 * g + 3] = s23.y;
-        }
+        add_token_rows(gs, qr, uj, d);
 #pragma unroll
         for (int c = 0; c < 32; c += 4) {
             const float4 m = make_float4(warp_absmax_redux(d[c]), warp_absmax_redux(d[c + 1]),
@@ -303,12 +410,16 @@ __device__ __forceinline__ bool fold_state(const PoolView& pv, size_t hd, float 
     tc_fence_before();
     if (gt == 0) {
         gs.next_item = next_item;
+        gs.next_hd = static_cast<int32_t>(next_hd);
+        gs.next_row = next_row;
         gs.next_lb = next_lb;
+        gs.next_lam = next_lam;
+        gs.next_beta = next_beta;
     }
-    named_barrier(bar_id, kGroupThreads);  // row maxima complete, codes consumed
+    named_barrier(bar_id, kGroupThreads);  // row maxima complete; codes and header consumed
     if (gt == 0 && next_hd >= 0) {
-        stage_codes(pv, static_cast<size_t>(next_hd), gs);
-        gp.cw_out = true;
+        stage_state<PER_KEY>(a, static_cast<size_t>(next_hd), next_row, gs);
+        gp.st_out = true;
     }
     {
         const float B = fmaxf(fmaxf(gs.red[0][gt], gs.red[1][gt]), fmaxf(gs.red[2][gt], gs.red[3][gt]));
@@ -319,7 +430,7 @@ __device__ __forceinline__ bool fold_state(const PoolView& pv, size_t hd, float 
     }
     named_barrier(bar_id, kGroupThreads);
     tc_fence_after();
-    // pass 2: codes rint(S 127 / B_i), four key rows per word, one warp
+    // pass 3: codes rint(S 127 / B_i), four key rows per word, one warp
     // writing 128 contiguous bytes per store
     uint32_t* const words = reinterpret_cast<uint32_t*>(pv.base) + hd * (kCodeBytes / 4) + gt;
 #pragma unroll
@@ -329,9 +440,9 @@ __device__ __forceinline__ bool fold_state(const PoolView& pv, size_t hd, float 
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
             const float4 f4 = reinterpret_cast<const float4*>(gs.fq)[8 * qr + g];
-            const float2 a = code_words2(make_float2(d[4 * g], d[4 * g + 1]), make_float2(f4.x, f4.y));
-            const float2 b = code_words2(make_float2(d[4 * g + 2], d[4 * g + 3]), make_float2(f4.z, f4.w));
-            words[(8 * qr + g) * kD] = pack_low_bytes(a.x, a.y, b.x, b.y);
+            const float2 a2 = code_words2(make_float2(d[4 * g], d[4 * g + 1]), make_float2(f4.x, f4.y));
+            const float2 b2 = code_words2(make_float2(d[4 * g + 2], d[4 * g + 3]), make_float2(f4.z, f4.w));
+            words[(8 * qr + g) * kD] = pack_low_bytes(a2.x, a2.y, b2.x, b2.y);
         }
     }
     tc_fence_before();  // these reads, before the group's next MMAs (after a barrier)
@@ -346,11 +457,12 @@ __device__ __forceinline__ bool fold_state(const PoolView& pv, size_t hd, float 
 }
 
 template <bool PER_KEY>
-__global__ void __launch_bounds__(kFoldThreads, 1) window_fold_kernel(const PoolView pv) {
+__global__ void __launch_bounds__(kFoldThreads, 1) window_fold_kernel(const StepArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ uint32_t tmem_base;
     __shared__ int32_t count_s;
     pdl_enter();
+    const PoolView& pv = a.pv;
     int32_t* const q = pv.foldq;
     const int tid = threadIdx.x;
     if (tid == 0) count_s = __ldcg(q);
@@ -361,21 +473,31 @@ __global__ void __launch_bounds__(kFoldThreads, 1) window_fold_kernel(const Pool
     const int g = warp >> 2, gt = tid & (kGroupThreads - 1), gw = warp & 3;
     GroupSmem& gs = reinterpret_cast<GroupSmem*>(smem)[g];
     const int bar_id = 1 + g;
+    const int n = pv.cap - 1;
     GroupPipe gp;
     if (gt == 0) {
-        mbar_init(&gs.ld_bar, 1);
-        mbar_init(&gs.cw_bar, 1);
+        mbar_init(&gs.rec_bar, 1);
+        mbar_init(&gs.st_bar, 1);
         mbar_init(&gs.mma_bar, 1);
         mbar_fence_init();
         // the group's first state
         const int item = atomicAdd(q + 1, 1);
         gs.next_item = item;
         if (item < count) {
-            const size_t hd = static_cast<size_t>(__ldcg(q + 4 + item));
-            if constexpr (!PER_KEY) gs.next_lb = __ldcg(pv.lbar + hd);
-            stage_records<PER_KEY>(pv, hd, 0, min(kChunkRecords, pv.cap), gs);
-            stage_codes(pv, hd, gs);
-            gp.ld_out = gp.cw_out = true;
+            const int2 it = queue_item(pv, item);
+            gs.next_hd = it.x;
+            gs.next_row = it.y;
+            if constexpr (!PER_KEY) {
+                gs.next_lb = __ldcg(pv.lbar + it.x);
+                gs.next_lam = __ldg(a.lam + it.y);
+            }
+            gs.next_beta = __ldg(a.beta + it.y);
+            stage_state<PER_KEY>(a, static_cast<size_t>(it.x), it.y, gs);
+            gp.st_out = true;
+            if (n > 0) {
+                stage_records<PER_KEY>(pv, static_cast<size_t>(it.x), 0, min(kChunkRecords, n), gs);
+                gp.rec_out = true;
+            }
         }
     }
     if (warp == 0) tmem_alloc512(&tmem_base);
@@ -385,21 +507,21 @@ __global__ void __launch_bounds__(kFoldThreads, 1) window_fold_kernel(const Pool
     const uint32_t tmem = tmem_base + 128u * g;                           // the group's columns
     const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * gw) << 16);  // the warp's lanes
     int item = gs.next_item;
-    float lb = gs.next_lb;
 #pragma unroll 1
     while (item < count) {
-        const size_t hd = static_cast<size_t>(__ldcg(q + 4 + item));
-        if (!fold_state<PER_KEY>(pv, hd, lb, gs, gp, tmem, tlane, bar_id, gt, lane, gw, count)) {
+        const size_t hd = static_cast<size_t>(gs.next_hd);
+        const int row = gs.next_row;
+        const float lb = gs.next_lb, lam = gs.next_lam, beta = gs.next_beta;
+        if (!fold_state<PER_KEY>(a, hd, row, lb, lam, beta, gs, gp, tmem, tlane, bar_id, gt, lane, gw, count)) {
             // after a timeout: let this group's copies and MMAs land before exit
             if (gt == 0) {
-                if (gp.ld_out) mbar_wait_bounded(&gs.ld_bar, gp.ld_ph);
-                if (gp.cw_out) mbar_wait_bounded(&gs.cw_bar, gp.cw_ph);
+                if (gp.rec_out) mbar_wait_bounded(&gs.rec_bar, gp.rec_ph);
+                if (gp.st_out) mbar_wait_bounded(&gs.st_bar, gp.st_ph);
                 if (gp.mma_out) mbar_wait_bounded(&gs.mma_bar, gp.mma_ph);
             }
             break;
         }
         item = gs.next_item;
-        lb = gs.next_lb;
     }
     tc_fence_before();
     __syncthreads();  // every group is done with tensor memory and the queue
@@ -424,9 +546,9 @@ cudaError_t prepare_window_fold_kernels() {
     return cudaFuncSetAttribute(window_fold_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
-cudaError_t launch_window_fold(const PoolView& pv, bool per_key, cudaStream_t s) {
+cudaError_t launch_window_fold(const StepArgs& a, bool per_key, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(pv.fold_grid > 0 ? pv.fold_grid : 1));
+    cfg.gridDim = dim3(static_cast<unsigned>(a.pv.fold_grid > 0 ? a.pv.fold_grid : 1));
     cfg.blockDim = dim3(kFoldThreads);
     cfg.dynamicSmemBytes = window_fold_smem_bytes();
     cfg.stream = s;
@@ -435,8 +557,8 @@ cudaError_t launch_window_fold(const PoolView& pv, bool per_key, cudaStream_t s)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return per_key ? cudaLaunchKernelEx(&cfg, window_fold_kernel<true>, pv)
-                   : cudaLaunchKernelEx(&cfg, window_fold_kernel<false>, pv);
+    return per_key ? cudaLaunchKernelEx(&cfg, window_fold_kernel<true>, a)
+                   : cudaLaunchKernelEx(&cfg, window_fold_kernel<false>, a);
 }
 
 }  // namespace ls

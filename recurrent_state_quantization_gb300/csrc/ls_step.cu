@@ -34,9 +34,10 @@ namespace {
 //   on the window's last token the log is folded into the base (DeltaLog
 //   eq. 6; LeapQuant eq. 4 + requantization), with y formed from the
 //   unquantized state: a deferred pool's CTA decodes that token in one pass
-//   over each closing head; an INT8 pool's warp appends the token, then the
-//   head is queued for the tensor-core fold kernel (per-row scales, no
-//   compensator pairs) or folded by the CTA (the other INT8 formats).
+//   over each closing head; an INT8 pool with column scales or compensator
+//   pairs appends the token, then the CTA folds the head.  (INT8 pools with
+//   per-row scales and no pairs use the kernels of ls_int8_step.cu and
+//   ls_mma_fold.cu instead.)
 //
 // Data movement: every warp streams its head through a private ring of
 // kRing shared-memory stages with 1-D bulk asynchronous copies (TMA,
@@ -427,15 +428,6 @@ __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, 
         if (lane == 0) pv.len[hd] = L + 1;
         return -1;
     }
-    if (INT8 && pv.foldq != nullptr) {
-        // window end, folded by the tensor-core kernel launched after this
-        // one: the log is full (len = W) until that kernel resets it
-        if (lane == 0) {
-            pv.len[hd] = W;
-            pv.foldq[4 + atomicAdd(pv.foldq, 1)] = static_cast<int32_t>(hd);
-        }
-        return -1;
-    }
     *lp_out = lp4.x;
     return static_cast<long long>(hd);  // INT8 window end: the CTA folds the W entries
 }
@@ -525,8 +517,10 @@ __global__ void __launch_bounds__(kThreads, 2) log_step_kernel(const StepArgs a)
 // of each (request, head) into a.coef[row * a.cstride + l] (DeltaLog §5.3).
 // One warp per head with the fused step's lane layout (lane l holds keys
 // 4l..4l+3) and reductions.  Heads with nothing to replay, heads the step
-// will flag, and FP32 heads whose merge interval closes on this token (the
-// CTA decodes those in one pass over the state) write nothing.
+// will flag, FP32 heads whose merge interval closes on this token (the CTA
+// decodes those in one pass over the state) and INT8 heads whose window
+// closes on a pool with a window-end queue (the window-end kernel decodes
+// those) write nothing.
 template <bool INT8, bool PER_KEY>
 __global__ void __launch_bounds__(kThreads) replay_prepare_kernel(const StepArgs a) {
     pdl_enter();
@@ -542,6 +536,7 @@ __global__ void __launch_bounds__(kThreads) replay_prepare_kernel(const StepArgs
     const int L = pv.len[hd];
     if (L <= 0 || L >= pv.cap) return;
     if (!INT8 && L + 1 == pv.W) return;
+    if (INT8 && pv.foldq != nullptr && L + 1 == pv.cap) return;
     const size_t ro = static_cast<size_t>(row) * kD + 4 * lane;
     const float4 k4 = __ldg(reinterpret_cast<const float4*>(a.k + ro));
     const float4 q4 = __ldg(reinterpret_cast<const float4*>(a.q + ro));

@@ -62,11 +62,11 @@ def test_required_bytes_layout(lib):
     assert rc == 0 and b == 256 + al(nh * 128 * 128 * 4)
     # INT8, scalar gate: INT8 base, scales, lbar, len, W entries (K, U, log-decay),
     # and the window-end queue of the tensor-core fold (16-byte header + one
-    # state index per state)
+    # (state index, request row) pair per state)
     rc, b = _bytes(lib, _desc())
     expect = (256 + al(nh * 128 * 128) + al(nh * 128 * 4) + al(nh * 4)
               + al(nh * 4) + 2 * al(nh * W * 128 * 4) + al(nh * ((W + 3) // 4 * 4) * 4)
-              + al(16 + nh * 4))
+              + al(16 + nh * 8))
     assert rc == 0 and b == expect
     # deferred, per-key gate
     rc, b = _bytes(lib, _desc(variant=N.LS_DEFERRED_FP32, gate=N.LS_GATE_PER_KEY))
