@@ -33,11 +33,10 @@ struct Layout {
     size_t status, base, scale, colf, lbar, len, klog, ulog, lamlog, foldq, mark, total;
 };
 
-// INT8 pools with per-row scales and no compensator pairs close their windows
-// on the tensor cores, in a kernel of its own after the step.
+// INT8 pools without compensator pairs (per-row or column scales) close
+// their windows on the tensor cores, in a kernel of its own after the step.
 bool int8_mma_fold(const ls_pool_desc* d) {
-    return d->variant == LS_WINDOW_INT8 && (d->flags & LS_INT8_COLUMN_SCALES) == 0 &&
-           ((d->flags >> 8) & 15u) == 0;
+    return d->variant == LS_WINDOW_INT8 && ((d->flags >> 8) & 15u) == 0;
 }
 
 // Checks a descriptor; fills the layout when it is valid.
@@ -90,7 +89,7 @@ int make_layout(const ls_pool_desc* d, Layout* L) {
     // scalar gate: one snapshot per entry, per-state stride padded to a
     // multiple of 4 floats so every state's snapshots start 16-byte aligned
     off = align_up(off + nh * (dl == 1 ? (W + 3) / 4 * 4 : W * dl) * 4);
-    // window-end queue of the tensor-core fold (INT8, per-row scales, no pairs)
+    // window-end queue of the tensor-core fold (INT8 without compensator pairs)
     L->foldq = off;
     off = align_up(off + (int8_mma_fold(d) ? 16 + nh * 8 : 0));
     // per-slot counts of the duplicate-slot check

@@ -64,7 +64,7 @@ struct PoolView {
     int32_t rec16;         // 1: klog and ulog hold IEEE binary16 (INT8 FP16 records)
     int32_t cap;           // log entries per state: W + R
     int32_t lam_stride;    // floats per state in lamlog
-    int32_t* foldq;        // INT8 with per-row scales and no compensator pairs:
+    int32_t* foldq;        // INT8 without compensator pairs:
                            //   window-end queue [0] count, [1] next, [2] done,
                            //   [3] unused, [4 ..] (state index, request row)
                            //   pairs (the tensor-core window-end kernel's work

@@ -1,11 +1,12 @@
 // ls_mma_fold.cu -- INT8 window ends on the 5th-generation tensor cores
 // (tcgen05, sm_103a).
 //
-// A token that closes an INT8 state's window (per-row scales, no
-// compensator pairs) is not decoded by the step kernel: it queues (state,
-// request row), and this kernel, launched right after every such step,
-// decodes it in one pass over the state (LeapQuant §3.2 eq. 3-4 with App. A;
-// DeltaLog §3.2 eq. 6, the merge that includes the current update):
+// A token that closes an INT8 state's window (per-row scales or the
+// smoothed column-scale format, no compensator pairs) is not decoded by the
+// step kernel: it queues (state, request row), and this kernel, launched
+// right after every such step, decodes it in one pass over the state
+// (LeapQuant §3.2 eq. 3-4 with App. A; DeltaLog §3.2 eq. 6, the merge that
+// includes the current update):
 //     lp   = lbar + lambda                          (cumulative log-decay)
 //     S    = exp(lp_i) s_i Z_ij + sum_{l<n} exp(lp_i - Lam_l,i) K_l,i U_l,j
 //          = D_t S_{t-1}, the decayed logical state (n = W - 1 stored records)
@@ -14,7 +15,10 @@
 //                     record would store them; y uses k and u themselves)
 //     B_i  = max_j |S_ij|,  s_i = B_i / 127,  Z_ij = rint(S_ij 127 / B_i)
 // (App. B.3), then lbar = 0 and the log is emptied.  y is read from the
-// unquantized state.  The codes and the records of a closing state are read
+// unquantized state.  The column-scale format (LeapQuant §3.4 eq. 7, App.
+// B.3) dequantizes the old base as c_i Z_ij b_j and quantizes the new state
+// as c_i = max(sqrt(mean_j |S_ij|), 2^-20), R = S / c (row-wise), b_j =
+// max_i |R_ij| / 127, Z_ij = rint(R_ij 127 / max_i |R_ij|).  The codes and the records of a closing state are read
 // once, here.
 //
 // The rank-n part is a GEMM, D = U^T A with D[j][i] (value column j in
@@ -45,10 +49,13 @@
 // words of a state hold 4 key rows of one value column, so each thread reads
 // and writes 32 whole words and a warp 128 contiguous bytes per access; a
 // key row's absmax over a warp's 32 columns is one redux.sync, over the
-// group's 4 warps a shared-memory max.  Pass 1 forms S (32 key rows at a
-// time) and the readouts and puts S back in tensor memory; pass 2 adds
-// k u^T, takes the row maxima and puts S back again; pass 3 writes the
-// codes, so no thread holds more than 32 of its 128 values.
+// group's 4 warps a shared-memory max (column scales: a row's sum of |S| by a
+// 31-shuffle reduce-scatter over the warp; a column's absmax is
+// thread-local).  Pass 1 forms S (32 key rows at a time) and the readouts
+// and puts S back in tensor memory; pass 2 adds k u^T, takes the row
+// statistics and puts S back again; (column scales: pass 3 puts R = S / c
+// back and takes the column's absmax;) the last pass writes the codes, so
+// no thread holds more than 32 of its 128 values.
 //
 // Queue protocol (pool memory, zeroed at creation): the step kernel appends
 // (state, row) pairs after atomically incrementing count; here groups take
@@ -86,12 +93,14 @@ struct alignas(128) GroupSmem {
     float hs[kD];
     float hlam[kD];
     float hlb[kD];
+    float hb[kD];                         // column-scale format: the old scales b_j
     float kk[kD];                         // the key of the state update, as a record
                                           //   stores it (the header is restaged
                                           //   after pass 2)
     float es[kD];                         // exp(lp_i) s_i
     float red[4][kD];                     // per-warp absmax of each key row
-    float fq[kD];                         // 127 / B_i
+    float fq[kD];                         // 127 / B_i (per-row scales) or the row
+                                          //   factors g_i = 1 / c_i (column scales)
     float gl[kChunkRecords];              // scalar gate: exp(lp - Lam_l) of the chunk
     float kqp[4];                         // per-warp partial sums of k.q
     uint64_t rec_bar;                     // records of a chunk
@@ -149,13 +158,13 @@ __device__ __forceinline__ void stage_records(const PoolView& pv, size_t hd, int
 
 // Stage the 16 KiB of codes and the header of state hd, whose closing token
 // is request row `row`, on st_bar (one thread).
-template <bool PER_KEY>
+template <bool PER_KEY, bool COLS>
 __device__ __forceinline__ void stage_state(const StepArgs& a, size_t hd, int row, GroupSmem& gs) {
     const PoolView& pv = a.pv;
     const unsigned char* src = reinterpret_cast<const unsigned char*>(pv.base) + hd * kCodeBytes;
     const size_t ro = static_cast<size_t>(row) * kD;
     fence_proxy_async();
-    mbar_arrive_expect_tx(&gs.st_bar, kCodeBytes + (PER_KEY ? 6 : 4) * kVecBytes);
+    mbar_arrive_expect_tx(&gs.st_bar, kCodeBytes + ((PER_KEY ? 6 : 4) + (COLS ? 1 : 0)) * kVecBytes);
 #pragma unroll
     for (int i = 0; i < 4; ++i)
         bulk_g2s(reinterpret_cast<unsigned char*>(gs.codes) + i * (kCodeBytes / 4), src + i * (kCodeBytes / 4),
@@ -168,6 +177,7 @@ __device__ __forceinline__ void stage_state(const StepArgs& a, size_t hd, int ro
         bulk_g2s(gs.hlam, a.lam + ro, kVecBytes, &gs.st_bar);
         bulk_g2s(gs.hlb, pv.lbar + hd * kD, kVecBytes, &gs.st_bar);
     }
+    if constexpr (COLS) bulk_g2s(gs.hb, pv.colf + hd * kD, kVecBytes, &gs.st_bar);
 }
 
 // Three MMAs per 8 records of the staged chunk (one thread).
@@ -206,8 +216,11 @@ __device__ __forceinline__ bool group_wait(const PoolView& pv, uint64_t* bar, ui
 }
 
 // The decayed, dequantized codes of key rows 32 qr .. 32 qr + 31 of value
-// column gt added to d (the rank-n fold of those rows).
-__device__ __forceinline__ void add_base_rows(const GroupSmem& gs, int qr, int gt, float (&d)[32]) {
+// column gt added to d (the rank-n fold of those rows); bj is the column's
+// scale (column-scale format) or 1.
+template <bool COLS>
+__device__ __forceinline__ void add_base_rows(const GroupSmem& gs, int qr, int gt, float bj, float (&d)[32]) {
+    const float2 b2 = make_float2(bj, bj);
 #pragma unroll
     for (int g = 0; g < 8; ++g) {
         const uint32_t w = gs.codes[(8 * qr + g) * kD + gt] ^ 0x80808080u;
@@ -218,13 +231,33 @@ __device__ __forceinline__ void add_base_rows(const GroupSmem& gs, int qr, int g
         const float2 z23 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7652)),
                                                   __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7653))),
                                       make_float2(-kCodeBias, -kCodeBias));
-        const float2 s01 = __ffma2_rn(z01, make_float2(e4.x, e4.y), make_float2(d[4 * g], d[4 * g + 1]));
-        const float2 s23 = __ffma2_rn(z23, make_float2(e4.z, e4.w), make_float2(d[4 * g + 2], d[4 * g + 3]));
+        const float2 s01 = __ffma2_rn(COLS ? __fmul2_rn(z01, b2) : z01, make_float2(e4.x, e4.y),
+                                      make_float2(d[4 * g], d[4 * g + 1]));
+        const float2 s23 = __ffma2_rn(COLS ? __fmul2_rn(z23, b2) : z23, make_float2(e4.z, e4.w),
+                                      make_float2(d[4 * g + 2], d[4 * g + 3]));
         d[4 * g + 0] = s01.x;
         d[4 * g + 1] = s01.y;
         d[4 * g + 2] = s23.x;
         d[4 * g + 3] = s23.y;
     }
+}
+
+// Sum over the warp's 32 lanes of each of 32 per-lane values |v[r]| (one
+// per key row), by recursive halving: 31 shuffles.  Lane l returns the sum
+// for row l.
+__device__ __forceinline__ float warp_abs_sum32_scatter(float (&v)[32], int lane) {
+#pragma unroll
+    for (int b = 4, h = 16; b >= 0; --b, h >>= 1) {
+        const bool upper = (lane >> b) & 1;
+#pragma unroll
+        for (int r = 0; r < h; ++r) {
+            const float send = upper ? v[r] : v[r + h];
+            const float keep = upper ? v[r + h] : v[r];
+            const float got = __shfl_xor_sync(0xffffffffu, send, 1 << b);
+            v[r] = h == 16 ? fabsf(keep) + fabsf(got) : keep + got;
+        }
+    }
+    return v[0];
 }
 
 // A key factor as a log record stores it: bfloat16 (k16), binary16 (rec16)
@@ -259,7 +292,7 @@ __device__ __forceinline__ void add_token_rows(const GroupSmem& gs, int qr, floa
 // records, and after pass 2 (the codes and the header are consumed) its codes
 // and header, so the copies overlap this state's epilogue.  Returns false after a
 // timeout (flagged).
-template <bool PER_KEY>
+template <bool PER_KEY, bool COLS>
 __device__ __forceinline__ bool fold_state(const StepArgs& a, size_t hd, int row, float lb_scalar,
                                            float lam_scalar, float beta, GroupSmem& gs, GroupPipe& gp,
                                            uint32_t tmem, uint32_t tlane, int bar_id, int gt, int lane, int gw,
@@ -291,6 +324,7 @@ __device__ __forceinline__ bool fold_state(const StepArgs& a, size_t hd, int row
     // keys, binary16 records); the token's own output uses k itself
     gs.kk[gt] = stored_key(gs.hk[gt], pv);
     const float vj = gs.hv[gt];
+    const float bj = COLS ? gs.hb[gt] : 1.0f;  // the old scale of this thread's value column
     {
         const float kq_part = warp_sum(gs.hk[gt] * gs.hq[gt]);
         if (lane == 0) gs.kqp[gw] = kq_part;
@@ -374,7 +408,7 @@ __device__ __forceinline__ bool fold_state(const StepArgs& a, size_t hd, int row
 #pragma unroll
             for (int c = 0; c < 32; ++c) d[c] = 0.0f;
         }
-        add_base_rows(gs, qr, gt, d);
+        add_base_rows<COLS>(gs, qr, gt, bj, d);
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
             const float4 k4 = reinterpret_cast<const float4*>(gs.hk)[8 * qr + g];  // k itself
@@ -392,20 +426,24 @@ __device__ __forceinline__ bool fold_state(const StepArgs& a, size_t hd, int row
     const float u_out = beta * (vj - r);
     a.y[static_cast<size_t>(row) * kD + gt] = fmaf(kq, u_out, y0);
     const float uj = pv.rec16 ? __half2float(__float2half_rn(u_out)) : u_out;  // as a record stores it
-    // pass 2: S + k u^T back to tensor memory; each key row's absmax over
-    // this warp's columns
+    // pass 2: S + k u^T back to tensor memory; per key row over this warp's
+    // columns, the absmax (per-row scales) or the sum of |S| (column scales)
 #pragma unroll
     for (int qr = 0; qr < 4; ++qr) {
         float d[32];
         tmem_ld32(tlane + 32u * qr, d);
         add_token_rows(gs, qr, uj, d);
-#pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-            const float4 m = make_float4(warp_absmax_redux(d[c]), warp_absmax_redux(d[c + 1]),
-                                         warp_absmax_redux(d[c + 2]), warp_absmax_redux(d[c + 3]));
-            if (lane == 0) reinterpret_cast<float4*>(gs.red[gw])[8 * qr + c / 4] = m;
-        }
         tmem_st32(tlane + 32u * qr, d);
+        if constexpr (COLS) {
+            gs.red[gw][32 * qr + lane] = warp_abs_sum32_scatter(d, lane);
+        } else {
+#pragma unroll
+            for (int c = 0; c < 32; c += 4) {
+                const float4 m = make_float4(warp_absmax_redux(d[c]), warp_absmax_redux(d[c + 1]),
+                                             warp_absmax_redux(d[c + 2]), warp_absmax_redux(d[c + 3]));
+                if (lane == 0) reinterpret_cast<float4*>(gs.red[gw])[8 * qr + c / 4] = m;
+            }
+        }
     }
     tc_fence_before();
     if (gt == 0) {
@@ -416,12 +454,19 @@ __device__ __forceinline__ bool fold_state(const StepArgs& a, size_t hd, int row
         gs.next_lam = next_lam;
         gs.next_beta = next_beta;
     }
-    named_barrier(bar_id, kGroupThreads);  // row maxima complete; codes and header consumed
+    named_barrier(bar_id, kGroupThreads);  // row statistics complete; codes and header consumed
     if (gt == 0 && next_hd >= 0) {
-        stage_state<PER_KEY>(a, static_cast<size_t>(next_hd), next_row, gs);
+        stage_state<PER_KEY, COLS>(a, static_cast<size_t>(next_hd), next_row, gs);
         gp.st_out = true;
     }
-    {
+    if constexpr (COLS) {
+        // smoothing factor c_i = max(sqrt(mean_j |S_ij|), 2^-20) and g_i = 1 / c_i
+        // (LeapQuant §3.4 eq. 7; the floor's value is a reading of the page)
+        float c = sqrtf(((gs.red[0][gt] + gs.red[1][gt]) + (gs.red[2][gt] + gs.red[3][gt])) * (1.0f / kD));
+        if (!(c >= kSmoothFloor)) c = kSmoothFloor;
+        pv.scale[hd * kD + gt] = c;
+        gs.fq[gt] = __fdiv_rn(1.0f, c);
+    } else {
         const float B = fmaxf(fmaxf(gs.red[0][gt], gs.red[1][gt]), fmaxf(gs.red[2][gt], gs.red[3][gt]));
         float sc, f;
         row_quant_params(B, sc, f);
@@ -430,8 +475,33 @@ __device__ __forceinline__ bool fold_state(const StepArgs& a, size_t hd, int row
     }
     named_barrier(bar_id, kGroupThreads);
     tc_fence_after();
-    // pass 3: codes rint(S 127 / B_i), four key rows per word, one warp
-    // writing 128 contiguous bytes per store
+    float fj = 0.0f;  // column-scale format: 127 / B_j of this thread's column
+    if constexpr (COLS) {
+        // pass 3: R = S g_i back to tensor memory, this column's absmax B_j
+        float B = 0.0f;
+#pragma unroll
+        for (int qr = 0; qr < 4; ++qr) {
+            float d[32];
+            tmem_ld32(tlane + 32u * qr, d);
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+                const float4 g4 = reinterpret_cast<const float4*>(gs.fq)[8 * qr + g];
+                const float2 a2 = __fmul2_rn(make_float2(d[4 * g], d[4 * g + 1]), make_float2(g4.x, g4.y));
+                const float2 b2 = __fmul2_rn(make_float2(d[4 * g + 2], d[4 * g + 3]), make_float2(g4.z, g4.w));
+                d[4 * g] = a2.x;
+                d[4 * g + 1] = a2.y;
+                d[4 * g + 2] = b2.x;
+                d[4 * g + 3] = b2.y;
+                B = fmaxf(B, fmaxf(fmaxf(fabsf(a2.x), fabsf(a2.y)), fmaxf(fabsf(b2.x), fabsf(b2.y))));
+            }
+            tmem_st32(tlane + 32u * qr, d);
+        }
+        float bcol;
+        row_quant_params(B, bcol, fj);  // b_j = B_j / 127, f_j = 127 / B_j (App. B.3)
+        pv.colf[hd * kD + gt] = bcol;
+    }
+    // last pass: codes rint(S 127 / B_i), or rint(R_ij 127 / B_j), four key rows
+    // per word, one warp writing 128 contiguous bytes per store
     uint32_t* const words = reinterpret_cast<uint32_t*>(pv.base) + hd * (kCodeBytes / 4) + gt;
 #pragma unroll
     for (int qr = 0; qr < 4; ++qr) {
@@ -439,9 +509,15 @@ __device__ __forceinline__ bool fold_state(const StepArgs& a, size_t hd, int row
         tmem_ld32(tlane + 32u * qr, d);
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
-            const float4 f4 = reinterpret_cast<const float4*>(gs.fq)[8 * qr + g];
-            const float2 a2 = code_words2(make_float2(d[4 * g], d[4 * g + 1]), make_float2(f4.x, f4.y));
-            const float2 b2 = code_words2(make_float2(d[4 * g + 2], d[4 * g + 3]), make_float2(f4.z, f4.w));
+            float2 a2, b2;
+            if constexpr (COLS) {
+                a2 = code_words(make_float2(d[4 * g], d[4 * g + 1]), fj);
+                b2 = code_words(make_float2(d[4 * g + 2], d[4 * g + 3]), fj);
+            } else {
+                const float4 f4 = reinterpret_cast<const float4*>(gs.fq)[8 * qr + g];
+                a2 = code_words2(make_float2(d[4 * g], d[4 * g + 1]), make_float2(f4.x, f4.y));
+                b2 = code_words2(make_float2(d[4 * g + 2], d[4 * g + 3]), make_float2(f4.z, f4.w));
+            }
             words[(8 * qr + g) * kD] = pack_low_bytes(a2.x, a2.y, b2.x, b2.y);
         }
     }
@@ -456,7 +532,7 @@ __device__ __forceinline__ bool fold_state(const StepArgs& a, size_t hd, int row
     return true;
 }
 
-template <bool PER_KEY>
+template <bool PER_KEY, bool COLS>
 __global__ void __launch_bounds__(kFoldThreads, 1) window_fold_kernel(const StepArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ uint32_t tmem_base;
@@ -492,7 +568,7 @@ __global__ void __launch_bounds__(kFoldThreads, 1) window_fold_kernel(const Step
                 gs.next_lam = __ldg(a.lam + it.y);
             }
             gs.next_beta = __ldg(a.beta + it.y);
-            stage_state<PER_KEY>(a, static_cast<size_t>(it.x), it.y, gs);
+            stage_state<PER_KEY, COLS>(a, static_cast<size_t>(it.x), it.y, gs);
             gp.st_out = true;
             if (n > 0) {
                 stage_records<PER_KEY>(pv, static_cast<size_t>(it.x), 0, min(kChunkRecords, n), gs);
@@ -512,7 +588,8 @@ __global__ void __launch_bounds__(kFoldThreads, 1) window_fold_kernel(const Step
         const size_t hd = static_cast<size_t>(gs.next_hd);
         const int row = gs.next_row;
         const float lb = gs.next_lb, lam = gs.next_lam, beta = gs.next_beta;
-        if (!fold_state<PER_KEY>(a, hd, row, lb, lam, beta, gs, gp, tmem, tlane, bar_id, gt, lane, gw, count)) {
+        if (!fold_state<PER_KEY, COLS>(a, hd, row, lb, lam, beta, gs, gp, tmem, tlane, bar_id, gt, lane, gw,
+                                       count)) {
             // after a timeout: let this group's copies and MMAs land before exit
             if (gt == 0) {
                 if (gp.rec_out) mbar_wait_bounded(&gs.rec_bar, gp.rec_ph);
@@ -540,10 +617,12 @@ __global__ void __launch_bounds__(kFoldThreads, 1) window_fold_kernel(const Step
 
 cudaError_t prepare_window_fold_kernels() {
     const int bytes = static_cast<int>(window_fold_smem_bytes());
-    cudaError_t e = cudaFuncSetAttribute(window_fold_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         bytes);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(window_fold_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    const cudaFuncAttribute attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(window_fold_kernel<false, false>, attr, bytes)) != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(window_fold_kernel<true, false>, attr, bytes)) != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(window_fold_kernel<false, true>, attr, bytes)) != cudaSuccess) return e;
+    return cudaFuncSetAttribute(window_fold_kernel<true, true>, attr, bytes);
 }
 
 cudaError_t launch_window_fold(const StepArgs& a, bool per_key, cudaStream_t s) {
@@ -557,8 +636,11 @@ cudaError_t launch_window_fold(const StepArgs& a, bool per_key, cudaStream_t s) 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return per_key ? cudaLaunchKernelEx(&cfg, window_fold_kernel<true>, a)
-                   : cudaLaunchKernelEx(&cfg, window_fold_kernel<false>, a);
+    if (a.pv.colf != nullptr)
+        return per_key ? cudaLaunchKernelEx(&cfg, window_fold_kernel<true, true>, a)
+                       : cudaLaunchKernelEx(&cfg, window_fold_kernel<false, true>, a);
+    return per_key ? cudaLaunchKernelEx(&cfg, window_fold_kernel<true, false>, a)
+                   : cudaLaunchKernelEx(&cfg, window_fold_kernel<false, false>, a);
 }
 
 }  // namespace ls

@@ -93,8 +93,8 @@ def test_column_scale_flag(lib):
     al = lambda x: (x + 255) // 256 * 256
     rc0, b0 = _bytes(lib, _desc())
     rc1, b1 = _bytes(lib, _desc(flags=N.LS_INT8_COLUMN_SCALES))
-    # no window-end queue: the column-scale format folds inside the step kernel
-    assert rc0 == 0 and rc1 == 0 and b1 == b0 + al(nh * 128 * 4) - al(16 + nh * 4)
+    # both formats keep the window-end queue of the tensor-core fold
+    assert rc0 == 0 and rc1 == 0 and b1 == b0 + al(nh * 128 * 4)
     for variant in (N.LS_EAGER_FP32, N.LS_DEFERRED_FP32):
         rc, _ = _bytes(lib, _desc(variant=variant, flags=N.LS_INT8_COLUMN_SCALES))
         assert rc == N.LS_ERR_INVALID
