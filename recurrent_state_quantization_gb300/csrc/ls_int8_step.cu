@@ -196,16 +196,15 @@ __device__ __forceinline__ void i8_issue(I8Warp& ws, const StepArgs& a, int row,
     }
 }
 
+// One warp decodes request row `row` (one head).  Returns (state index,
+// row) when the token closes the state's window and is left to the
+// window-end kernel, else (-1, -1).
 template <bool PER_KEY, bool SPLIT, int REC>
-__global__ void __launch_bounds__(kI8Threads, 4) int8_step_kernel(const StepArgs a) {
-    extern __shared__ __align__(128) unsigned char smem[];
+__device__ __forceinline__ int2 i8_warp_step(const StepArgs& a, I8Warp& ws, int row) {
     constexpr int EPC = I8Plan<PER_KEY, SPLIT>::EPC;
-    pdl_enter();
+    const int2 none = make_int2(-1, -1);
     const PoolView& pv = a.pv;
     const int lane = threadIdx.x & 31;
-    const int row = blockIdx.x * kI8Warps + (threadIdx.x >> 5);
-    if (row >= a.batch * pv.H) return;
-    I8Warp& ws = reinterpret_cast<I8Warp*>(smem)[threadIdx.x >> 5];
     const int H = pv.H, W = pv.cap;  // W: log capacity (window + compensator pairs)
     const int b = row / H, h = row - b * H;
     const size_t ro = static_cast<size_t>(row) * kD + 4 * lane;
@@ -215,24 +214,20 @@ __global__ void __launch_bounds__(kI8Threads, 4) int8_step_kernel(const StepArgs
     if (slot < 0 || slot >= pv.P) {
         if (lane == 0) flag_status(pv.status, kDevSlotRange);
         st4(a.y + ro, nan4);
-        return;
+        return none;
     }
     const size_t hd = static_cast<size_t>(slot) * H + h;
     const int L = pv.len[hd];
     if (L < 0 || L >= W) {  // the pool memory of this state was overwritten
         if (lane == 0) flag_status(pv.status, kDevBadState);
         st4(a.y + ro, nan4);
-        return;
+        return none;
     }
     if (L + 1 == W) {
         // the token closes the state's window: the whole token (its output, the
         // fold of the W - 1 stored records and the requantization) is left to
         // the window-end kernel, which reads the codes and records once
-        if (lane == 0) {
-            const int i = atomicAdd(pv.foldq, 1);
-            reinterpret_cast<int2*>(pv.foldq + 4)[i] = make_int2(static_cast<int>(hd), row);
-        }
-        return;
+        return make_int2(static_cast<int>(hd), row);
     }
     if (lane == 0) {
 #pragma unroll
@@ -269,7 +264,7 @@ __global__ void __launch_bounds__(kI8Threads, 4) int8_step_kernel(const StepArgs
             }
             __syncwarp();
             st4(a.y + ro, nan4);
-            return;
+            return none;
         }
         const unsigned char* st = ws.ring[stg];
         const float4* st4p = reinterpret_cast<const float4*>(st);
@@ -413,6 +408,34 @@ __global__ void __launch_bounds__(kI8Threads, 4) int8_step_kernel(const StepArgs
         pv.lbar[hd] = lp4.x;
     }
     if (lane == 0) pv.len[hd] = L + 1;
+    return none;
+}
+
+// The queue of closing tokens is appended once per CTA (one atomic for the
+// CTA's closing heads), not once per head.
+template <bool PER_KEY, bool SPLIT, int REC>
+__global__ void __launch_bounds__(kI8Threads, 4) int8_step_kernel(const StepArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int2 closing[kI8Warps];
+    pdl_enter();
+    const int warp = threadIdx.x >> 5;
+    const int row = blockIdx.x * kI8Warps + warp;
+    int2 e = make_int2(-1, -1);
+    if (row < a.batch * a.pv.H) e = i8_warp_step<PER_KEY, SPLIT, REC>(a, reinterpret_cast<I8Warp*>(smem)[warp], row);
+    if ((threadIdx.x & 31) == 0) closing[warp] = e;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int n = 0;
+#pragma unroll
+        for (int w = 0; w < kI8Warps; ++w) n += closing[w].x >= 0 ? 1 : 0;
+        if (n > 0) {
+            int i = atomicAdd(a.pv.foldq, n);
+            int2* const q = reinterpret_cast<int2*>(a.pv.foldq + 4);
+#pragma unroll
+            for (int w = 0; w < kI8Warps; ++w)
+                if (closing[w].x >= 0) q[i++] = closing[w];
+        }
+    }
 }
 
 // Shared memory per CTA, and the largest shared-memory carveout so that four
