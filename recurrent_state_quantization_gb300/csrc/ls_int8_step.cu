@@ -217,29 +217,44 @@ __device__ __forceinline__ int2 i8_warp_step(const StepArgs& a, I8Warp& ws, int 
         return none;
     }
     const size_t hd = static_cast<size_t>(slot) * H + h;
-    const int L = pv.len[hd];
-    if (L < 0 || L >= W) {  // the pool memory of this state was overwritten
-        if (lane == 0) flag_status(pv.status, kDevBadState);
-        st4(a.y + ro, nan4);
-        return none;
-    }
-    if (L + 1 == W) {
-        // the token closes the state's window: the whole token (its output, the
-        // fold of the W - 1 stored records and the requantization) is left to
-        // the window-end kernel, which reads the codes and records once
-        return make_int2(static_cast<int>(hd), row);
-    }
+    // the inputs and the first code chunk do not depend on the log length, so
+    // they are in flight while it is read (for a token that closes its window
+    // they bring into L2 what the window-end kernel reads next)
+    constexpr int kEarly = 2;
+    static_assert(kEarly <= kI8Ring && kEarly <= kI8LogItem0, "early items are never log chunks");
     if (lane == 0) {
 #pragma unroll
         for (int s = 0; s < kI8Ring; ++s) mbar_init(&ws.bar[s], 1);
         mbar_fence_init();
-        // the first kI8Ring items are never log chunks
 #pragma unroll
-        for (int it = 0; it < kI8Ring; ++it) i8_issue<PER_KEY, SPLIT, REC>(ws, a, row, hd, L, it);
+        for (int it = 0; it < kEarly; ++it) i8_issue<PER_KEY, SPLIT, REC>(ws, a, row, hd, 0, it);
     }
+    const int L = pv.len[hd];
     const float beta = __ldg(a.beta + row);
     float lp_scalar = 0.0f;
     if constexpr (!PER_KEY) lp_scalar = pv.lbar[hd] + __ldg(a.lam + row);
+    const bool bad = L < 0 || L >= W;  // the pool memory of this state was overwritten
+    if (bad || L + 1 == W) {
+        // a bad state is skipped; a token that closes its window is left whole
+        // (its output, the fold of the W - 1 stored records, the
+        // requantization) to the window-end kernel, which reads the codes and
+        // records once.  Either way the early copies land before the warp leaves.
+        if (lane == 0) {
+            if (bad) flag_status(pv.status, kDevBadState);
+            for (int s = 0; s < kEarly; ++s)
+                if (!mbar_wait_bounded(&ws.bar[s], 0)) flag_status(pv.status, kDevTimeout);
+        }
+        __syncwarp();
+        if (bad) {
+            st4(a.y + ro, nan4);
+            return none;
+        }
+        return make_int2(static_cast<int>(hd), row);
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int it = kEarly; it < kI8Ring; ++it) i8_issue<PER_KEY, SPLIT, REC>(ws, a, row, hd, L, it);
+    }
     __syncwarp();
     const int NI = kI8LogItem0 + (L + EPC - 1) / EPC;
 
