@@ -228,6 +228,14 @@ __host__ __device__ __forceinline__ uint32_t key_bytes(const PoolView& pv) {
 }
 __host__ __device__ __forceinline__ uint32_t val_bytes(const PoolView& pv) { return pv.rec16 ? 2u : 4u; }
 
+// exp(d) of a replay decay d = lp - Lambda_l <= 0 (per-key gate: four per lane
+// and log entry), by the hardware exponential: relative error about 2^-21
+// plus |d| 2^-24, with |d| at most a window's cumulative log-decay, far inside
+// the FP32 tolerance of the readouts.  Every replay of a log entry (the fused
+// step kernels and the split-replay prepare kernel) uses this one function,
+// so the split and fused paths stay bit-identical.
+__device__ __forceinline__ float replay_decay(float d) { return __expf(d); }
+
 // Log record formats, a template parameter of the step kernels so that the
 // per-entry replay carries no format branches: FP32 key and value factors,
 // bfloat16 keys (DeltaLog §3.4), or binary16 keys and values (LeapQuant

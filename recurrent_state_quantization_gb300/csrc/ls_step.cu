@@ -379,8 +379,8 @@ __device__ __forceinline__ long long warp_step(const StepArgs& a, WarpSmem& ws, 
                 float ck, cq;
                 if constexpr (PER_KEY) {
                     const float4 Lm = st4p[(2 * P::EPC + e) * 32 + lane];
-                    const float ax = K4.x * expf(lp4.x - Lm.x), ay = K4.y * expf(lp4.y - Lm.y);
-                    const float az = K4.z * expf(lp4.z - Lm.z), aw = K4.w * expf(lp4.w - Lm.w);
+                    const float ax = K4.x * replay_decay(lp4.x - Lm.x), ay = K4.y * replay_decay(lp4.y - Lm.y);
+                    const float az = K4.z * replay_decay(lp4.z - Lm.z), aw = K4.w * replay_decay(lp4.w - Lm.w);
                     ck = warp_sum(fmaf(ax, k4.x, fmaf(ay, k4.y, fmaf(az, k4.z, aw * k4.w))));
                     cq = warp_sum(fmaf(ax, q4.x, fmaf(ay, q4.y, fmaf(az, q4.z, aw * q4.w))));
                 } else {
@@ -560,8 +560,8 @@ __global__ void __launch_bounds__(kThreads) replay_prepare_kernel(const StepArgs
         if constexpr (PER_KEY) {
             const float4 Lm = *reinterpret_cast<const float4*>(pv.lamlog + lb0 + static_cast<size_t>(e) * kD +
                                                                 4 * lane);
-            const float ax = K4.x * expf(lp4.x - Lm.x), ay = K4.y * expf(lp4.y - Lm.y);
-            const float az = K4.z * expf(lp4.z - Lm.z), aw = K4.w * expf(lp4.w - Lm.w);
+            const float ax = K4.x * replay_decay(lp4.x - Lm.x), ay = K4.y * replay_decay(lp4.y - Lm.y);
+            const float az = K4.z * replay_decay(lp4.z - Lm.z), aw = K4.w * replay_decay(lp4.w - Lm.w);
             ck = warp_sum(fmaf(ax, k4.x, fmaf(ay, k4.y, fmaf(az, k4.z, aw * k4.w))));
             cq = warp_sum(fmaf(ax, q4.x, fmaf(ay, q4.y, fmaf(az, q4.z, aw * q4.w))));
         } else {
