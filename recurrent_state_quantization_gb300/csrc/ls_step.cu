@@ -630,10 +630,8 @@ cudaError_t launch_step_kernel(const StepArgs& a, bool per_key, dim3 grid, cudaS
 cudaError_t prepare_log_step_kernels() {
     cudaError_t e;
     if ((e = prepare_formats<false, false, false>()) != cudaSuccess) return e;
-    if ((e = prepare_formats<true, false, false>()) != cudaSuccess) return e;
     if ((e = prepare_formats<true, true, false>()) != cudaSuccess) return e;
     if ((e = prepare_formats<false, false, true>()) != cudaSuccess) return e;
-    if ((e = prepare_formats<true, false, true>()) != cudaSuccess) return e;
     return prepare_formats<true, true, true>();
 }
 
@@ -641,10 +639,10 @@ cudaError_t launch_log_step(const StepArgs& a, bool int8, bool per_key, cudaStre
     const int64_t rows = static_cast<int64_t>(a.batch) * a.pv.H;
     const dim3 grid(static_cast<unsigned>((rows + kWarps - 1) / kWarps));
     if (!int8) return launch_step_kernel<false, false, false>(a, per_key, grid, s);
+    // INT8 without compensator pairs: the INT8 step and window-end kernels;
+    // with pairs: this kernel, which also fits them at the window end
     if (a.pv.foldq != nullptr) return launch_int8_step(a, per_key, false, s);
-    if (a.pv.R > 0)  // compensator pairs: the kernel that also fits them
-        return launch_step_kernel<true, true, false>(a, per_key, grid, s);
-    return launch_step_kernel<true, false, false>(a, per_key, grid, s);
+    return launch_step_kernel<true, true, false>(a, per_key, grid, s);
 }
 
 cudaError_t launch_log_step_split(const StepArgs& a, bool int8, bool per_key, cudaStream_t s) {
@@ -660,8 +658,7 @@ cudaError_t launch_log_step_split(const StepArgs& a, bool int8, bool per_key, cu
     if (e != cudaSuccess) return e;
     if (!int8) return launch_step_kernel<false, false, true>(a, per_key, grid, s);
     if (a.pv.foldq != nullptr) return launch_int8_step(a, per_key, true, s);
-    if (a.pv.R > 0) return launch_step_kernel<true, true, true>(a, per_key, grid, s);
-    return launch_step_kernel<true, false, true>(a, per_key, grid, s);
+    return launch_step_kernel<true, true, true>(a, per_key, grid, s);
 }
 
 }  // namespace ls
