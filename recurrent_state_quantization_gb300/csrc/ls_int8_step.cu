@@ -196,6 +196,28 @@ __device__ __forceinline__ void i8_issue(I8Warp& ws, const StepArgs& a, int row,
     }
 }
 
+// Wait (bounded) for item `it` of the warp's ring; warp-uniform result.  On
+// a timeout the status is flagged and the items still in flight (it ..
+// min(NI, it + kI8Ring) - 1) are waited for, so that no copy lands after the
+// warp has left.
+__device__ __forceinline__ bool i8_wait(I8Warp& ws, const PoolView& pv, int it, int NI) {
+    const bool ok = mbar_wait_bounded(&ws.bar[it % kI8Ring], (it / kI8Ring) & 1);
+    if (!__any_sync(0xffffffffu, !ok)) return true;
+    if ((threadIdx.x & 31) == 0) {
+        flag_status(pv.status, kDevTimeout);
+        for (int j = it; j < min(NI, it + kI8Ring); ++j) mbar_wait_bounded(&ws.bar[j % kI8Ring], (j / kI8Ring) & 1);
+    }
+    __syncwarp();
+    return false;
+}
+
+// The output row of a head given up after a timeout: NaN.
+__device__ __forceinline__ int2 i8_abandon(const StepArgs& a, size_t ro) {
+    const float nan = __int_as_float(0x7fc00000);
+    st4(a.y + ro, make_float4(nan, nan, nan, nan));
+    return make_int2(-1, -1);
+}
+
 // One warp decodes request row `row` (one head).  Returns (state index,
 // row) when the token closes the state's window and is left to the
 // window-end kernel, else (-1, -1).
@@ -258,6 +280,10 @@ __device__ __forceinline__ int2 i8_warp_step(const StepArgs& a, I8Warp& ws, int 
     __syncwarp();
     const int NI = kI8LogItem0 + (L + EPC - 1) / EPC;
 
+    // The items are consumed in straight-line code: the first kI8LogItem0
+    // items have fixed kinds, stages and phases, so each one's wait and the
+    // copy issued behind it compile to their own few instructions; only the
+    // log chunks run in a loop.
     float4 k4, q4, v4, lp4;
     float kq = 0.0f, unit_k = 0.0f, unit_q = 0.0f;
     float2 r01 = make_float2(0.f, 0.f), r23 = r01, y01 = r01, y23 = r01;
@@ -266,96 +292,106 @@ __device__ __forceinline__ int2 i8_warp_step(const StepArgs& a, I8Warp& ws, int 
     for (int m = 0; m < 4; ++m)
 #pragma unroll
         for (int d = 0; d < 3; ++d) acck[m][d] = accq[m][d] = 0;
-#pragma unroll 1
-    for (int it = 0; it < NI; ++it) {
-        const int stg = it % kI8Ring;
-        const bool ok = mbar_wait_bounded(&ws.bar[stg], (it / kI8Ring) & 1);
-        if (__any_sync(0xffffffffu, !ok)) {
-            // a copy did not land: flag, drain what is still in flight, give up
-            if (lane == 0) {
-                flag_status(pv.status, kDevTimeout);
-                for (int j = it; j < min(NI, it + kI8Ring); ++j)
-                    mbar_wait_bounded(&ws.bar[j % kI8Ring], (j / kI8Ring) & 1);
-            }
-            __syncwarp();
-            st4(a.y + ro, nan4);
-            return none;
+
+    // item 0: read vectors e . s . k and e . s . q as fixed-point digits
+    if (!i8_wait(ws, pv, 0, NI)) return i8_abandon(a, ro);
+    {
+        const float4* st4p = reinterpret_cast<const float4*>(ws.ring[0]);
+        const float4 kk = st4p[lane];
+        const float4 qq = st4p[32 + lane];
+        const float4 s4 = st4p[64 + lane];  // key-row factors
+        float4 es;
+        if constexpr (PER_KEY) {
+            const float4 lam4 = st4p[96 + lane];
+            const float4 lb4 = st4p[128 + lane];
+            es = make_float4(expf(lb4.x + lam4.x) * s4.x, expf(lb4.y + lam4.y) * s4.y,
+                             expf(lb4.z + lam4.z) * s4.z, expf(lb4.w + lam4.w) * s4.w);
+        } else {
+            const float e = expf(lp_scalar);
+            es = make_float4(e * s4.x, e * s4.y, e * s4.z, e * s4.w);
         }
-        const unsigned char* st = ws.ring[stg];
-        const float4* st4p = reinterpret_cast<const float4*>(st);
-        if (it == 0) {
-            // read vectors e . s . k and e . s . q as fixed-point digits
-            const float4 kk = st4p[lane];
-            const float4 qq = st4p[32 + lane];
-            const float4 s4 = st4p[64 + lane];  // key-row factors
-            float4 es;
-            if constexpr (PER_KEY) {
-                const float4 lam4 = st4p[96 + lane];
-                const float4 lb4 = st4p[128 + lane];
-                es = make_float4(expf(lb4.x + lam4.x) * s4.x, expf(lb4.y + lam4.y) * s4.y,
-                                 expf(lb4.z + lam4.z) * s4.z, expf(lb4.w + lam4.w) * s4.w);
-            } else {
-                const float e = expf(lp_scalar);
-                es = make_float4(e * s4.x, e * s4.y, e * s4.z, e * s4.w);
-            }
-            const uint3 dk = fixed_point_digits(es.x * kk.x, es.y * kk.y, es.z * kk.z, es.w * kk.w, &unit_k);
-            const uint3 dq = fixed_point_digits(es.x * qq.x, es.y * qq.y, es.z * qq.z, es.w * qq.w, &unit_q);
-            ws.dig[lane][0] = make_uint4(dk.x, dk.y, dk.z, dq.x);
-            reinterpret_cast<uint2*>(&ws.dig[lane][1])[0] = make_uint2(dq.y, dq.z);
-            __syncwarp();  // the digits visible to every lane before the code chunks
-        } else if (it <= kI8CodeItems) {
-            // exact integer GEMVs over this chunk's 32 key rows; the lane keeps
-            // its 4 value columns
-            const int g0 = (it - 1) * 8;
+        const uint3 dk = fixed_point_digits(es.x * kk.x, es.y * kk.y, es.z * kk.z, es.w * kk.w, &unit_k);
+        const uint3 dq = fixed_point_digits(es.x * qq.x, es.y * qq.y, es.z * qq.z, es.w * qq.w, &unit_q);
+        ws.dig[lane][0] = make_uint4(dk.x, dk.y, dk.z, dq.x);
+        reinterpret_cast<uint2*>(&ws.dig[lane][1])[0] = make_uint2(dq.y, dq.z);
+    }
+    __syncwarp();  // the stage is read and the digits are visible to every lane
+    if (lane == 0) i8_issue<PER_KEY, SPLIT, REC>(ws, a, row, hd, L, kI8Ring);
+
+    // items 1 .. 4: exact integer GEMVs over 32 key rows each; the lane keeps
+    // its 4 value columns
 #pragma unroll
-            for (int g = 0; g < 8; ++g) {
-                const uint4 cw = reinterpret_cast<const uint4*>(st)[g * 32 + lane];
-                const uint4 d0 = ws.dig[g0 + g][0];  // k0, k1, k2, q0
-                const uint2 d1 = reinterpret_cast<const uint2*>(&ws.dig[g0 + g][1])[0];  // q1, q2
-                const int col[4] = {static_cast<int>(cw.x), static_cast<int>(cw.y), static_cast<int>(cw.z),
-                                    static_cast<int>(cw.w)};
+    for (int it = 1; it <= kI8CodeItems; ++it) {
+        if (!i8_wait(ws, pv, it, NI)) return i8_abandon(a, ro);
+        const uint4* cw4 = reinterpret_cast<const uint4*>(ws.ring[it % kI8Ring]);
+        const int g0 = (it - 1) * 8;
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    acck[m][0] = dp4a_su(col[m], d0.x, acck[m][0]);
-                    acck[m][1] = dp4a_su(col[m], d0.y, acck[m][1]);
-                    acck[m][2] = dp4a_ss(col[m], d0.z, acck[m][2]);
-                    accq[m][0] = dp4a_su(col[m], d0.w, accq[m][0]);
-                    accq[m][1] = dp4a_su(col[m], d1.x, accq[m][1]);
-                    accq[m][2] = dp4a_ss(col[m], d1.y, accq[m][2]);
-                }
-            }
-        } else if (it == kI8TailItem) {
-            // sum_d acc_d 256^d: digits 0 and 1 pair exactly in int32
-            // (|acc_d| <= 128 * 127 * 255), digit 2 joins in one FMA; then the
-            // unit and the column scales (eq. 10: applied to the column sums)
-            v4 = st4p[lane];
-            k4 = st4p[32 + lane];
-            q4 = st4p[64 + lane];
-            if constexpr (PER_KEY) {
-                const float4 lam4 = st4p[96 + lane];
-                const float4 lb4 = st4p[128 + lane];
-                lp4 = make_float4(lb4.x + lam4.x, lb4.y + lam4.y, lb4.z + lam4.z, lb4.w + lam4.w);
-            } else {
-                lp4 = make_float4(lp_scalar, lp_scalar, lp_scalar, lp_scalar);
-            }
-            kq = warp_sum(fmaf(k4.x, q4.x, fmaf(k4.y, q4.y, fmaf(k4.z, q4.z, k4.w * q4.w))));
-            const float4 colf4 =
-                pv.colf != nullptr ? st4p[(PER_KEY ? 160 : 96) + lane] : make_float4(1.f, 1.f, 1.f, 1.f);
-            float rk[4], rq[4];
+        for (int g = 0; g < 8; ++g) {
+            const uint4 cw = cw4[g * 32 + lane];
+            const uint4 d0 = ws.dig[g0 + g][0];  // k0, k1, k2, q0
+            const uint2 d1 = reinterpret_cast<const uint2*>(&ws.dig[g0 + g][1])[0];  // q1, q2
+            const int col[4] = {static_cast<int>(cw.x), static_cast<int>(cw.y), static_cast<int>(cw.z),
+                                static_cast<int>(cw.w)};
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
-                const int k01 = acck[m][0] + (acck[m][1] << 8), q01 = accq[m][0] + (accq[m][1] << 8);
-                rk[m] = fmaf(static_cast<float>(acck[m][2]), 65536.0f, static_cast<float>(k01)) * unit_k;
-                rq[m] = fmaf(static_cast<float>(accq[m][2]), 65536.0f, static_cast<float>(q01)) * unit_q;
+                acck[m][0] = dp4a_su(col[m], d0.x, acck[m][0]);
+                acck[m][1] = dp4a_su(col[m], d0.y, acck[m][1]);
+                acck[m][2] = dp4a_ss(col[m], d0.z, acck[m][2]);
+                accq[m][0] = dp4a_su(col[m], d0.w, accq[m][0]);
+                accq[m][1] = dp4a_su(col[m], d1.x, accq[m][1]);
+                accq[m][2] = dp4a_ss(col[m], d1.y, accq[m][2]);
             }
-            r01 = make_float2(rk[0] * colf4.x, rk[1] * colf4.y);
-            r23 = make_float2(rk[2] * colf4.z, rk[3] * colf4.w);
-            y01 = make_float2(rq[0] * colf4.x, rq[1] * colf4.y);
-            y23 = make_float2(rq[2] * colf4.z, rq[3] * colf4.w);
-        } else if constexpr (SPLIT) {
+        }
+        __syncwarp();  // every lane is done with the stage
+        if (lane == 0 && it + kI8Ring < NI) i8_issue<PER_KEY, SPLIT, REC>(ws, a, row, hd, L, it + kI8Ring);
+    }
+
+    // item 5: v, k, q (+ lambda, lbar, column scales); sum_d acc_d 256^d:
+    // digits 0 and 1 pair exactly in int32 (|acc_d| <= 128 * 127 * 255),
+    // digit 2 joins in one FMA; then the unit and the column scales (eq. 10:
+    // applied to the column sums)
+    if (!i8_wait(ws, pv, kI8TailItem, NI)) return i8_abandon(a, ro);
+    {
+        const float4* st4p = reinterpret_cast<const float4*>(ws.ring[kI8TailItem % kI8Ring]);
+        v4 = st4p[lane];
+        k4 = st4p[32 + lane];
+        q4 = st4p[64 + lane];
+        if constexpr (PER_KEY) {
+            const float4 lam4 = st4p[96 + lane];
+            const float4 lb4 = st4p[128 + lane];
+            lp4 = make_float4(lb4.x + lam4.x, lb4.y + lam4.y, lb4.z + lam4.z, lb4.w + lam4.w);
+        } else {
+            lp4 = make_float4(lp_scalar, lp_scalar, lp_scalar, lp_scalar);
+        }
+        kq = warp_sum(fmaf(k4.x, q4.x, fmaf(k4.y, q4.y, fmaf(k4.z, q4.z, k4.w * q4.w))));
+        const float4 colf4 =
+            pv.colf != nullptr ? st4p[(PER_KEY ? 160 : 96) + lane] : make_float4(1.f, 1.f, 1.f, 1.f);
+        float rk[4], rq[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int k01 = acck[m][0] + (acck[m][1] << 8), q01 = accq[m][0] + (accq[m][1] << 8);
+            rk[m] = fmaf(static_cast<float>(acck[m][2]), 65536.0f, static_cast<float>(k01)) * unit_k;
+            rq[m] = fmaf(static_cast<float>(accq[m][2]), 65536.0f, static_cast<float>(q01)) * unit_q;
+        }
+        r01 = make_float2(rk[0] * colf4.x, rk[1] * colf4.y);
+        r23 = make_float2(rk[2] * colf4.z, rk[3] * colf4.w);
+        y01 = make_float2(rq[0] * colf4.x, rq[1] * colf4.y);
+        y23 = make_float2(rq[2] * colf4.z, rq[3] * colf4.w);
+    }
+    __syncwarp();
+    if (lane == 0 && kI8TailItem + kI8Ring < NI)
+        i8_issue<PER_KEY, SPLIT, REC>(ws, a, row, hd, L, kI8TailItem + kI8Ring);
+
+    // items 6 ..: the log chunks
+#pragma unroll 1
+    for (int it = kI8LogItem0; it < NI; ++it) {
+        if (!i8_wait(ws, pv, it, NI)) return i8_abandon(a, ro);
+        const unsigned char* st = ws.ring[it % kI8Ring];
+        const float4* st4p = reinterpret_cast<const float4*>(st);
+        const int e0 = (it - kI8LogItem0) * EPC;
+        const int n = min(EPC, L - e0);
+        if constexpr (SPLIT) {
             // replay with precomputed coefficients (c_k, c_q) per entry
-            const int e0 = (it - kI8LogItem0) * EPC;
-            const int n = min(EPC, L - e0);
             const float2* cf = reinterpret_cast<const float2*>(st + EPC * kVecBytes);
             // the chunk carries the coefficients of all EPC entries; only the
             // first n (written by this call's prepare kernel) are read
@@ -369,8 +405,6 @@ __device__ __forceinline__ int2 i8_warp_step(const StepArgs& a, I8Warp& ws, int 
             }
         } else {
             // replay of this chunk's log entries (LeapQuant eq. 9)
-            const int e0 = (it - kI8LogItem0) * EPC;
-            const int n = min(EPC, L - e0);
             for (int e = 0; e < n; ++e) {
                 const float4 K4 = rec_key4<REC>(st, static_cast<size_t>(e) * kD + 4 * lane);
                 const float4 U4 = rec_val4<REC>(st + EPC * kVecBytes, static_cast<size_t>(e) * kD + 4 * lane);

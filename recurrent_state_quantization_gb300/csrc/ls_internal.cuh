@@ -65,7 +65,7 @@ struct PoolView {
     int32_t cap;           // log entries per state: W + R
     int32_t lam_stride;    // floats per state in lamlog
     int32_t* foldq;        // INT8 without compensator pairs:
-                           //   window-end queue [0] count, [1] next, [2] done,
+                           //   window-end queue [0] count, [2] done, [1] and
                            //   [3] unused, [4 ..] (state index, request row)
                            //   pairs (the tensor-core window-end kernel's work
                            //   list); nullptr otherwise

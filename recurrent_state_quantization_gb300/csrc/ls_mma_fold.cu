@@ -58,10 +58,12 @@
 // no thread holds more than 32 of its 128 values.
 //
 // Queue protocol (pool memory, zeroed at creation): the step kernel appends
-// (state, row) pairs after atomically incrementing count; here groups take
-// items by atomically incrementing next; the last CTA to finish resets
-// count, next and done to zero for the next token.  With an empty queue
-// every CTA returns at once.
+// (state, row) pairs after atomically incrementing count; here the items are
+// dealt round-robin over the groups of the grid (group g of CTA b takes
+// items 4 b + g, 4 b + g + 4 grid, ...), so that each group knows its next
+// item's position without an atomic and loads its entry one state ahead;
+// the last CTA to finish resets count and done to zero for the next token.
+// With an empty queue every CTA returns at once.
 #include <cuda_runtime.h>
 
 #include "ls_device.cuh"
@@ -287,34 +289,35 @@ __device__ __forceinline__ void add_token_rows(const GroupSmem& gs, int qr, floa
 // Decode the closing token of state hd (request row `row`), fold and
 // requantize the state with the 128 threads of one group (gt = thread in the
 // group, gw = its warp in the group).  On entry its header and codes, and its
-// first records, are staged or in flight.  Thread 0 takes the next queue item
-// early; once the last MMA has read the operands it stages that state's first
-// records, and after pass 2 (the codes and the header are consumed) its codes
-// and header, so the copies overlap this state's epilogue.  Returns false after a
-// timeout (flagged).
+// first records, are staged or in flight.  Thread 0 knows the group's next
+// item (its queue entry was loaded during the previous state); once the last
+// MMA has read the operands it stages that state's first records, and after
+// pass 2 (the codes and the header are consumed) its codes and header, so the
+// copies overlap this state's epilogue.  Returns false after a timeout
+// (flagged).
 template <bool PER_KEY, bool COLS>
 __device__ __forceinline__ bool fold_state(const StepArgs& a, size_t hd, int row, float lb_scalar,
                                            float lam_scalar, float beta, GroupSmem& gs, GroupPipe& gp,
                                            uint32_t tmem, uint32_t tlane, int bar_id, int gt, int lane, int gw,
-                                           int count) {
+                                           int count, int item, int stride, int2& ahead) {
     const PoolView& pv = a.pv;
     const int n = pv.cap - 1;  // stored records; the closing token itself is never stored
-    int next_item = 0;
+    const int next_item = item + stride;
     long long next_hd = -1;
     int next_row = 0;
     float next_lb = 0.0f, next_lam = 0.0f, next_beta = 0.0f;
-    if (gt == 0) {  // the next state, early: its index is needed once the MMAs are done
-        next_item = atomicAdd(pv.foldq + 1, 1);
-        if (next_item < count) {
-            const int2 it = queue_item(pv, next_item);
-            next_hd = it.x;
-            next_row = it.y;
-            if constexpr (!PER_KEY) {
-                next_lb = __ldcg(pv.lbar + next_hd);
-                next_lam = __ldg(a.lam + next_row);
-            }
-            next_beta = __ldg(a.beta + next_row);
+    int2 after = make_int2(-1, 0);
+    if (gt == 0 && next_item < count) {
+        // the next state's queue entry was loaded during the previous state;
+        // its scalars are needed after pass 2, the entry after it next time
+        next_hd = ahead.x;
+        next_row = ahead.y;
+        if constexpr (!PER_KEY) {
+            next_lb = __ldcg(pv.lbar + next_hd);
+            next_lam = __ldg(a.lam + next_row);
         }
+        next_beta = __ldg(a.beta + next_row);
+        if (next_item + stride < count) after = queue_item(pv, next_item + stride);
     }
     // header and codes: lp of key row gt, exp(lp) s, the token's k.q
     if (!group_wait(pv, &gs.st_bar, gp.st_ph, gp.st_out, bar_id, gt)) return false;
@@ -453,6 +456,7 @@ __device__ __forceinline__ bool fold_state(const StepArgs& a, size_t hd, int row
         gs.next_lb = next_lb;
         gs.next_lam = next_lam;
         gs.next_beta = next_beta;
+        ahead = after;
     }
     named_barrier(bar_id, kGroupThreads);  // row statistics complete; codes and header consumed
     if (gt == 0 && next_hd >= 0) {
@@ -551,14 +555,18 @@ __global__ void __launch_bounds__(kFoldThreads, 1) window_fold_kernel(const Step
     const int bar_id = 1 + g;
     const int n = pv.cap - 1;
     GroupPipe gp;
+    // queue items are dealt round-robin: group gid takes gid, gid + stride, ...
+    const int stride = static_cast<int>(gridDim.x) * kGroups;
+    int2 ahead = make_int2(-1, 0);  // thread 0: the queue entry of the group's next item
     if (gt == 0) {
         mbar_init(&gs.rec_bar, 1);
         mbar_init(&gs.st_bar, 1);
         mbar_init(&gs.mma_bar, 1);
         mbar_fence_init();
         // the group's first state
-        const int item = atomicAdd(q + 1, 1);
+        const int item = static_cast<int>(blockIdx.x) * kGroups + g;
         gs.next_item = item;
+        if (item + stride < count) ahead = queue_item(pv, item + stride);
         if (item < count) {
             const int2 it = queue_item(pv, item);
             gs.next_hd = it.x;
@@ -589,7 +597,7 @@ __global__ void __launch_bounds__(kFoldThreads, 1) window_fold_kernel(const Step
         const int row = gs.next_row;
         const float lb = gs.next_lb, lam = gs.next_lam, beta = gs.next_beta;
         if (!fold_state<PER_KEY, COLS>(a, hd, row, lb, lam, beta, gs, gp, tmem, tlane, bar_id, gt, lane, gw,
-                                       count)) {
+                                       count, item, stride, ahead)) {
             // after a timeout: let this group's copies and MMAs land before exit
             if (gt == 0) {
                 if (gp.rec_out) mbar_wait_bounded(&gs.rec_bar, gp.rec_ph);
@@ -607,7 +615,6 @@ __global__ void __launch_bounds__(kFoldThreads, 1) window_fold_kernel(const Step
         __threadfence();
         if (atomicAdd(q + 2, 1) == static_cast<int>(gridDim.x) - 1) {
             q[0] = 0;
-            q[1] = 0;
             q[2] = 0;
         }
     }
