@@ -45,8 +45,9 @@
 //           lbar from L2) so that no register holds them during the GEMVs
 //   then    log chunks: K and U of EPC entries (+ their snapshots), or with
 //           split replay U and the precomputed coefficients
-// The first two items are issued before the log length is read, so the
-// dependent load of the state's metadata overlaps the first copies.
+// Item 0 and the first code chunk (as a copy, or with windows of up to 16
+// tokens as an L2 prefetch) are issued before the log length is read, so
+// the dependent load of the state's metadata overlaps the first copies.
 #include <cuda_runtime.h>
 
 #include "ls_device.cuh"
@@ -66,6 +67,7 @@ constexpr int kI8CodeItems = 4;          // 16 KiB of codes, 32 key rows per ite
 constexpr int kI8TailItem = kI8CodeItems + 1;  // v (+ column scales)
 constexpr int kI8LogItem0 = kI8TailItem + 1;   // first log chunk
 static_assert(kI8Ring <= kI8LogItem0, "the ring's first fill holds no log chunk");
+constexpr int kShortWindow = 16;               // see i8_warp_step: the early copies
 
 struct I8Warp {
     unsigned char ring[kI8Ring][kI8Stage];
@@ -99,6 +101,12 @@ __device__ __forceinline__ int dp4a_ss(int a, uint32_t b, int c) {
     int d;
     asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
+}
+
+// Prefetch `bytes` (a multiple of 16) at p (16-byte aligned) into L2; nothing
+// to wait for.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // Byte transpose of the low three bytes of four words: byte r of w[d] =
@@ -239,17 +247,26 @@ __device__ __forceinline__ int2 i8_warp_step(const StepArgs& a, I8Warp& ws, int 
         return none;
     }
     const size_t hd = static_cast<size_t>(slot) * H + h;
-    // the inputs and the first code chunk do not depend on the log length, so
-    // they are in flight while it is read (for a token that closes its window
-    // they bring into L2 what the window-end kernel reads next)
-    constexpr int kEarly = 2;
-    static_assert(kEarly <= kI8Ring && kEarly <= kI8LogItem0, "early items are never log chunks");
+    // The inputs and the first code chunk do not depend on the log length, so
+    // they are in flight while it is read.  A token that closes its window
+    // needs neither here, and the warp must wait for every copy it issued
+    // before it leaves: with windows of up to kShortWindow tokens, where one
+    // token in W closes, only the inputs are copied early and the first code
+    // chunk is prefetched into L2 (no wait), its copy issued once the log
+    // length is known; with longer windows both are copied early.  Measured
+    // on GB300, chained tokens of 256 x 48 heads: W = 8 62.3 against 62.9 us,
+    // W = 16 62.1 against 62.4 us; 128 x 32 per-key-gate heads, W = 32: 34.5
+    // against 34.3 us.
+    const int early = W <= kShortWindow ? 1 : 2;
     if (lane == 0) {
 #pragma unroll
         for (int s = 0; s < kI8Ring; ++s) mbar_init(&ws.bar[s], 1);
         mbar_fence_init();
-#pragma unroll
-        for (int it = 0; it < kEarly; ++it) i8_issue<PER_KEY, SPLIT, REC>(ws, a, row, hd, 0, it);
+        i8_issue<PER_KEY, SPLIT, REC>(ws, a, row, hd, 0, 0);
+        if (early == 2)
+            i8_issue<PER_KEY, SPLIT, REC>(ws, a, row, hd, 0, 1);
+        else
+            bulk_prefetch_l2(reinterpret_cast<const unsigned char*>(pv.base) + hd * (kD * kD), kI8Chunk);
     }
     const int L = pv.len[hd];
     const float beta = __ldg(a.beta + row);
@@ -263,7 +280,7 @@ __device__ __forceinline__ int2 i8_warp_step(const StepArgs& a, I8Warp& ws, int 
         // records once.  Either way the early copies land before the warp leaves.
         if (lane == 0) {
             if (bad) flag_status(pv.status, kDevBadState);
-            for (int s = 0; s < kEarly; ++s)
+            for (int s = 0; s < early; ++s)
                 if (!mbar_wait_bounded(&ws.bar[s], 0)) flag_status(pv.status, kDevTimeout);
         }
         __syncwarp();
@@ -275,7 +292,8 @@ __device__ __forceinline__ int2 i8_warp_step(const StepArgs& a, I8Warp& ws, int 
     }
     if (lane == 0) {
 #pragma unroll
-        for (int it = kEarly; it < kI8Ring; ++it) i8_issue<PER_KEY, SPLIT, REC>(ws, a, row, hd, L, it);
+        for (int it = 1; it < kI8Ring; ++it)
+            if (it >= early) i8_issue<PER_KEY, SPLIT, REC>(ws, a, row, hd, L, it);
     }
     __syncwarp();
     const int NI = kI8LogItem0 + (L + EPC - 1) / EPC;

@@ -43,7 +43,9 @@
 // issues the MMAs into the group's 128 tensor-memory columns and commits them
 // to the group's mbarrier, and the copies of the next state start as soon as
 // the MMAs have read the operands (records) and pass 2 is done with the
-// codes (codes, header).  The epilogue runs on the CUDA cores: thread t of a group
+// codes (codes, header); lane 0 of each of the group's four warps issues a
+// part of them, so that no warp arrives late at the next group barrier.  The
+// epilogue runs on the CUDA cores: thread t of a group
 // owns value column j = t (the tensor-memory lanes its warp may read) for
 // all 128 key rows, so r_j, y0_j and u_j are thread-local sums.  The INT8
 // words of a state hold 4 key rows of one value column, so each thread reads
@@ -139,47 +141,69 @@ __device__ __forceinline__ int2 queue_item(const PoolView& pv, int item) {
     return __ldcg(reinterpret_cast<const int2*>(pv.foldq + 4) + item);
 }
 
-// Stage records c0 .. c0 + nl - 1 of state hd on rec_bar (one thread).
+// Part p (0..3) of the staging of records c0 .. c0 + nl - 1 of state hd,
+// issued by lane 0 of the group's warp p on rec_bar (arrival count 4): U,
+// K, the log-decay snapshots, or (p = 3) an arrival alone.
 template <bool PER_KEY>
-__device__ __forceinline__ void stage_records(const PoolView& pv, size_t hd, int c0, int nl, GroupSmem& gs) {
+__device__ __forceinline__ void stage_records_part(const PoolView& pv, size_t hd, int c0, int nl, GroupSmem& gs,
+                                                   int p) {
     const size_t eo = (hd * static_cast<size_t>(pv.cap) + c0) * kD;
-    const uint32_t part = static_cast<uint32_t>(nl) * kVecBytes;
-    const uint32_t kpart = static_cast<uint32_t>(nl) * kD * key_bytes(pv);
-    const uint32_t upart = static_cast<uint32_t>(nl) * kD * val_bytes(pv);
     const size_t lb0 = hd * static_cast<size_t>(pv.lam_stride);
-    const uint32_t lam_bytes = PER_KEY ? part : static_cast<uint32_t>((nl + 3) / 4 * 16);
     fence_proxy_async();  // the buffers were last used by generic loads and stores
-    mbar_arrive_expect_tx(&gs.rec_bar, upart + kpart + lam_bytes);
-    bulk_g2s(gs.ops[1], reinterpret_cast<const unsigned char*>(pv.ulog) + eo * val_bytes(pv), upart, &gs.rec_bar);
-    bulk_g2s(gs.ops[3], reinterpret_cast<const unsigned char*>(pv.klog) + eo * key_bytes(pv), kpart, &gs.rec_bar);
-    if constexpr (PER_KEY)
-        bulk_g2s(gs.ops[2], pv.lamlog + lb0 + static_cast<size_t>(c0) * kD, part, &gs.rec_bar);
-    else
-        bulk_g2s(gs.ops[2], pv.lamlog + lb0 + c0, lam_bytes, &gs.rec_bar);
+    if (p == 0) {
+        const uint32_t upart = static_cast<uint32_t>(nl) * kD * val_bytes(pv);
+        mbar_arrive_expect_tx(&gs.rec_bar, upart);
+        bulk_g2s(gs.ops[1], reinterpret_cast<const unsigned char*>(pv.ulog) + eo * val_bytes(pv), upart, &gs.rec_bar);
+    } else if (p == 1) {
+        const uint32_t kpart = static_cast<uint32_t>(nl) * kD * key_bytes(pv);
+        mbar_arrive_expect_tx(&gs.rec_bar, kpart);
+        bulk_g2s(gs.ops[3], reinterpret_cast<const unsigned char*>(pv.klog) + eo * key_bytes(pv), kpart, &gs.rec_bar);
+    } else if (p == 2) {
+        if constexpr (PER_KEY) {
+            const uint32_t part = static_cast<uint32_t>(nl) * kVecBytes;
+            mbar_arrive_expect_tx(&gs.rec_bar, part);
+            bulk_g2s(gs.ops[2], pv.lamlog + lb0 + static_cast<size_t>(c0) * kD, part, &gs.rec_bar);
+        } else {
+            const uint32_t lam_bytes = static_cast<uint32_t>((nl + 3) / 4 * 16);
+            mbar_arrive_expect_tx(&gs.rec_bar, lam_bytes);
+            bulk_g2s(gs.ops[2], pv.lamlog + lb0 + c0, lam_bytes, &gs.rec_bar);
+        }
+    } else {
+        mbar_arrive_expect_tx(&gs.rec_bar, 0);
+    }
 }
 
-// Stage the 16 KiB of codes and the header of state hd, whose closing token
-// is request row `row`, on st_bar (one thread).
+// Part p (0..3) of the staging of state hd, issued by lane 0 of the group's
+// warp p on st_bar (arrival count 4): code quarter p and a share of the
+// header (k, q | v, s | lambda, lbar for the per-key gate | the old column
+// scales), so that no warp of the group issues all the copies.
 template <bool PER_KEY, bool COLS>
-__device__ __forceinline__ void stage_state(const StepArgs& a, size_t hd, int row, GroupSmem& gs) {
+__device__ __forceinline__ void stage_state_part(const StepArgs& a, size_t hd, int row, GroupSmem& gs, int p) {
     const PoolView& pv = a.pv;
     const unsigned char* src = reinterpret_cast<const unsigned char*>(pv.base) + hd * kCodeBytes;
     const size_t ro = static_cast<size_t>(row) * kD;
+    uint32_t bytes = kCodeBytes / 4;
+    if (p == 0 || p == 1) bytes += 2 * kVecBytes;
+    if (p == 2 && PER_KEY) bytes += 2 * kVecBytes;
+    if (p == 3 && COLS) bytes += kVecBytes;
     fence_proxy_async();
-    mbar_arrive_expect_tx(&gs.st_bar, kCodeBytes + ((PER_KEY ? 6 : 4) + (COLS ? 1 : 0)) * kVecBytes);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        bulk_g2s(reinterpret_cast<unsigned char*>(gs.codes) + i * (kCodeBytes / 4), src + i * (kCodeBytes / 4),
-                 kCodeBytes / 4, &gs.st_bar);
-    bulk_g2s(gs.hk, a.k + ro, kVecBytes, &gs.st_bar);
-    bulk_g2s(gs.hq, a.q + ro, kVecBytes, &gs.st_bar);
-    bulk_g2s(gs.hv, a.v + ro, kVecBytes, &gs.st_bar);
-    bulk_g2s(gs.hs, pv.scale + hd * kD, kVecBytes, &gs.st_bar);
-    if constexpr (PER_KEY) {
-        bulk_g2s(gs.hlam, a.lam + ro, kVecBytes, &gs.st_bar);
-        bulk_g2s(gs.hlb, pv.lbar + hd * kD, kVecBytes, &gs.st_bar);
+    mbar_arrive_expect_tx(&gs.st_bar, bytes);
+    bulk_g2s(reinterpret_cast<unsigned char*>(gs.codes) + p * (kCodeBytes / 4), src + p * (kCodeBytes / 4),
+             kCodeBytes / 4, &gs.st_bar);
+    if (p == 0) {
+        bulk_g2s(gs.hk, a.k + ro, kVecBytes, &gs.st_bar);
+        bulk_g2s(gs.hq, a.q + ro, kVecBytes, &gs.st_bar);
+    } else if (p == 1) {
+        bulk_g2s(gs.hv, a.v + ro, kVecBytes, &gs.st_bar);
+        bulk_g2s(gs.hs, pv.scale + hd * kD, kVecBytes, &gs.st_bar);
+    } else if (p == 2) {
+        if constexpr (PER_KEY) {
+            bulk_g2s(gs.hlam, a.lam + ro, kVecBytes, &gs.st_bar);
+            bulk_g2s(gs.hlb, pv.lbar + hd * kD, kVecBytes, &gs.st_bar);
+        }
+    } else {
+        if constexpr (COLS) bulk_g2s(gs.hb, pv.colf + hd * kD, kVecBytes, &gs.st_bar);
     }
-    if constexpr (COLS) bulk_g2s(gs.hb, pv.colf + hd * kD, kVecBytes, &gs.st_bar);
 }
 
 // Three MMAs per 8 records of the staged chunk (one thread).
@@ -290,11 +314,11 @@ __device__ __forceinline__ void add_token_rows(const GroupSmem& gs, int qr, floa
 // requantize the state with the 128 threads of one group (gt = thread in the
 // group, gw = its warp in the group).  On entry its header and codes, and its
 // first records, are staged or in flight.  Thread 0 knows the group's next
-// item (its queue entry was loaded during the previous state); once the last
-// MMA has read the operands it stages that state's first records, and after
-// pass 2 (the codes and the header are consumed) its codes and header, so the
-// copies overlap this state's epilogue.  Returns false after a timeout
-// (flagged).
+// item (its queue entry was loaded during the previous state) and publishes
+// it once every thread has read this state's; once the last MMA has read the
+// operands the four warps stage that state's first records, and after pass 2
+// (the codes and the header are consumed) its codes and header, so the copies
+// overlap this state's epilogue.  Returns false after a timeout (flagged).
 template <bool PER_KEY, bool COLS>
 __device__ __forceinline__ bool fold_state(const StepArgs& a, size_t hd, int row, float lb_scalar,
                                            float lam_scalar, float beta, GroupSmem& gs, GroupPipe& gp,
@@ -321,6 +345,11 @@ __device__ __forceinline__ bool fold_state(const StepArgs& a, size_t hd, int row
     }
     // header and codes: lp of key row gt, exp(lp) s, the token's k.q
     if (!group_wait(pv, &gs.st_bar, gp.st_ph, gp.st_out, bar_id, gt)) return false;
+    if (gt == 0) {  // every thread has read this state's entry: publish the next one's
+        gs.next_item = next_item;
+        gs.next_hd = static_cast<int32_t>(next_hd);
+        gs.next_row = next_row;
+    }
     const float lp = PER_KEY ? gs.hlb[gt] + gs.hlam[gt] : lb_scalar + lam_scalar;
     gs.es[gt] = expf(lp) * gs.hs[gt];
     // the key of the state update is the one a record would store (bfloat16
@@ -384,13 +413,15 @@ __device__ __forceinline__ bool fold_state(const StepArgs& a, size_t hd, int row
             gp.mma_out = true;
         }
         if (!group_wait(pv, &gs.mma_bar, gp.mma_ph, gp.mma_out, bar_id, gt)) return false;
-        // the operands are consumed: stage the next chunk, or the next state's first
-        if (gt == 0) {
+        // the operands are consumed: stage the next chunk, or the next state's
+        // first, a part per warp
+        if (lane == 0) {
             if (c0 + kChunkRecords < n) {
-                stage_records<PER_KEY>(pv, hd, c0 + kChunkRecords, min(kChunkRecords, n - c0 - kChunkRecords), gs);
+                stage_records_part<PER_KEY>(pv, hd, c0 + kChunkRecords, min(kChunkRecords, n - c0 - kChunkRecords),
+                                            gs, gw);
                 gp.rec_out = true;
-            } else if (next_hd >= 0) {
-                stage_records<PER_KEY>(pv, static_cast<size_t>(next_hd), 0, min(kChunkRecords, n), gs);
+            } else if (gs.next_hd >= 0) {
+                stage_records_part<PER_KEY>(pv, static_cast<size_t>(gs.next_hd), 0, min(kChunkRecords, n), gs, gw);
                 gp.rec_out = true;
             }
         }
@@ -450,17 +481,14 @@ __device__ __forceinline__ bool fold_state(const StepArgs& a, size_t hd, int row
     }
     tc_fence_before();
     if (gt == 0) {
-        gs.next_item = next_item;
-        gs.next_hd = static_cast<int32_t>(next_hd);
-        gs.next_row = next_row;
         gs.next_lb = next_lb;
         gs.next_lam = next_lam;
         gs.next_beta = next_beta;
         ahead = after;
     }
     named_barrier(bar_id, kGroupThreads);  // row statistics complete; codes and header consumed
-    if (gt == 0 && next_hd >= 0) {
-        stage_state<PER_KEY, COLS>(a, static_cast<size_t>(next_hd), next_row, gs);
+    if (lane == 0 && gs.next_hd >= 0) {
+        stage_state_part<PER_KEY, COLS>(a, static_cast<size_t>(gs.next_hd), gs.next_row, gs, gw);
         gp.st_out = true;
     }
     if constexpr (COLS) {
@@ -559,8 +587,8 @@ __global__ void __launch_bounds__(kFoldThreads, 1) window_fold_kernel(const Step
     const int stride = static_cast<int>(gridDim.x) * kGroups;
     int2 ahead = make_int2(-1, 0);  // thread 0: the queue entry of the group's next item
     if (gt == 0) {
-        mbar_init(&gs.rec_bar, 1);
-        mbar_init(&gs.st_bar, 1);
+        mbar_init(&gs.rec_bar, 4);  // one arrival per warp of the group
+        mbar_init(&gs.st_bar, 4);  // one arrival per warp of the group
         mbar_init(&gs.mma_bar, 1);
         mbar_fence_init();
         // the group's first state
@@ -576,18 +604,20 @@ __global__ void __launch_bounds__(kFoldThreads, 1) window_fold_kernel(const Step
                 gs.next_lam = __ldg(a.lam + it.y);
             }
             gs.next_beta = __ldg(a.beta + it.y);
-            stage_state<PER_KEY, COLS>(a, static_cast<size_t>(it.x), it.y, gs);
-            gp.st_out = true;
-            if (n > 0) {
-                stage_records<PER_KEY>(pv, static_cast<size_t>(it.x), 0, min(kChunkRecords, n), gs);
-                gp.rec_out = true;
-            }
         }
     }
     if (warp == 0) tmem_alloc512(&tmem_base);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (lane == 0 && gs.next_item < count) {  // the group's first state, a part per warp
+        stage_state_part<PER_KEY, COLS>(a, static_cast<size_t>(gs.next_hd), gs.next_row, gs, gw);
+        gp.st_out = true;
+        if (n > 0) {
+            stage_records_part<PER_KEY>(pv, static_cast<size_t>(gs.next_hd), 0, min(kChunkRecords, n), gs, gw);
+            gp.rec_out = true;
+        }
+    }
     const uint32_t tmem = tmem_base + 128u * g;                           // the group's columns
     const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * gw) << 16);  // the warp's lanes
     int item = gs.next_item;

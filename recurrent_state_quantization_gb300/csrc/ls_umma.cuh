@@ -118,12 +118,14 @@ __device__ __forceinline__ void named_barrier(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// Round to TF32 (nearest, ties away), as an FP32 bit pattern with the low 13
-// mantissa bits zero.
+// Round to TF32 (nearest, ties away from zero), as an FP32 bit pattern with
+// the low 13 mantissa bits zero: half a TF32 unit added to the magnitude bits
+// of the encoding, then the 13 low bits cleared (a carry moves into the
+// exponent, as rounding up to the next binade requires).  Finite x only.  Two
+// integer operations: the window-end kernel executed 3.4 % more instructions
+// with the conversion instruction (counter totals on GB300).
 __device__ __forceinline__ float tf32_rna(float x) {
-    uint32_t t;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(t) : "f"(x));
-    return __uint_as_float(t);
+    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
 }
 
 }  // namespace ls
