@@ -45,9 +45,9 @@
 //           lbar from L2) so that no register holds them during the GEMVs
 //   then    log chunks: K and U of EPC entries (+ their snapshots), or with
 //           split replay U and the precomputed coefficients
-// Item 0 and the first code chunk (as a copy, or with windows of up to 16
-// tokens as an L2 prefetch) are issued before the log length is read, so
-// the dependent load of the state's metadata overlaps the first copies.
+// Item 0 and the first code chunk are issued before the log length is read
+// (as copies, or with windows of up to 16 tokens as L2 prefetches), so the
+// dependent load of the state's metadata overlaps their first reads.
 #include <cuda_runtime.h>
 
 #include "ls_device.cuh"
@@ -248,25 +248,33 @@ __device__ __forceinline__ int2 i8_warp_step(const StepArgs& a, I8Warp& ws, int 
     }
     const size_t hd = static_cast<size_t>(slot) * H + h;
     // The inputs and the first code chunk do not depend on the log length, so
-    // they are in flight while it is read.  A token that closes its window
+    // they are on their way while it is read.  A token that closes its window
     // needs neither here, and the warp must wait for every copy it issued
     // before it leaves: with windows of up to kShortWindow tokens, where one
-    // token in W closes, only the inputs are copied early and the first code
-    // chunk is prefetched into L2 (no wait), its copy issued once the log
-    // length is known; with longer windows both are copied early.  Measured
-    // on GB300, chained tokens of 256 x 48 heads: W = 8 62.3 against 62.9 us,
-    // W = 16 62.1 against 62.4 us; 128 x 32 per-key-gate heads, W = 32: 34.5
-    // against 34.3 us.
-    const int early = W <= kShortWindow ? 1 : 2;
+    // token in W closes, they are prefetched into L2 (nothing to wait for) and
+    // copied once the log length is known; with longer windows they are
+    // copied at once.  Measured on GB300, chained tokens of 256 x 48 heads: W
+    // = 8 62.2 against 62.9 us with the early copies, W = 16 62.0 against
+    // 62.4 us; 128 x 32 per-key-gate heads, W = 32: 34.5 against 34.3 us with
+    // the prefetches.
+    const int early = W <= kShortWindow ? 0 : 2;  // items copied before the log length is read
     if (lane == 0) {
 #pragma unroll
         for (int s = 0; s < kI8Ring; ++s) mbar_init(&ws.bar[s], 1);
         mbar_fence_init();
-        i8_issue<PER_KEY, SPLIT, REC>(ws, a, row, hd, 0, 0);
-        if (early == 2)
+        if (early == 2) {
+            i8_issue<PER_KEY, SPLIT, REC>(ws, a, row, hd, 0, 0);
             i8_issue<PER_KEY, SPLIT, REC>(ws, a, row, hd, 0, 1);
-        else
+        } else {
+            bulk_prefetch_l2(a.k + static_cast<size_t>(row) * kD, kVecBytes);
+            bulk_prefetch_l2(a.q + static_cast<size_t>(row) * kD, kVecBytes);
+            bulk_prefetch_l2(pv.scale + hd * kD, kVecBytes);
+            if constexpr (PER_KEY) {
+                bulk_prefetch_l2(a.lam + static_cast<size_t>(row) * kD, kVecBytes);
+                bulk_prefetch_l2(pv.lbar + hd * kD, kVecBytes);
+            }
             bulk_prefetch_l2(reinterpret_cast<const unsigned char*>(pv.base) + hd * (kD * kD), kI8Chunk);
+        }
     }
     const int L = pv.len[hd];
     const float beta = __ldg(a.beta + row);
@@ -292,7 +300,7 @@ __device__ __forceinline__ int2 i8_warp_step(const StepArgs& a, I8Warp& ws, int 
     }
     if (lane == 0) {
 #pragma unroll
-        for (int it = 1; it < kI8Ring; ++it)
+        for (int it = 0; it < kI8Ring; ++it)
             if (it >= early) i8_issue<PER_KEY, SPLIT, REC>(ws, a, row, hd, L, it);
     }
     __syncwarp();
