@@ -51,6 +51,8 @@ def parse():
                     help="skip e2e, window sweep and CPU baseline (profiling runs)")
     ap.add_argument("--ring", type=int, default=64, help="distinct token inputs kept in HBM")
     ap.add_argument("--pools", type=int, default=None, help="override the pool count (profiling runs)")
+    ap.add_argument("--window", type=int, default=None,
+                    help="override the window / merge interval of the log variants (profiling runs)")
     return ap.parse_args()
 
 
@@ -217,7 +219,8 @@ def run_native(args, rank, world, local):
         over.update(pools=args.pools)
     w = wl.Workload(**{**base.__dict__, **over}) if over else base
     only = set(args.only.split(",")) if args.only else None
-    variants = [(n, W) for n, W in VARIANTS if only is None or n in only]
+    variants = [(n, W if (args.window is None or not W) else args.window)
+                for n, W in VARIANTS if only is None or n in only]
     heads = w.batch * w.heads
     slot_idx = wl.slot_index(w, dev)
     masks = wl.static_masks(w, dev)
@@ -384,7 +387,8 @@ def window_sweep(w, slot_idx, masks, inputs, ring, dev, peak, peak_kind, eager_p
     """INT8 head-steps/s and achieved algorithmic GB/s for each window W (a
     whole number of windows, 4 pools, warmed states); for W = 16 in the
     smoothed per-value-column format, without and with 4 Compensator Tokens
-    (the full LeapQuant boundary format); with bfloat16 key-side log factors
+    (the full LeapQuant boundary format), and per-key-row with 4 Compensator
+    Tokens (the ladder of LeapQuant §4.4 Table 2); with bfloat16 key-side log factors
     (DeltaLog §3.4), INT8 W = 16 and deferred FP32 M = 16; and with FP16
     records (LeapQuant §4.1, §4.3), INT8 W = 16 per-key-row and in the full
     LeapQuant format (smoothed + 4 FP16 Compensator Tokens)."""
@@ -395,7 +399,8 @@ def window_sweep(w, slot_idx, masks, inputs, ring, dev, peak, peak_kind, eager_p
     stream = torch.cuda.current_stream()
     heads = w.batch * w.heads
     cases = ([("int8", W_, False, 0, False, False) for W_ in SWEEP_W]
-             + [("int8", 16, True, 0, False, False), ("int8", 16, True, 4, False, False),
+             + [("int8", 16, True, 0, False, False), ("int8", 16, False, 4, False, False),
+                ("int8", 16, True, 4, False, False),
                 ("int8", 16, False, 0, True, False), ("deferred", 16, False, 0, True, False),
                 ("int8", 16, False, 0, False, True), ("int8", 16, True, 4, False, True)])
     for variant, W, cols, comp, k16, r16 in cases:
