@@ -66,6 +66,10 @@
 // item's position without an atomic and loads its entry one state ahead;
 // the last CTA to finish resets count and done to zero for the next token.
 // With an empty queue every CTA returns at once.
+//
+// The record format (FP32, bfloat16 keys, binary16 records) is a template
+// parameter, like the step kernels', so that the operand build reads each
+// record element without a branch on the format.
 #include <cuda_runtime.h>
 
 #include "ls_device.cuh"
@@ -144,20 +148,21 @@ __device__ __forceinline__ int2 queue_item(const PoolView& pv, int item) {
 // Part p (0..3) of the staging of records c0 .. c0 + nl - 1 of state hd,
 // issued by lane 0 of the group's warp p on rec_bar (arrival count 4): U,
 // K, the log-decay snapshots, or (p = 3) an arrival alone.
-template <bool PER_KEY>
+template <bool PER_KEY, int REC>
 __device__ __forceinline__ void stage_records_part(const PoolView& pv, size_t hd, int c0, int nl, GroupSmem& gs,
                                                    int p) {
+    constexpr uint32_t kb = rec_key_bytes(REC), vb = rec_val_bytes(REC);
     const size_t eo = (hd * static_cast<size_t>(pv.cap) + c0) * kD;
     const size_t lb0 = hd * static_cast<size_t>(pv.lam_stride);
     fence_proxy_async();  // the buffers were last used by generic loads and stores
     if (p == 0) {
-        const uint32_t upart = static_cast<uint32_t>(nl) * kD * val_bytes(pv);
+        const uint32_t upart = static_cast<uint32_t>(nl) * kD * vb;
         mbar_arrive_expect_tx(&gs.rec_bar, upart);
-        bulk_g2s(gs.ops[1], reinterpret_cast<const unsigned char*>(pv.ulog) + eo * val_bytes(pv), upart, &gs.rec_bar);
+        bulk_g2s(gs.ops[1], reinterpret_cast<const unsigned char*>(pv.ulog) + eo * vb, upart, &gs.rec_bar);
     } else if (p == 1) {
-        const uint32_t kpart = static_cast<uint32_t>(nl) * kD * key_bytes(pv);
+        const uint32_t kpart = static_cast<uint32_t>(nl) * kD * kb;
         mbar_arrive_expect_tx(&gs.rec_bar, kpart);
-        bulk_g2s(gs.ops[3], reinterpret_cast<const unsigned char*>(pv.klog) + eo * key_bytes(pv), kpart, &gs.rec_bar);
+        bulk_g2s(gs.ops[3], reinterpret_cast<const unsigned char*>(pv.klog) + eo * kb, kpart, &gs.rec_bar);
     } else if (p == 2) {
         if constexpr (PER_KEY) {
             const uint32_t part = static_cast<uint32_t>(nl) * kVecBytes;
@@ -286,11 +291,12 @@ __device__ __forceinline__ float warp_abs_sum32_scatter(float (&v)[32], int lane
     return v[0];
 }
 
-// A key factor as a log record stores it: bfloat16 (k16), binary16 (rec16)
+// A key factor as a log record of format REC stores it: bfloat16, binary16
 // or FP32, widened back to FP32.
-__device__ __forceinline__ float stored_key(float k, const PoolView& pv) {
-    if (pv.k16) return __bfloat162float(__float2bfloat16_rn(k));
-    if (pv.rec16) return __half2float(__float2half_rn(k));
+template <int REC>
+__device__ __forceinline__ float stored_key(float k) {
+    if constexpr (REC == kRecBF16K) return __bfloat162float(__float2bfloat16_rn(k));
+    if constexpr (REC == kRecFP16) return __half2float(__float2half_rn(k));
     return k;
 }
 
@@ -319,7 +325,7 @@ __device__ __forceinline__ void add_token_rows(const GroupSmem& gs, int qr, floa
 // operands the four warps stage that state's first records, and after pass 2
 // (the codes and the header are consumed) its codes and header, so the copies
 // overlap this state's epilogue.  Returns false after a timeout (flagged).
-template <bool PER_KEY, bool COLS>
+template <bool PER_KEY, bool COLS, int REC>
 __device__ __forceinline__ bool fold_state(const StepArgs& a, size_t hd, int row, float lb_scalar,
                                            float lam_scalar, float beta, GroupSmem& gs, GroupPipe& gp,
                                            uint32_t tmem, uint32_t tlane, int bar_id, int gt, int lane, int gw,
@@ -354,7 +360,7 @@ __device__ __forceinline__ bool fold_state(const StepArgs& a, size_t hd, int row
     gs.es[gt] = expf(lp) * gs.hs[gt];
     // the key of the state update is the one a record would store (bfloat16
     // keys, binary16 records); the token's own output uses k itself
-    gs.kk[gt] = stored_key(gs.hk[gt], pv);
+    gs.kk[gt] = stored_key<REC>(gs.hk[gt]);
     const float vj = gs.hv[gt];
     const float bj = COLS ? gs.hb[gt] : 1.0f;  // the old scale of this thread's value column
     {
@@ -376,12 +382,15 @@ __device__ __forceinline__ bool fold_state(const StepArgs& a, size_t hd, int row
             u[l] = 0.0f;
             x[l] = 0.0f;
             if (l < nl) {
-                u[l] = pv.rec16 ? __half2float(reinterpret_cast<const __half*>(gs.ops[1])[l * kD + gt])
-                                : ru[l * kD + gt];
-                x[l] = (pv.k16 || pv.rec16)
-                           ? key16_to_float(reinterpret_cast<const unsigned short*>(gs.ops[3])[l * kD + gt],
-                                            pv.k16 != 0)
-                           : reinterpret_cast<const float*>(gs.ops[3])[l * kD + gt];
+                if constexpr (REC == kRecFP16)
+                    u[l] = __half2float(reinterpret_cast<const __half*>(gs.ops[1])[l * kD + gt]);
+                else
+                    u[l] = ru[l * kD + gt];
+                if constexpr (REC == kRecFP32)
+                    x[l] = reinterpret_cast<const float*>(gs.ops[3])[l * kD + gt];
+                else
+                    x[l] = key16_to_float(reinterpret_cast<const unsigned short*>(gs.ops[3])[l * kD + gt],
+                                          REC == kRecBF16K);
                 if constexpr (PER_KEY) x[l] *= expf(lp - rl[l * kD + gt]);
             }
         }
@@ -417,11 +426,11 @@ __device__ __forceinline__ bool fold_state(const StepArgs& a, size_t hd, int row
         // first, a part per warp
         if (lane == 0) {
             if (c0 + kChunkRecords < n) {
-                stage_records_part<PER_KEY>(pv, hd, c0 + kChunkRecords, min(kChunkRecords, n - c0 - kChunkRecords),
+                stage_records_part<PER_KEY, REC>(pv, hd, c0 + kChunkRecords, min(kChunkRecords, n - c0 - kChunkRecords),
                                             gs, gw);
                 gp.rec_out = true;
             } else if (gs.next_hd >= 0) {
-                stage_records_part<PER_KEY>(pv, static_cast<size_t>(gs.next_hd), 0, min(kChunkRecords, n), gs, gw);
+                stage_records_part<PER_KEY, REC>(pv, static_cast<size_t>(gs.next_hd), 0, min(kChunkRecords, n), gs, gw);
                 gp.rec_out = true;
             }
         }
@@ -459,7 +468,7 @@ __device__ __forceinline__ bool fold_state(const StepArgs& a, size_t hd, int row
     const float r = r2.x + r2.y, y0 = y2.x + y2.y;
     const float u_out = beta * (vj - r);
     a.y[static_cast<size_t>(row) * kD + gt] = fmaf(kq, u_out, y0);
-    const float uj = pv.rec16 ? __half2float(__float2half_rn(u_out)) : u_out;  // as a record stores it
+    const float uj = REC == kRecFP16 ? __half2float(__float2half_rn(u_out)) : u_out;  // as a record stores it
     // pass 2: S + k u^T back to tensor memory; per key row over this warp's
     // columns, the absmax (per-row scales) or the sum of |S| (column scales)
 #pragma unroll
@@ -564,7 +573,7 @@ __device__ __forceinline__ bool fold_state(const StepArgs& a, size_t hd, int row
     return true;
 }
 
-template <bool PER_KEY, bool COLS>
+template <bool PER_KEY, bool COLS, int REC>
 __global__ void __launch_bounds__(kFoldThreads, 1) window_fold_kernel(const StepArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ uint32_t tmem_base;
@@ -614,7 +623,7 @@ __global__ void __launch_bounds__(kFoldThreads, 1) window_fold_kernel(const Step
         stage_state_part<PER_KEY, COLS>(a, static_cast<size_t>(gs.next_hd), gs.next_row, gs, gw);
         gp.st_out = true;
         if (n > 0) {
-            stage_records_part<PER_KEY>(pv, static_cast<size_t>(gs.next_hd), 0, min(kChunkRecords, n), gs, gw);
+            stage_records_part<PER_KEY, REC>(pv, static_cast<size_t>(gs.next_hd), 0, min(kChunkRecords, n), gs, gw);
             gp.rec_out = true;
         }
     }
@@ -626,7 +635,7 @@ __global__ void __launch_bounds__(kFoldThreads, 1) window_fold_kernel(const Step
         const size_t hd = static_cast<size_t>(gs.next_hd);
         const int row = gs.next_row;
         const float lb = gs.next_lb, lam = gs.next_lam, beta = gs.next_beta;
-        if (!fold_state<PER_KEY, COLS>(a, hd, row, lb, lam, beta, gs, gp, tmem, tlane, bar_id, gt, lane, gw,
+        if (!fold_state<PER_KEY, COLS, REC>(a, hd, row, lb, lam, beta, gs, gp, tmem, tlane, bar_id, gt, lane, gw,
                                        count, item, stride, ahead)) {
             // after a timeout: let this group's copies and MMAs land before exit
             if (gt == 0) {
@@ -650,16 +659,32 @@ __global__ void __launch_bounds__(kFoldThreads, 1) window_fold_kernel(const Step
     }
 }
 
+template <bool PER_KEY, bool COLS>
+cudaError_t prepare_format(int bytes) {
+    const cudaFuncAttribute attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(window_fold_kernel<PER_KEY, COLS, kRecFP32>, attr, bytes)) != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(window_fold_kernel<PER_KEY, COLS, kRecBF16K>, attr, bytes)) != cudaSuccess)
+        return e;
+    return cudaFuncSetAttribute(window_fold_kernel<PER_KEY, COLS, kRecFP16>, attr, bytes);
+}
+
+template <bool PER_KEY, bool COLS>
+cudaError_t launch_format(const cudaLaunchConfig_t& cfg, const StepArgs& a) {
+    if (a.pv.k16) return cudaLaunchKernelEx(&cfg, window_fold_kernel<PER_KEY, COLS, kRecBF16K>, a);
+    if (a.pv.rec16) return cudaLaunchKernelEx(&cfg, window_fold_kernel<PER_KEY, COLS, kRecFP16>, a);
+    return cudaLaunchKernelEx(&cfg, window_fold_kernel<PER_KEY, COLS, kRecFP32>, a);
+}
+
 }  // namespace
 
 cudaError_t prepare_window_fold_kernels() {
     const int bytes = static_cast<int>(window_fold_smem_bytes());
-    const cudaFuncAttribute attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(window_fold_kernel<false, false>, attr, bytes)) != cudaSuccess) return e;
-    if ((e = cudaFuncSetAttribute(window_fold_kernel<true, false>, attr, bytes)) != cudaSuccess) return e;
-    if ((e = cudaFuncSetAttribute(window_fold_kernel<false, true>, attr, bytes)) != cudaSuccess) return e;
-    return cudaFuncSetAttribute(window_fold_kernel<true, true>, attr, bytes);
+    if ((e = prepare_format<false, false>(bytes)) != cudaSuccess) return e;
+    if ((e = prepare_format<true, false>(bytes)) != cudaSuccess) return e;
+    if ((e = prepare_format<false, true>(bytes)) != cudaSuccess) return e;
+    return prepare_format<true, true>(bytes);
 }
 
 cudaError_t launch_window_fold(const StepArgs& a, bool per_key, cudaStream_t s) {
@@ -673,11 +698,8 @@ cudaError_t launch_window_fold(const StepArgs& a, bool per_key, cudaStream_t s) 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (a.pv.colf != nullptr)
-        return per_key ? cudaLaunchKernelEx(&cfg, window_fold_kernel<true, true>, a)
-                       : cudaLaunchKernelEx(&cfg, window_fold_kernel<false, true>, a);
-    return per_key ? cudaLaunchKernelEx(&cfg, window_fold_kernel<true, false>, a)
-                   : cudaLaunchKernelEx(&cfg, window_fold_kernel<false, false>, a);
+    if (a.pv.colf != nullptr) return per_key ? launch_format<true, true>(cfg, a) : launch_format<false, true>(cfg, a);
+    return per_key ? launch_format<true, false>(cfg, a) : launch_format<false, false>(cfg, a);
 }
 
 }  // namespace ls
