@@ -53,6 +53,10 @@ def parse():
     ap.add_argument("--pools", type=int, default=None, help="override the pool count (profiling runs)")
     ap.add_argument("--window", type=int, default=None,
                     help="override the window / merge interval of the log variants (profiling runs)")
+    ap.add_argument("--col-scales", action="store_true",
+                    help="INT8 pools in the smoothed per-value-column format (profiling runs)")
+    ap.add_argument("--compensators", type=int, default=0,
+                    help="Compensator Tokens per INT8 state (profiling runs)")
     return ap.parse_args()
 
 
@@ -225,7 +229,8 @@ def run_native(args, rank, world, local):
     slot_idx = wl.slot_index(w, dev)
     masks = wl.static_masks(w, dev)
 
-    pools = {n: make_pools(w, n, W, dev) for n, W in variants}
+    fmt = {"col_scales": args.col_scales, "compensators": args.compensators}
+    pools = {n: make_pools(w, n, W, dev, **(fmt if n == "int8" else {})) for n, W in variants}
     if "eager" not in pools:
         pools["eager"] = make_pools(w, "eager", 0, dev)
     prewarm(w, pools, slot_idx, masks, dev)
@@ -291,22 +296,24 @@ def run_native(args, rank, world, local):
         torch.cuda.synchronize()
         ms = a_ev.elapsed_time(b_ev)
         hs = heads * w.pools * per_tokens
-        bytes_ = bm.variant_bytes(n, w.gate, W) * hs
+        per_hs = (bm.int8_bytes(w.gate, W, col_scales=args.col_scales, compensators=args.compensators)
+                  if n == "int8" else bm.variant_bytes(n, w.gate, W))
+        bytes_ = per_hs * hs
         gbs = bytes_ / (ms * 1e-3) / 1e9
         per_variant[n] = {"window": W or None, "tokens": per_tokens,
                           "ms_per_token_all_pools": ms / per_tokens,
                           "head_steps_per_s": hs / (ms * 1e-3),
-                          "algorithmic_bytes_per_head_step": bm.variant_bytes(n, w.gate, W),
+                          "algorithmic_bytes_per_head_step": per_hs,
                           "achieved_gbs": gbs, "frac_of_" + peak_kind + "_hbm": gbs / hbm_peak}
     value = job_throughput(heads * w.pools * len(variants) * args.steps, world, elapsed_ms)
     # windows that close inside the headline's timed region: the pools start
     # at a boundary, so token t closes a window when (t + 1) % W == 0
     window_ends = {n: sum(1 for t in range(args.warmup, args.warmup + args.steps) if (t + 1) % W == 0)
                    for n, W in variants if W}
-    # kernel launches per decode call: one step kernel; an INT8 pool with
-    # per-row scales also launches the tensor-core window-end fold after it
+    # kernel launches per decode call: one step kernel; an INT8 pool without
+    # compensator pairs also launches the tensor-core window-end fold after it
     # (every token; it returns at once unless a window closed)
-    launches_per_step = w.pools * sum(2 if n == "int8" else 1 for n, _ in variants)
+    launches_per_step = w.pools * sum(2 if (n == "int8" and not args.compensators) else 1 for n, _ in variants)
 
     out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
@@ -314,7 +321,10 @@ def run_native(args, rank, world, local):
            "data": "synthetic",
            "config": {"workload": w.name, "gate": "scalar (Gated DeltaNet)", "batch": w.batch,
                       "heads": w.heads, "d_k": w.d_k, "d_v": w.d_v, "pools": w.pools,
-                      "variants": [f"{n}" + (f" window={W}" if W else "") for n, W in variants],
+                      "variants": [f"{n}" + (f" window={W}" if W else "") +
+                                   (" smoothed per-value-column" if n == "int8" and args.col_scales else "") +
+                                   (f" + {args.compensators} compensator tokens"
+                                    if n == "int8" and args.compensators else "") for n, W in variants],
                       "prewarm_tokens": w.prewarm_tokens, "distinct_token_inputs": ring,
                       "l2": "inputs larger than L2: every pool's state is 0.2-0.8 GB and the "
                             "step streams 4 pools x 3 variants (about 5 GB) per token",
