@@ -55,3 +55,18 @@ def test_reference_arm_json_line():
 
 def test_reference_arm_other_ranks_print_nothing():
     assert _reference_line({"RANK": "1", "WORLD_SIZE": "2"}).strip() == ""
+
+
+def test_profiling_options_parse(monkeypatch):
+    """The options the profiles' commands use: defaults leave the bench's own
+    workload (W = 16 log variants, per-key-row INT8 without pairs)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setattr(sys, "argv", ["bench.py"])
+    a = bench.parse()
+    assert a.window is None and not a.col_scales and a.compensators == 0 and a.only is None
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--only", "int8", "--window", "8", "--col-scales",
+                                      "--compensators", "4", "--pools", "1", "--ring", "2", "--no-extras"])
+    a = bench.parse()
+    assert (a.only, a.window, a.col_scales, a.compensators, a.pools, a.ring, a.no_extras) == \
+        ("int8", 8, True, 4, 1, 2, True)
