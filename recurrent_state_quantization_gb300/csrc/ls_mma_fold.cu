@@ -395,12 +395,16 @@ __device__ __forceinline__ bool fold_state(const StepArgs& a, size_t hd, int row
             }
         }
         named_barrier(bar_id, kGroupThreads);  // every row is in registers: the buffers are free
+        // the MMAs read the records of (nl + 7) / 8 k-steps of 8: only those are split and stored
+        const bool half = nl <= kChunkRecords / 2;
         if constexpr (!PER_KEY) {
 #pragma unroll
-            for (int l = 0; l < kChunkRecords; ++l) x[l] *= gs.gl[l];
+            for (int l = 0; l < kChunkRecords; ++l)
+                if (!half || l < kChunkRecords / 2) x[l] *= gs.gl[l];
         }
 #pragma unroll
         for (int qq = 0; qq < kChunkRecords / 4; ++qq) {
+            if (half && qq >= kChunkRecords / 8) break;
             const uint32_t off = operand_offset(gt, qq);
             float4 h = make_float4(tf32_rna(u[4 * qq]), tf32_rna(u[4 * qq + 1]), tf32_rna(u[4 * qq + 2]),
                                    tf32_rna(u[4 * qq + 3]));
